@@ -1,0 +1,229 @@
+"""gated_delta_ssm_gb300 -- Python binding of libgdn, the gated-delta SSM layer step on GB300.
+
+Argument marshalling only: every entry point forwards device pointers, sizes
+and the current CUDA stream to the function of the same name in libgdn.so
+(declared in include/gdn.h) and raises on a non-OK status. There is no
+fallback: if the compiled library is missing or fails to load, every call
+raises.
+
+Tensors are torch CUDA tensors (PyTorch supplies device memory and streams);
+activations may be float32 or bfloat16, everything else is float32.
+"""
+from __future__ import annotations
+
+import ctypes as _ct
+import dataclasses as _dc
+import os as _os
+import threading as _th
+
+__all__ = [
+    "Dims", "Params", "GdnError", "load", "library_path",
+    "decay_gate", "conv_update", "recurrence_decode", "gated_norm",
+    "decode_step", "verify_k2", "verify_commit", "prefill_chunked", "version",
+]
+
+_PKG = _os.path.dirname(_os.path.abspath(__file__))
+_LIB_PATH = _os.path.join(_PKG, "libgdn.so")
+_lib = None
+_lock = _th.Lock()
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
+GDN_F32, GDN_BF16 = 0, 1
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, fn: str, detail: str = ""):
+        self.status = status
+        names = {1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_CUDA"}
+        super().__init__(f"{fn}: {names.get(status, status)}" + (f" ({detail})" if detail else ""))
+
+
+class _CDims(_ct.Structure):
+    _fields_ = [("n_seq", _ct.c_int32), ("n_qk_heads", _ct.c_int32), ("n_v_heads", _ct.c_int32),
+                ("head_dim", _ct.c_int32), ("d_conv", _ct.c_int32), ("reserved", _ct.c_int32),
+                ("x_stride", _ct.c_int64), ("z_stride", _ct.c_int64), ("gate_stride", _ct.c_int64)]
+
+
+class _CParams(_ct.Structure):
+    _fields_ = [("conv_w", _ct.c_void_p), ("dt", _ct.c_void_p), ("A_log", _ct.c_void_p),
+                ("norm_w", _ct.c_void_p), ("l2_eps", _ct.c_float), ("rms_eps", _ct.c_float)]
+
+
+@_dc.dataclass
+class Dims:
+    """Shape of a layer call (see gdn_dims in include/gdn.h). Strides are in elements."""
+    n_seq: int
+    n_qk_heads: int
+    n_v_heads: int
+    head_dim: int = 128
+    d_conv: int = 4
+    x_stride: int = 0       # 0 -> conv_dim
+    z_stride: int = 0       # 0 -> n_v_heads * head_dim
+    gate_stride: int = 0    # 0 -> n_v_heads
+
+    @property
+    def conv_dim(self) -> int:
+        return (2 * self.n_qk_heads + self.n_v_heads) * self.head_dim
+
+    def c(self) -> _CDims:
+        return _CDims(self.n_seq, self.n_qk_heads, self.n_v_heads, self.head_dim, self.d_conv, 0,
+                      self.x_stride or self.conv_dim, self.z_stride or self.n_v_heads * self.head_dim,
+                      self.gate_stride or self.n_v_heads)
+
+
+@_dc.dataclass
+class Params:
+    """Per-layer float32 parameters (device tensors)."""
+    conv_w: object
+    dt: object
+    A_log: object
+    norm_w: object
+    l2_eps: float = 1e-6
+    rms_eps: float = 1e-6
+
+    def c(self) -> _CParams:
+        return _CParams(_ptr(self.conv_w), _ptr(self.dt), _ptr(self.A_log), _ptr(self.norm_w),
+                        self.l2_eps, self.rms_eps)
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libgdn.so (built by __graft_entry__.build() or gated_delta_ssm_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not _os.path.exists(_LIB_PATH):
+            raise ImportError(f"libgdn.so is not built ({_LIB_PATH}); run "
+                              "`python -m gated_delta_ssm_gb300.build`")
+        L = _ct.CDLL(_LIB_PATH)
+        vp, i32, i64, f32 = _ct.c_void_p, _ct.c_int32, _ct.c_int64, _ct.c_float
+        pd, pp = _ct.POINTER(_CDims), _ct.POINTER(_CParams)
+        sigs = {
+            "gdn_decay_gate": [vp, _ct.c_int, i64, vp, vp, vp, i32, i32, vp],
+            "gdn_conv_update": [vp, vp, _ct.c_int, vp, vp, pd, i32, f32, vp],
+            "gdn_recurrence_decode": [vp, vp, vp, vp, i64, vp, vp, vp, pd, f32, vp],
+            "gdn_gated_norm": [vp, vp, vp, _ct.c_int, i64, vp, i32, i32, i32, f32, vp],
+            "gdn_decode_step": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, vp],
+            "gdn_verify_k2": [vp, vp, vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, vp],
+            "gdn_verify_commit": [vp, vp, vp, vp, vp, pd, vp],
+            "gdn_prefill_chunked": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, i32, i32, vp],
+        }
+        for name, args in sigs.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = _ct.c_int
+        for name in ("gdn_last_cuda_error", "gdn_version"):
+            getattr(L, name).restype = _ct.c_char_p
+            getattr(L, name).argtypes = []
+        L.gdn_status_string.restype = _ct.c_char_p
+        L.gdn_status_string.argtypes = [_ct.c_int]
+        _lib = L
+    return _lib
+
+
+def version() -> str:
+    return load().gdn_version().decode()
+
+
+# ------------------------------------------------------------------ marshalling helpers
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _dtype(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise TypeError(f"activation dtype must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, fn: str):
+    if status != GDN_OK:
+        detail = load().gdn_last_cuda_error().decode() if status == GDN_ERR_CUDA else ""
+        raise GdnError(status, fn, detail)
+
+
+# ------------------------------------------------------------------ entry points
+def decay_gate(alpha, dt, A_log, g, rows: int, n_heads: int, alpha_stride: int = 0, stream=None):
+    _check(load().gdn_decay_gate(_ptr(alpha), _dtype(alpha), alpha_stride or n_heads, _ptr(dt),
+                                 _ptr(A_log), _ptr(g), rows, n_heads, _stream(stream)),
+           "gdn_decay_gate")
+
+
+def conv_update(conv_state, x, conv_w, out, dims: Dims, n_tokens: int = 1, l2_eps: float = 1e-6,
+                stream=None):
+    cd = dims.c()
+    _check(load().gdn_conv_update(_ptr(conv_state), _ptr(x), _dtype(x), _ptr(conv_w), _ptr(out),
+                                  _ct.byref(cd), n_tokens, l2_eps, _stream(stream)),
+           "gdn_conv_update")
+
+
+def recurrence_decode(state, q, k, v, qkv_stride: int, g, beta, y, dims: Dims, scale: float,
+                      stream=None):
+    cd = dims.c()
+    _check(load().gdn_recurrence_decode(_ptr(state), _ptr(q), _ptr(k), _ptr(v), qkv_stride,
+                                        _ptr(g), _ptr(beta), _ptr(y), _ct.byref(cd), scale,
+                                        _stream(stream)),
+           "gdn_recurrence_decode")
+
+
+def gated_norm(y, norm_w, z, out, rows: int, n_v_heads: int, head_dim: int = 128,
+               z_stride: int = 0, eps: float = 1e-6, stream=None):
+    _check(load().gdn_gated_norm(_ptr(y), _ptr(norm_w), _ptr(z), _dtype(z),
+                                 z_stride or n_v_heads * head_dim, _ptr(out), rows, n_v_heads,
+                                 head_dim, eps, _stream(stream)),
+           "gdn_gated_norm")
+
+
+def decode_step(state, conv_state, x, z, alpha, beta_logit, params: Params, out, dims: Dims,
+                stream=None):
+    cd, cp = dims.c(), params.c()
+    _check(load().gdn_decode_step(_ptr(state), _ptr(conv_state), _ptr(x), _ptr(z), _ptr(alpha),
+                                  _ptr(beta_logit), _dtype(x), _ct.byref(cp), _ptr(out),
+                                  _ct.byref(cd), _stream(stream)),
+           "gdn_decode_step")
+
+
+def verify_k2(state, conv_state, state_snap, conv_snap, x, z, alpha, beta_logit, params: Params,
+              out, dims: Dims, stream=None):
+    cd, cp = dims.c(), params.c()
+    _check(load().gdn_verify_k2(_ptr(state), _ptr(conv_state), _ptr(state_snap), _ptr(conv_snap),
+                                _ptr(x), _ptr(z), _ptr(alpha), _ptr(beta_logit), _dtype(x),
+                                _ct.byref(cp), _ptr(out), _ct.byref(cd), _stream(stream)),
+           "gdn_verify_k2")
+
+
+def verify_commit(state, conv_state, state_snap, conv_snap, n_accept, dims: Dims, stream=None):
+    cd = dims.c()
+    _check(load().gdn_verify_commit(_ptr(state), _ptr(conv_state), _ptr(state_snap),
+                                    _ptr(conv_snap), _ptr(n_accept), _ct.byref(cd),
+                                    _stream(stream)),
+           "gdn_verify_commit")
+
+
+def prefill_chunked(state, conv_state, x, z, alpha, beta_logit, params: Params, out, dims: Dims,
+                    n_tokens: int, chunk: int = 64, stream=None):
+    cd, cp = dims.c(), params.c()
+    _check(load().gdn_prefill_chunked(_ptr(state), _ptr(conv_state), _ptr(x), _ptr(z), _ptr(alpha),
+                                      _ptr(beta_logit), _dtype(x), _ct.byref(cp), _ptr(out),
+                                      _ct.byref(cd), n_tokens, chunk, _stream(stream)),
+           "gdn_prefill_chunked")

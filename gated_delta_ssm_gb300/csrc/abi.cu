@@ -1,0 +1,303 @@
+// abi.cu -- the extern "C" entry points of libgdn (declared in include/gdn.h):
+// host-side argument validation, then one launch on the caller's stream.
+// Nothing here allocates, synchronises or keeps state between calls (the
+// last-error text is thread-local).
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/gdn.h"
+#include "gdn_device.cuh"
+#include "gdn_kernels.h"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+gdn_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return GDN_OK;
+    snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", cudaGetErrorName(e),
+             cudaGetErrorString(e));
+    return GDN_ERR_CUDA;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t act_size(gdn_dtype t) { return t == GDN_BF16 ? 2 : 4; }
+
+bool valid_dtype(gdn_dtype t) { return t == GDN_F32 || t == GDN_BF16; }
+
+cudaStream_t as_cuda(gdn_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Shape checks shared by every entry point that takes gdn_dims.
+// need: bit 0 = x_stride used, bit 1 = z_stride used, bit 2 = gate_stride used.
+gdn_status check_dims(const gdn_dims *d, int need)
+{
+    if (!d)
+        return GDN_ERR_INVALID_ARG;
+    if (d->n_seq < 1 || d->n_seq > 65535 || d->n_qk_heads < 1 || d->n_v_heads < 1 ||
+        d->head_dim < 1 || d->d_conv < 1 || d->reserved != 0)
+        return GDN_ERR_INVALID_ARG;
+    if (d->n_v_heads % d->n_qk_heads != 0)
+        return GDN_ERR_INVALID_ARG;
+    const int64_t conv_dim = (int64_t)(2 * (int64_t)d->n_qk_heads + d->n_v_heads) * d->head_dim;
+    if (conv_dim > (1 << 24))
+        return GDN_ERR_INVALID_ARG;
+    if ((need & 1) && d->x_stride < conv_dim)
+        return GDN_ERR_INVALID_ARG;
+    if ((need & 2) && d->z_stride < (int64_t)d->n_v_heads * d->head_dim)
+        return GDN_ERR_INVALID_ARG;
+    if ((need & 4) && d->gate_stride < d->n_v_heads)
+        return GDN_ERR_INVALID_ARG;
+    if (d->head_dim != gdn::kD)
+        return GDN_ERR_UNSUPPORTED;
+    if (d->d_conv < 2 || d->d_conv > gdn::kMaxW)
+        return GDN_ERR_UNSUPPORTED;
+    if (d->n_v_heads / d->n_qk_heads > 8)
+        return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+gdn_status check_params(const gdn_params *p)
+{
+    if (!p || !p->conv_w || !p->dt || !p->A_log || !p->norm_w)
+        return GDN_ERR_INVALID_ARG;
+    if (!(p->l2_eps >= 0.0f) || !(p->rms_eps >= 0.0f))
+        return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+int conv_dim_of(const gdn_dims *d) { return (2 * d->n_qk_heads + d->n_v_heads) * d->head_dim; }
+
+gdn_status fused_common(float *state, float *conv_state, float *state_snap, float *conv_snap,
+                        const void *x, const void *z, const void *alpha, const void *beta_logit,
+                        gdn_dtype act_dtype, const gdn_params *params, float *out,
+                        const gdn_dims *dims, int ntok, gdn_stream_t stream)
+{
+    gdn_status st = check_dims(dims, 7);
+    if (st != GDN_OK)
+        return st;
+    if ((st = check_params(params)) != GDN_OK)
+        return st;
+    if (!valid_dtype(act_dtype))
+        return GDN_ERR_INVALID_ARG;
+    if (!state || !conv_state || !x || !z || !alpha || !beta_logit || !out)
+        return GDN_ERR_INVALID_ARG;
+    if (ntok == 2 && (!state_snap || !conv_snap))
+        return GDN_ERR_INVALID_ARG;
+    const size_t es = act_size(act_dtype);
+    if (!aligned(state, 16) || (state_snap && !aligned(state_snap, 16)) || !aligned(x, es) ||
+        !aligned(z, es) || !aligned(alpha, es) || !aligned(beta_logit, es) || !aligned(out, 4) ||
+        !aligned(conv_state, 4) || (conv_snap && !aligned(conv_snap, 4)))
+        return GDN_ERR_INVALID_ARG;
+    gdn::FusedArgs a;
+    a.state = state;
+    a.conv_state = conv_state;
+    a.state_snap = state_snap;
+    a.conv_snap = conv_snap;
+    a.x = x;
+    a.z = z;
+    a.alpha = alpha;
+    a.beta_logit = beta_logit;
+    a.conv_w = params->conv_w;
+    a.dt = params->dt;
+    a.A_log = params->A_log;
+    a.norm_w = params->norm_w;
+    a.out = out;
+    a.x_stride = dims->x_stride;
+    a.z_stride = dims->z_stride;
+    a.gate_stride = dims->gate_stride;
+    a.B = dims->n_seq;
+    a.Hq = dims->n_qk_heads;
+    a.Hv = dims->n_v_heads;
+    a.W = dims->d_conv;
+    a.conv_dim = conv_dim_of(dims);
+    a.l2_eps = params->l2_eps;
+    a.rms_eps = params->rms_eps;
+    a.scale = 1.0f / sqrtf((float)dims->head_dim);
+    return from_cuda(gdn::launch_decode_fused(a, act_dtype == GDN_BF16, ntok, as_cuda(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_decay_gate(const void *alpha, gdn_dtype alpha_dtype, int64_t alpha_stride,
+                          const float *dt, const float *A_log, float *g, int32_t rows,
+                          int32_t n_heads, gdn_stream_t stream)
+{
+    if (!alpha || !dt || !A_log || !g || rows < 1 || n_heads < 1 || alpha_stride < n_heads ||
+        !valid_dtype(alpha_dtype) || !aligned(alpha, act_size(alpha_dtype)))
+        return GDN_ERR_INVALID_ARG;
+    return from_cuda(gdn::launch_decay_gate(alpha, alpha_dtype == GDN_BF16, alpha_stride, dt,
+                                            A_log, g, rows, n_heads, as_cuda(stream)));
+}
+
+gdn_status gdn_conv_update(float *conv_state, const void *x, gdn_dtype x_dtype,
+                           const float *conv_w, float *out, const gdn_dims *dims,
+                           int32_t n_tokens, float l2_eps, gdn_stream_t stream)
+{
+    gdn_status st = check_dims(dims, 1);
+    if (st != GDN_OK)
+        return st;
+    if (!conv_state || !x || !conv_w || !out || n_tokens < 1 || !valid_dtype(x_dtype) ||
+        !(l2_eps >= 0.0f) || !aligned(x, act_size(x_dtype)))
+        return GDN_ERR_INVALID_ARG;
+    gdn::ConvArgs a;
+    a.conv_state = conv_state;
+    a.x = x;
+    a.conv_w = conv_w;
+    a.out = out;
+    a.x_stride = dims->x_stride;
+    a.B = dims->n_seq;
+    a.Hq = dims->n_qk_heads;
+    a.Hv = dims->n_v_heads;
+    a.W = dims->d_conv;
+    a.conv_dim = conv_dim_of(dims);
+    a.T = n_tokens;
+    a.l2_eps = l2_eps;
+    return from_cuda(gdn::launch_conv_update(a, x_dtype == GDN_BF16, as_cuda(stream)));
+}
+
+gdn_status gdn_recurrence_decode(float *state, const float *q, const float *k, const float *v,
+                                 int64_t qkv_stride, const float *g, const float *beta, float *y,
+                                 const gdn_dims *dims, float scale, gdn_stream_t stream)
+{
+    gdn_status st = check_dims(dims, 0);
+    if (st != GDN_OK)
+        return st;
+    if (!state || !q || !k || !v || !g || !beta || !y || !aligned(state, 16))
+        return GDN_ERR_INVALID_ARG;
+    if (dims->n_seq > 1 && qkv_stride < (int64_t)dims->n_v_heads * dims->head_dim)
+        return GDN_ERR_INVALID_ARG;
+    gdn::RecArgs a;
+    a.state = state;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.qkv_stride = qkv_stride;
+    a.g = g;
+    a.beta = beta;
+    a.y = y;
+    a.B = dims->n_seq;
+    a.Hq = dims->n_qk_heads;
+    a.Hv = dims->n_v_heads;
+    a.scale = scale;
+    return from_cuda(gdn::launch_recurrence_decode(a, as_cuda(stream)));
+}
+
+gdn_status gdn_gated_norm(const float *y, const float *norm_w, const void *z, gdn_dtype z_dtype,
+                          int64_t z_stride, float *out, int32_t rows, int32_t n_v_heads,
+                          int32_t head_dim, float eps, gdn_stream_t stream)
+{
+    if (!y || !norm_w || !z || !out || rows < 1 || n_v_heads < 1 || head_dim < 1 ||
+        !valid_dtype(z_dtype) || z_stride < (int64_t)n_v_heads * head_dim || !(eps >= 0.0f) ||
+        !aligned(z, act_size(z_dtype)))
+        return GDN_ERR_INVALID_ARG;
+    if (head_dim != gdn::kD)
+        return GDN_ERR_UNSUPPORTED;
+    return from_cuda(gdn::launch_gated_norm(y, norm_w, z, z_dtype == GDN_BF16, z_stride, out, rows,
+                                            n_v_heads, eps, as_cuda(stream)));
+}
+
+gdn_status gdn_decode_step(float *state, float *conv_state, const void *x, const void *z,
+                           const void *alpha, const void *beta_logit, gdn_dtype act_dtype,
+                           const gdn_params *params, float *out, const gdn_dims *dims,
+                           gdn_stream_t stream)
+{
+    return fused_common(state, conv_state, nullptr, nullptr, x, z, alpha, beta_logit, act_dtype,
+                        params, out, dims, 1, stream);
+}
+
+gdn_status gdn_verify_k2(float *state, float *conv_state, float *state_snap, float *conv_snap,
+                         const void *x, const void *z, const void *alpha, const void *beta_logit,
+                         gdn_dtype act_dtype, const gdn_params *params, float *out,
+                         const gdn_dims *dims, gdn_stream_t stream)
+{
+    if (state_snap == state || conv_snap == conv_state)
+        return GDN_ERR_INVALID_ARG;
+    return fused_common(state, conv_state, state_snap, conv_snap, x, z, alpha, beta_logit,
+                        act_dtype, params, out, dims, 2, stream);
+}
+
+gdn_status gdn_verify_commit(float *state, float *conv_state, const float *state_snap,
+                             const float *conv_snap, const int32_t *n_accept,
+                             const gdn_dims *dims, gdn_stream_t stream)
+{
+    gdn_status st = check_dims(dims, 0);
+    if (st != GDN_OK)
+        return st;
+    if (!state || !conv_state || !state_snap || !conv_snap || !n_accept || !aligned(state, 16) ||
+        !aligned(state_snap, 16))
+        return GDN_ERR_INVALID_ARG;
+    const int64_t d = dims->head_dim;
+    return from_cuda(gdn::launch_verify_commit(state, conv_state, state_snap, conv_snap, n_accept,
+                                               dims->n_seq, (int64_t)dims->n_v_heads * d * d,
+                                               (int64_t)conv_dim_of(dims) * (dims->d_conv - 1),
+                                               as_cuda(stream)));
+}
+
+gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, const void *z,
+                               const void *alpha, const void *beta_logit, gdn_dtype act_dtype,
+                               const gdn_params *params, float *out, const gdn_dims *dims,
+                               int32_t n_tokens, int32_t chunk, gdn_stream_t stream)
+{
+    gdn_status st = check_dims(dims, 7);
+    if (st != GDN_OK)
+        return st;
+    if ((st = check_params(params)) != GDN_OK)
+        return st;
+    if (!valid_dtype(act_dtype) || n_tokens < 1)
+        return GDN_ERR_INVALID_ARG;
+    if (!state || !conv_state || !x || !z || !alpha || !beta_logit || !out)
+        return GDN_ERR_INVALID_ARG;
+    const size_t es = act_size(act_dtype);
+    if (!aligned(state, 16) || !aligned(x, es) || !aligned(z, es) || !aligned(alpha, es) ||
+        !aligned(beta_logit, es) || !aligned(out, 16))
+        return GDN_ERR_INVALID_ARG;
+    if (chunk != 64)
+        return GDN_ERR_UNSUPPORTED;
+    gdn::PrefillArgs a;
+    a.state = state;
+    a.conv_state = conv_state;
+    a.x = x;
+    a.z = z;
+    a.alpha = alpha;
+    a.beta_logit = beta_logit;
+    a.conv_w = params->conv_w;
+    a.dt = params->dt;
+    a.A_log = params->A_log;
+    a.norm_w = params->norm_w;
+    a.out = out;
+    a.x_stride = dims->x_stride;
+    a.z_stride = dims->z_stride;
+    a.gate_stride = dims->gate_stride;
+    a.B = dims->n_seq;
+    a.Hq = dims->n_qk_heads;
+    a.Hv = dims->n_v_heads;
+    a.W = dims->d_conv;
+    a.conv_dim = conv_dim_of(dims);
+    a.T = n_tokens;
+    a.l2_eps = params->l2_eps;
+    a.rms_eps = params->rms_eps;
+    a.scale = 1.0f / sqrtf((float)dims->head_dim);
+    return from_cuda(gdn::launch_prefill(a, act_dtype == GDN_BF16, as_cuda(stream)));
+}
+
+const char *gdn_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char *gdn_status_string(gdn_status s)
+{
+    switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    }
+    return "unknown gdn_status";
+}
+
+const char *gdn_version(void) { return "libgdn 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

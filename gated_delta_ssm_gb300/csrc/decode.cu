@@ -1,0 +1,393 @@
+// decode.cu -- decode-side kernels of libgdn: the fused one-launch layer step
+// (single token, and the K=2 verify form with its rollback snapshot), the
+// standalone gate / conv / recurrence / gated-norm kernels it is equal to bit
+// for bit, and the verify commit.
+//
+// Decode is bound by HBM bandwidth on the recurrent state (128x128 fp32 per
+// V head, read once and written once per step); everything else is small.
+// Work split: one CTA per (sequence, V head, 128/NSPLIT value rows), 8 warps,
+// each warp streaming 4*NG rows held in registers. The CTAs that share a QK
+// head (r V heads x NSPLIT row slices) form one thread-block cluster, which
+// orders every CTA's read of the shared Q/K conv history before its single
+// owner rewrites it, and carries the gated-norm partial sums between the row
+// slices of a head through distributed shared memory.
+#include <cooperative_groups.h>
+
+#include "gdn_device.cuh"
+#include "gdn_kernels.h"
+
+namespace cg = cooperative_groups;
+
+namespace gdn {
+
+// ------------------------------------------------------------------ decay gate
+template <typename TIn>
+__global__ void __launch_bounds__(256) decay_gate_kernel(const TIn *alpha, int64_t alpha_stride,
+                                                         const float *dt, const float *A_log,
+                                                         float *g, int rows, int H)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)rows * H)
+        return;
+    const int64_t r = i / H;
+    const int h = (int)(i % H);
+    g[i] = decay_gate_f(load_act<TIn>(alpha + r * alpha_stride + h), __ldg(dt + h), __ldg(A_log + h));
+}
+
+// ------------------------------------------------------------------ conv + L2
+// One CTA of 128 threads per (128-channel head, sequence); thread i owns
+// channel i of the head and scans the tokens of the call in order.
+template <typename TIn>
+__global__ void __launch_bounds__(kD) conv_update_kernel(ConvArgs a)
+{
+    __shared__ float red[2][4];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.y;
+    const int c = blockIdx.x * kD + tid;
+    const bool is_qk = blockIdx.x < 2 * a.Hq;
+    const int W = a.W;
+    float *hist_c = a.conv_state + ((size_t)b * a.conv_dim + c) * (W - 1);
+    const TIn *x_c = static_cast<const TIn *>(a.x) + (int64_t)b * a.T * a.x_stride + c;
+    const float *w_c = a.conv_w + (size_t)c * W;
+    float *out_c = a.out + (size_t)b * a.T * a.conv_dim + c;
+    for (int t = 0; t < a.T; ++t) {
+        float v = silu_f(conv_pre<TIn>(hist_c, x_c, a.x_stride, w_c, W, t));
+        if (is_qk)
+            v = __fmul_rn(v, head_l2_inv(v, a.l2_eps, red[t & 1], warp, lane));
+        out_c[(size_t)t * a.conv_dim] = v;
+    }
+    float nh[kMaxW - 1];
+    conv_history_after<TIn>(hist_c, x_c, a.x_stride, W, a.T, nh);
+    store_history(hist_c, W, nh);
+}
+
+// ------------------------------------------------------------------ recurrence
+template <int NSPLIT>
+__global__ void __launch_bounds__(256, 2) recurrence_decode_kernel(RecArgs a)
+{
+    constexpr int ROWS = kD / NSPLIT;
+    constexpr int RPW = ROWS / 8;
+    constexpr int NG = RPW / 4;
+    __shared__ __align__(16) float sq[kD];
+    __shared__ __align__(16) float sk[kD];
+    __shared__ float sv[ROWS], sy[ROWS];
+    __shared__ float sdecay[1], sbeta[1];
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int b = blockIdx.y;
+    const int h = blockIdx.x / NSPLIT, split = blockIdx.x % NSPLIT;
+    const int hk = h / (a.Hv / a.Hq);
+    const int row0 = split * ROWS;
+    if (tid < kD)
+        sq[tid] = __ldg(a.q + (int64_t)b * a.qkv_stride + hk * kD + tid);
+    else
+        sk[tid - kD] = __ldg(a.k + (int64_t)b * a.qkv_stride + hk * kD + (tid - kD));
+    if (tid < ROWS)
+        sv[tid] = __ldg(a.v + (int64_t)b * a.qkv_stride + h * kD + row0 + tid);
+    if (tid == 255) {
+        sdecay[0] = expf(__ldg(a.g + (size_t)b * a.Hv + h));
+        sbeta[0] = __ldg(a.beta + (size_t)b * a.Hv + h);
+    }
+    __syncthreads();
+    float *rows = a.state + (((size_t)b * a.Hv + h) * kD + row0 + warp * RPW) * kD;
+    recurrence_rows<NG, 1, false>(rows, nullptr, sk, sq, sv, ROWS, sdecay, sbeta, sy, warp * RPW,
+                                  a.scale);
+    __syncthreads();
+    if (tid < ROWS)
+        a.y[((size_t)b * a.Hv + h) * kD + row0 + tid] = sy[tid];
+}
+
+// ------------------------------------------------------------------ gated norm
+// One warp per (row, head); lane l holds elements l, 32+l, 64+l, 96+l.
+template <typename TZ>
+__global__ void __launch_bounds__(256) gated_norm_kernel(const float *y, const float *w,
+                                                         const TZ *z, int64_t z_stride,
+                                                         float *out, int rows, int Hv, float eps)
+{
+    const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= (int64_t)rows * Hv)
+        return;
+    const int64_t row = gw / Hv;
+    const int h = (int)(gw % Hv);
+    const float *yr = y + gw * kD;
+    float yv[4], bp[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+        yv[m] = yr[32 * m + lane];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+        bp[m] = norm_block_partial(yv[m]);
+    const float inv = norm_inv(bp[0], bp[1], bp[2], bp[3], eps);
+    const TZ *zr = z + row * z_stride + (int64_t)h * kD;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int j = 32 * m + lane;
+        out[gw * kD + j] = gated_out(yv[m], inv, __ldg(w + j), load_act<TZ>(zr + j));
+    }
+}
+
+// ------------------------------------------------------------------ fused step
+// NTOK = 1: one decode step. NTOK = 2: K=2 verify, snapshot after token 0.
+template <typename TIn, int NTOK, int NSPLIT>
+__global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
+{
+    constexpr int ROWS = kD / NSPLIT;   // value rows of one head in this CTA
+    constexpr int RPW = ROWS / 8;       // rows per warp
+    constexpr int NG = RPW / 4;         // 4-row groups per warp
+    constexpr int NBLK = ROWS / 32;     // 32-row norm blocks in this CTA
+    constexpr bool SNAP = NTOK == 2;
+    __shared__ __align__(16) float sq[NTOK * kD];
+    __shared__ __align__(16) float sk[NTOK * kD];
+    __shared__ float sv[NTOK * ROWS], sy[NTOK * ROWS];
+    __shared__ float sdecay[NTOK], sbeta[NTOK];
+    __shared__ float sred[NTOK][8];
+    __shared__ float spart[NTOK * NBLK];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.y;
+    const int h = blockIdx.x / NSPLIT, split = blockIdx.x % NSPLIT;
+    const int r = a.Hv / a.Hq;
+    const int hk = h / r;
+    const int csize = r * NSPLIT;                 // CTAs sharing QK head hk
+    const int crank = blockIdx.x % csize;          // rank in the cluster
+    const int W = a.W, cd = a.conv_dim;
+    const int row0 = split * ROWS;
+    const int64_t tok0 = (int64_t)b * NTOK;       // input row of token 0 of sequence b
+    const TIn *xb = static_cast<const TIn *>(a.x) + tok0 * a.x_stride;
+    float *histb = a.conv_state + (size_t)b * cd * (W - 1);
+
+    // ---- Q / K conv + SiLU + per-head L2 (threads 0..127: Q head, 128..255: K head)
+    const bool is_k = tid >= kD;
+    const int c_qk = (is_k ? a.Hq * kD : 0) + hk * kD + (tid & (kD - 1));
+    {
+        const float *hist_c = histb + (size_t)c_qk * (W - 1);
+        const float *w_c = a.conv_w + (size_t)c_qk * W;
+        float vals[NTOK];
+#pragma unroll
+        for (int p = 0; p < NTOK; ++p)
+            vals[p] = silu_f(conv_pre<TIn>(hist_c, xb + c_qk, a.x_stride, w_c, W, p));
+#pragma unroll
+        for (int p = 0; p < NTOK; ++p) {
+            const float inv = head_l2_inv(vals[p], a.l2_eps, &sred[p][is_k ? 4 : 0], warp & 3, lane);
+            (is_k ? sk : sq)[p * kD + (tid & (kD - 1))] = __fmul_rn(vals[p], inv);
+        }
+    }
+    // ---- V conv + SiLU for this CTA's rows (exclusively owned), gates
+    if (tid < ROWS) {
+        const int c = 2 * a.Hq * kD + h * kD + row0 + tid;
+        float *hist_c = histb + (size_t)c * (W - 1);
+        const float *w_c = a.conv_w + (size_t)c * W;
+#pragma unroll
+        for (int p = 0; p < NTOK; ++p)
+            sv[p * ROWS + tid] = silu_f(conv_pre<TIn>(hist_c, xb + c, a.x_stride, w_c, W, p));
+        float nh[kMaxW - 1];
+        if (SNAP) {
+            conv_history_after<TIn>(hist_c, xb + c, a.x_stride, W, 1, nh);
+            store_history(a.conv_snap + ((size_t)b * cd + c) * (W - 1), W, nh);
+        }
+        conv_history_after<TIn>(hist_c, xb + c, a.x_stride, W, NTOK, nh);
+        store_history(hist_c, W, nh);
+    } else if (tid < ROWS + NTOK) {
+        const int p = tid - ROWS;
+        const int64_t row = tok0 + p;
+        const float g = decay_gate_f(load_act<TIn>(static_cast<const TIn *>(a.alpha) + row * a.gate_stride + h),
+                                     __ldg(a.dt + h), __ldg(a.A_log + h));
+        sdecay[p] = expf(g);
+        sbeta[p] = sigmoid_f(load_act<TIn>(static_cast<const TIn *>(a.beta_logit) + row * a.gate_stride + h));
+    }
+    __syncthreads();
+
+    // ---- recurrence over this CTA's rows, state read once and written once
+    const size_t head_off = ((size_t)b * a.Hv + h) * kD * kD;
+    const size_t warp_off = (size_t)(row0 + warp * RPW) * kD;
+    recurrence_rows<NG, NTOK, SNAP>(a.state + head_off + warp_off,
+                                    SNAP ? a.state_snap + head_off + warp_off : nullptr, sk, sq,
+                                    sv, ROWS, sdecay, sbeta, sy, warp * RPW, a.scale);
+    __syncthreads();
+
+    // ---- gated RMSNorm: 32-row block partials, combined in block order
+    if (warp < NTOK * NBLK) {
+        const int p = warp / NBLK, bl = warp % NBLK;
+        const float s = norm_block_partial(sy[p * ROWS + bl * 32 + lane]);
+        if (lane == 0)
+            spart[p * NBLK + bl] = s;
+    }
+    // One cluster barrier serves two purposes: every CTA of the cluster has
+    // finished reading the shared Q/K history (read in the first phase), and
+    // every CTA's norm partials are visible to its peers.
+    cg::cluster_group cluster = cg::this_cluster();
+    if (csize > 1)
+        cluster.sync();
+    else
+        __syncthreads();
+
+    if (tid < ROWS) {
+#pragma unroll
+        for (int p = 0; p < NTOK; ++p) {
+            float bp[4];
+#pragma unroll
+            for (int bg = 0; bg < 4; ++bg) {
+                const int owner = bg / NBLK, loc = bg % NBLK;
+                if (NSPLIT == 1) {
+                    bp[bg] = spart[p * NBLK + loc];
+                } else {
+                    const float *peer = cluster.map_shared_rank(spart, (h % r) * NSPLIT + owner);
+                    bp[bg] = peer[p * NBLK + loc];
+                }
+            }
+            const float inv = norm_inv(bp[0], bp[1], bp[2], bp[3], a.rms_eps);
+            const int j = row0 + tid;
+            const int64_t row = tok0 + p;
+            const float zj = load_act<TIn>(static_cast<const TIn *>(a.z) + row * a.z_stride + (int64_t)h * kD + j);
+            a.out[((size_t)row * a.Hv + h) * kD + j] = gated_out(sy[p * ROWS + tid], inv, __ldg(a.norm_w + j), zj);
+        }
+    }
+
+    // ---- Q / K history: each channel rewritten by exactly one CTA of the cluster
+    if (tid % csize == crank) {
+        float *hist_c = histb + (size_t)c_qk * (W - 1);
+        float nh[kMaxW - 1];
+        if (SNAP) {
+            conv_history_after<TIn>(hist_c, xb + c_qk, a.x_stride, W, 1, nh);
+            store_history(a.conv_snap + ((size_t)b * cd + c_qk) * (W - 1), W, nh);
+        }
+        conv_history_after<TIn>(hist_c, xb + c_qk, a.x_stride, W, NTOK, nh);
+        store_history(hist_c, W, nh);
+    }
+    // peers may still be reading this CTA's norm partials
+    if (NSPLIT > 1)
+        cluster.sync();
+}
+
+// ------------------------------------------------------------------ commit
+__global__ void __launch_bounds__(256) verify_commit_kernel(float *state, float *conv_state,
+                                                            const float *state_snap,
+                                                            const float *conv_snap,
+                                                            const int32_t *n_accept,
+                                                            int64_t state_elems, int64_t hist_elems)
+{
+    const int b = blockIdx.y;
+    if (__ldg(n_accept + b) != 1)
+        return;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const float4 *src = reinterpret_cast<const float4 *>(state_snap + b * state_elems);
+    float4 *dst = reinterpret_cast<float4 *>(state + b * state_elems);
+    for (int64_t i = i0; i < state_elems / 4; i += stride)
+        __stcs(dst + i, __ldcs(src + i));
+    for (int64_t i = i0; i < hist_elems; i += stride)
+        conv_state[b * hist_elems + i] = conv_snap[b * hist_elems + i];
+}
+
+// ------------------------------------------------------------------ host launchers
+static int pick_nsplit(int B, int Hv, int r)
+{
+    // Enough CTAs to keep every SM streaming, within an 8-CTA cluster.
+    const int target = 4 * 152;
+    int ns = 1;
+    while (ns < 4 && (int64_t)B * Hv * ns < target && r * ns * 2 <= 8)
+        ns *= 2;
+    return ns;
+}
+
+template <typename K, typename A>
+static cudaError_t launch_cluster(K kernel, dim3 grid, int csize, cudaStream_t s, const A &args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = csize > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args);
+}
+
+template <typename TIn, int NTOK>
+static cudaError_t fused_dispatch(const FusedArgs &a, cudaStream_t s)
+{
+    const int r = a.Hv / a.Hq;
+    const int ns = pick_nsplit(a.B, a.Hv, r);
+    const dim3 grid(a.Hv * ns, a.B, 1);
+    switch (ns) {
+    case 1: return launch_cluster(decode_fused_kernel<TIn, NTOK, 1>, grid, r, s, a);
+    case 2: return launch_cluster(decode_fused_kernel<TIn, NTOK, 2>, grid, r * 2, s, a);
+    default: return launch_cluster(decode_fused_kernel<TIn, NTOK, 4>, grid, r * 4, s, a);
+    }
+}
+
+cudaError_t launch_decode_fused(const FusedArgs &a, bool bf16, int ntok, cudaStream_t s)
+{
+    if (bf16)
+        return ntok == 1 ? fused_dispatch<__nv_bfloat16, 1>(a, s) : fused_dispatch<__nv_bfloat16, 2>(a, s);
+    return ntok == 1 ? fused_dispatch<float, 1>(a, s) : fused_dispatch<float, 2>(a, s);
+}
+
+cudaError_t launch_decay_gate(const void *alpha, bool bf16, int64_t alpha_stride, const float *dt,
+                              const float *A_log, float *g, int rows, int H, cudaStream_t s)
+{
+    const int64_t n = (int64_t)rows * H;
+    const unsigned blocks = (unsigned)((n + 255) / 256);
+    if (bf16)
+        decay_gate_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(alpha),
+                                                 alpha_stride, dt, A_log, g, rows, H);
+    else
+        decay_gate_kernel<<<blocks, 256, 0, s>>>(static_cast<const float *>(alpha), alpha_stride,
+                                                 dt, A_log, g, rows, H);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_conv_update(const ConvArgs &a, bool bf16, cudaStream_t s)
+{
+    const dim3 grid(a.conv_dim / kD, a.B, 1);
+    if (bf16)
+        conv_update_kernel<__nv_bfloat16><<<grid, kD, 0, s>>>(a);
+    else
+        conv_update_kernel<float><<<grid, kD, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_recurrence_decode(const RecArgs &a, cudaStream_t s)
+{
+    const int r = a.Hv / a.Hq;
+    const int ns = pick_nsplit(a.B, a.Hv, r);
+    const dim3 grid(a.Hv * ns, a.B, 1);
+    switch (ns) {
+    case 1: recurrence_decode_kernel<1><<<grid, 256, 0, s>>>(a); break;
+    case 2: recurrence_decode_kernel<2><<<grid, 256, 0, s>>>(a); break;
+    default: recurrence_decode_kernel<4><<<grid, 256, 0, s>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gated_norm(const float *y, const float *w, const void *z, bool bf16,
+                              int64_t z_stride, float *out, int rows, int Hv, float eps,
+                              cudaStream_t s)
+{
+    const int64_t n = (int64_t)rows * Hv;
+    const unsigned blocks = (unsigned)((n + 7) / 8);
+    if (bf16)
+        gated_norm_kernel<<<blocks, 256, 0, s>>>(y, w, static_cast<const __nv_bfloat16 *>(z),
+                                                 z_stride, out, rows, Hv, eps);
+    else
+        gated_norm_kernel<<<blocks, 256, 0, s>>>(y, w, static_cast<const float *>(z), z_stride,
+                                                 out, rows, Hv, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify_commit(float *state, float *conv_state, const float *state_snap,
+                                 const float *conv_snap, const int32_t *n_accept, int B,
+                                 int64_t state_elems, int64_t hist_elems, cudaStream_t s)
+{
+    const dim3 grid(64, B, 1);
+    verify_commit_kernel<<<grid, 256, 0, s>>>(state, conv_state, state_snap, conv_snap, n_accept,
+                                              state_elems, hist_elems);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,67 @@
+// gdn_kernels.h -- internal launch interface between the C ABI (abi.cu) and
+// the kernel files. Not installed; the public interface is include/gdn.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+struct FusedArgs {
+    float *state;          // [B][Hv][d][d]
+    float *conv_state;     // [B][conv_dim][W-1]
+    float *state_snap;     // verify only
+    float *conv_snap;      // verify only
+    const void *x, *z, *alpha, *beta_logit;
+    const float *conv_w, *dt, *A_log, *norm_w;
+    float *out;            // [B][NTOK][Hv][d]
+    int64_t x_stride, z_stride, gate_stride;
+    int B, Hq, Hv, W, conv_dim;
+    float l2_eps, rms_eps, scale;
+};
+
+struct ConvArgs {
+    float *conv_state;
+    const void *x;
+    const float *conv_w;
+    float *out;            // [B][T][conv_dim]
+    int64_t x_stride;
+    int B, Hq, Hv, W, conv_dim, T;
+    float l2_eps;
+};
+
+struct RecArgs {
+    float *state;
+    const float *q, *k, *v;
+    int64_t qkv_stride;
+    const float *g, *beta;
+    float *y;
+    int B, Hq, Hv;
+    float scale;
+};
+
+struct PrefillArgs {
+    float *state;
+    float *conv_state;
+    const void *x, *z, *alpha, *beta_logit;
+    const float *conv_w, *dt, *A_log, *norm_w;
+    float *out;            // [B][T][Hv][d]
+    int64_t x_stride, z_stride, gate_stride;
+    int B, Hq, Hv, W, conv_dim, T;
+    float l2_eps, rms_eps, scale;
+};
+
+cudaError_t launch_decode_fused(const FusedArgs &a, bool bf16, int ntok, cudaStream_t s);
+cudaError_t launch_decay_gate(const void *alpha, bool bf16, int64_t alpha_stride, const float *dt,
+                              const float *A_log, float *g, int rows, int H, cudaStream_t s);
+cudaError_t launch_conv_update(const ConvArgs &a, bool bf16, cudaStream_t s);
+cudaError_t launch_recurrence_decode(const RecArgs &a, cudaStream_t s);
+cudaError_t launch_gated_norm(const float *y, const float *w, const void *z, bool bf16,
+                              int64_t z_stride, float *out, int rows, int Hv, float eps,
+                              cudaStream_t s);
+cudaError_t launch_verify_commit(float *state, float *conv_state, const float *state_snap,
+                                 const float *conv_snap, const int32_t *n_accept, int B,
+                                 int64_t state_elems, int64_t hist_elems, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s);
+
+}  // namespace gdn

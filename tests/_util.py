@@ -1,0 +1,83 @@
+"""Shared helpers for the test suite: device upload, oracle runs, error metrics."""
+from __future__ import annotations
+
+import numpy as np
+
+from gated_delta_ssm_gb300 import synth
+
+OUT_TOL = 1e-3      # max relative error on layer outputs
+STATE_TOL = 1e-4    # max relative error on the fp32 recurrent state
+
+
+def as_f32(a, dtype):
+    """Exact float32 values of an activation array (bf16 bits or float32)."""
+    if dtype == "bf16":
+        return synth.bf16_to_f32(np.ascontiguousarray(a))
+    return np.ascontiguousarray(a, np.float32)
+
+
+def to_dev(a, dtype="f32"):
+    import torch
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(a, np.float32))
+    return t.cuda()
+
+
+def device_inputs(shape: synth.Shape, inp: dict) -> dict:
+    """Upload one workload; z stays a view into x when the shape keeps it in the row."""
+    import torch
+    dt = shape.act_dtype
+    dev = {"x": to_dev(inp["x"], dt)}
+    if shape.z_in_x:
+        cd = shape.conv_dim
+        dev["z"] = dev["x"][..., cd:cd + shape.Hv * shape.d]
+    else:
+        dev["z"] = to_dev(inp["z"], dt)
+    for k in ("alpha", "beta_logit"):
+        dev[k] = to_dev(inp[k], dt)
+    for k in ("conv_w", "dt", "A_log", "norm_w", "state", "hist"):
+        dev[k] = to_dev(inp[k])
+    dev["accept"] = torch.from_numpy(inp["accept"]).cuda()
+    return dev
+
+
+def dims_of(shape: synth.Shape, rows_per_seq: int = 1):
+    """ABI dims. rows_per_seq > 1 when single-token calls read one token slice
+    ([:, t]) of a buffer that holds rows_per_seq tokens per sequence."""
+    import gated_delta_ssm_gb300 as gdn
+    m = rows_per_seq
+    return gdn.Dims(n_seq=shape.B, n_qk_heads=shape.Hq, n_v_heads=shape.Hv, head_dim=shape.d,
+                    d_conv=shape.W, x_stride=shape.xs * m,
+                    z_stride=(shape.xs if shape.z_in_x else shape.Hv * shape.d) * m,
+                    gate_stride=shape.Hv * m)
+
+
+def params_of(dev: dict):
+    import gated_delta_ssm_gb300 as gdn
+    return gdn.Params(dev["conv_w"], dev["dt"], dev["A_log"], dev["norm_w"], 1e-6, 1e-6)
+
+
+def run_oracle(shape: synth.Shape, inp: dict, T=None, seqs=None, **kw):
+    import oracle
+    T = shape.T if T is None else T
+    dt = shape.act_dtype
+    x = as_f32(inp["x"][:, :T], dt)
+    z = as_f32(np.ascontiguousarray(inp["z"][:, :T]), dt)
+    return oracle.layer(x, z, as_f32(inp["alpha"][:, :T], dt), as_f32(inp["beta_logit"][:, :T], dt),
+                        inp["conv_w"], inp["dt"], inp["A_log"], inp["norm_w"], inp["state"],
+                        inp["hist"], Hq=shape.Hq, W=shape.W, seqs=seqs, **kw)
+
+
+def max_rel(x, ref, slice_axes: int):
+    """Normwise relative error: max over slices (the trailing `slice_axes` axes form one
+    slice) of max|x - ref| / max|ref| within the slice."""
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    lead = x.shape[:x.ndim - slice_axes]
+    xf = x.reshape(int(np.prod(lead)) if lead else 1, -1)
+    rf = ref.reshape(xf.shape)
+    den = np.abs(rf).max(axis=1)
+    den = np.where(den == 0, 1.0, den)
+    return float((np.abs(xf - rf).max(axis=1) / den).max())

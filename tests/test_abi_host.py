@@ -1,0 +1,124 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/gdn.h declares, and rejects bad arguments on the host before any
+CUDA call is made."""
+import ctypes as ct
+import os
+import re
+
+import pytest
+
+import gated_delta_ssm_gb300 as gdn
+from gated_delta_ssm_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdn.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("gdn_conv_update", "gdn_decay_gate", "gdn_recurrence_decode", "gdn_verify_k2",
+                     "gdn_prefill_chunked", "gdn_gated_norm", "gdn_decode_step",
+                     "gdn_verify_commit", "gdn_last_cuda_error", "gdn_version"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_strings(lib):
+    assert b"sm_103a" in lib.gdn_version()
+    assert lib.gdn_status_string(1) == b"GDN_ERR_INVALID_ARG"
+    assert lib.gdn_last_cuda_error() == b""
+
+
+FAKE = 1 << 40      # a well-aligned non-null address; never dereferenced on these paths
+
+
+def _dims(**kw):
+    d = dict(n_seq=2, n_qk_heads=2, n_v_heads=4, head_dim=128, d_conv=4)
+    d.update(kw)
+    return gdn.Dims(**d)
+
+
+def _params():
+    return gdn.Params(FAKE, FAKE, FAKE, FAKE)
+
+
+def _decode(lib, dims, **ptrs):
+    p = dict(state=FAKE, conv=FAKE, x=FAKE, z=FAKE, a=FAKE, b=FAKE, out=FAKE)
+    p.update(ptrs)
+    cd, cp = dims.c(), _params().c()
+    return lib.gdn_decode_step(p["state"], p["conv"], p["x"], p["z"], p["a"], p["b"], gdn.GDN_BF16,
+                               ct.byref(cp), p["out"], ct.byref(cd), None)
+
+
+@pytest.mark.parametrize("field", ["state", "conv", "x", "z", "a", "b", "out"])
+def test_decode_step_rejects_null_pointers(lib, field):
+    assert _decode(lib, _dims(), **{field: None}) == gdn.GDN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n_seq=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(n_qk_heads=3, n_v_heads=4), gdn.GDN_ERR_INVALID_ARG),      # Hv not a multiple of Hq
+    (dict(head_dim=64), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(d_conv=1), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(d_conv=9), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(n_qk_heads=1, n_v_heads=16), gdn.GDN_ERR_UNSUPPORTED),     # r = 16 > 8
+    (dict(x_stride=100), gdn.GDN_ERR_INVALID_ARG),
+    (dict(z_stride=5), gdn.GDN_ERR_INVALID_ARG),
+    (dict(gate_stride=3), gdn.GDN_ERR_INVALID_ARG),
+])
+def test_decode_step_rejects_bad_dims(lib, kw, status):
+    assert _decode(lib, _dims(**kw)) == status
+
+
+def test_decode_step_rejects_misaligned_state(lib):
+    assert _decode(lib, _dims(), state=FAKE + 4) == gdn.GDN_ERR_INVALID_ARG
+    assert _decode(lib, _dims(), x=FAKE + 1) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_verify_rejects_aliased_snapshot(lib):
+    cd, cp = _dims().c(), _params().c()
+    st = lib.gdn_verify_k2(FAKE, FAKE + 64, FAKE, FAKE + 128, FAKE, FAKE, FAKE, FAKE, gdn.GDN_F32,
+                           ct.byref(cp), FAKE, ct.byref(cd), None)
+    assert st == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_prefill_rejects_bad_chunk_and_tokens(lib):
+    cd, cp = _dims().c(), _params().c()
+    args = [FAKE] * 6 + [gdn.GDN_BF16, ct.byref(cp), FAKE, ct.byref(cd)]
+    assert lib.gdn_prefill_chunked(*args, 128, 32, None) == gdn.GDN_ERR_UNSUPPORTED
+    assert lib.gdn_prefill_chunked(*args, 0, 64, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_other_entry_points_validate(lib):
+    cd = _dims().c()
+    assert lib.gdn_decay_gate(None, 0, 4, FAKE, FAKE, FAKE, 1, 4, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_decay_gate(FAKE, 0, 3, FAKE, FAKE, FAKE, 1, 4, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_conv_update(FAKE, FAKE, 0, FAKE, FAKE, ct.byref(cd), 0, 1e-6, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_gated_norm(FAKE, FAKE, FAKE, 0, 512, FAKE, 1, 4, 64, 1e-6, None) == gdn.GDN_ERR_UNSUPPORTED
+    assert lib.gdn_gated_norm(FAKE, FAKE, FAKE, 0, 100, FAKE, 1, 4, 128, 1e-6, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_recurrence_decode(FAKE, FAKE, FAKE, FAKE, 10, FAKE, FAKE, FAKE, ct.byref(cd),
+                                     1.0, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_verify_commit(FAKE, FAKE, FAKE, FAKE, None, ct.byref(cd), None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 7, ct.byref(_params().c()), FAKE,
+                               ct.byref(cd), None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_binding_raises_loudly_on_bad_status(lib):
+    with pytest.raises(gdn.GdnError):
+        gdn._check(gdn.GDN_ERR_INVALID_ARG, "gdn_decode_step")

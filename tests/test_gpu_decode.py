@@ -1,0 +1,277 @@
+"""GPU parity of the decode-side entry points against the fp64 oracle, and the
+bitwise invariants between them (verify vs decode, commit vs one step,
+scan vs steps, fused vs standalone)."""
+import math
+
+import numpy as np
+import pytest
+
+from gated_delta_ssm_gb300 import synth
+from tests._util import (OUT_TOL, STATE_TOL, as_f32, device_inputs, dims_of, max_rel, params_of,
+                         run_oracle, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import gated_delta_ssm_gb300 as gdn  # noqa: E402
+
+
+def _decode_tokens(shape, dev, T):
+    """Run T single-token decode steps; returns outputs [B][T][Hv][d]."""
+    dims = dims_of(shape, rows_per_seq=dev["x"].shape[1])
+    prm = params_of(dev)
+    B, Hv, d = shape.B, shape.Hv, shape.d
+    outs = torch.empty(B, T, Hv, d, device="cuda")
+    step_out = torch.empty(B, Hv, d, device="cuda")
+    for t in range(T):
+        gdn.decode_step(dev["state"], dev["hist"], dev["x"][:, t], dev["z"][:, t],
+                        dev["alpha"][:, t], dev["beta_logit"][:, t], prm, step_out, dims)
+        outs[:, t] = step_out
+    torch.cuda.synchronize()
+    return outs
+
+
+# ------------------------------------------------------------------ workload parity
+def test_tiny_sequential_16_steps_matches_oracle():
+    shape = synth.WORKLOADS["tiny_seq"]
+    inp = synth.make_inputs(shape, seed=0)
+    ref = run_oracle(shape, inp)
+    dev = device_inputs(shape, inp)
+    outs = _decode_tokens(shape, dev, shape.T).cpu().numpy()
+    assert max_rel(outs, ref["out"], 1) <= OUT_TOL
+    assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= STATE_TOL
+    assert max_rel(dev["hist"].cpu().numpy(), ref["hist"], 2) == 0.0
+
+
+@pytest.mark.parametrize("name", ["decode_b1", "decode_b64"])
+def test_single_step_workloads_match_oracle(name):
+    shape = synth.WORKLOADS[name]
+    inp = synth.make_inputs(shape, seed=1 if name == "decode_b1" else 2)
+    ref = run_oracle(shape, inp)
+    dev = device_inputs(shape, inp)
+    out = torch.empty(shape.B, shape.Hv, shape.d, device="cuda")
+    gdn.decode_step(dev["state"], dev["hist"], dev["x"], dev["z"], dev["alpha"],
+                    dev["beta_logit"], params_of(dev), out, dims_of(shape))
+    torch.cuda.synchronize()
+    assert max_rel(out.cpu().numpy(), ref["out"][:, 0], 1) <= OUT_TOL
+    assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= STATE_TOL
+    assert max_rel(dev["hist"].cpu().numpy(), ref["hist"], 2) == 0.0
+
+
+def test_decode_b1_sixteen_steps_state():
+    shape = synth.Shape(B=1, T=16, Hq=16, Hv=32, warm=True)
+    inp = synth.make_inputs(shape, seed=7)
+    ref = run_oracle(shape, inp)
+    dev = device_inputs(shape, inp)
+    outs = _decode_tokens(shape, dev, 16).cpu().numpy()
+    assert max_rel(outs, ref["out"], 1) <= OUT_TOL
+    assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= STATE_TOL
+
+
+@pytest.mark.parametrize("W,Hq,Hv,B", [(2, 1, 1, 3), (8, 2, 2, 2), (3, 1, 3, 5), (4, 1, 8, 2),
+                                       (5, 2, 8, 1)])
+def test_edge_shapes_match_oracle(W, Hq, Hv, B):
+    shape = synth.Shape(B=B, T=3, Hq=Hq, Hv=Hv, W=W, warm=True)
+    inp = synth.make_inputs(shape, seed=100 + W)
+    ref = run_oracle(shape, inp)
+    dev = device_inputs(shape, inp)
+    outs = _decode_tokens(shape, dev, 3).cpu().numpy()
+    assert max_rel(outs, ref["out"], 1) <= OUT_TOL
+    assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= STATE_TOL
+    assert max_rel(dev["hist"].cpu().numpy(), ref["hist"], 2) == 0.0
+
+
+# ------------------------------------------------------------------ verify K=2 + commit
+def test_verify_k2_matches_oracle_and_decode_bitwise():
+    shape = synth.WORKLOADS["verify_k2"]
+    inp = synth.make_inputs(shape, seed=3)
+    ref = run_oracle(shape, inp, snap_after=0)
+    dev = device_inputs(shape, inp)
+    dims, prm = dims_of(shape), params_of(dev)
+    B, Hv, d = shape.B, shape.Hv, shape.d
+    st0, hi0 = dev["state"].clone(), dev["hist"].clone()
+    snap = torch.empty_like(dev["state"])
+    hsnap = torch.empty_like(dev["hist"])
+    out = torch.empty(B, 2, Hv, d, device="cuda")
+    gdn.verify_k2(dev["state"], dev["hist"], snap, hsnap, dev["x"], dev["z"], dev["alpha"],
+                  dev["beta_logit"], prm, out, dims)
+    torch.cuda.synchronize()
+    # against the oracle
+    assert max_rel(out.cpu().numpy(), ref["out"], 1) <= OUT_TOL
+    assert max_rel(snap.cpu().numpy(), ref["state_snap"], 2) <= STATE_TOL
+    assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= STATE_TOL
+    assert np.array_equal(hsnap.cpu().numpy(), ref["hist_snap"].astype(np.float32))
+    assert np.array_equal(dev["hist"].cpu().numpy(), ref["hist"].astype(np.float32))
+    # against two single-token decode steps, bit for bit
+    dims = dims_of(shape, rows_per_seq=2)
+    dec = dict(dev, state=st0.clone(), hist=hi0.clone())
+    step = torch.empty(B, Hv, d, device="cuda")
+    gdn.decode_step(dec["state"], dec["hist"], dev["x"][:, 0], dev["z"][:, 0], dev["alpha"][:, 0],
+                    dev["beta_logit"][:, 0], prm, step, dims)
+    torch.cuda.synchronize()
+    assert torch.equal(step, out[:, 0])
+    assert torch.equal(dec["state"], snap) and torch.equal(dec["hist"], hsnap)
+    gdn.decode_step(dec["state"], dec["hist"], dev["x"][:, 1], dev["z"][:, 1], dev["alpha"][:, 1],
+                    dev["beta_logit"][:, 1], prm, step, dims)
+    torch.cuda.synchronize()
+    assert torch.equal(step, out[:, 1])
+    assert torch.equal(dec["state"], dev["state"]) and torch.equal(dec["hist"], dev["hist"])
+    # commit: accept 1 rolls back to the one-step state, accept 2 keeps both
+    acc = dev["accept"]
+    gdn.verify_commit(dev["state"], dev["hist"], snap, hsnap, acc, dims_of(shape))
+    torch.cuda.synchronize()
+    one = (acc == 1).cpu().numpy()
+    assert one.any() and (~one).any()
+    want_state = torch.where(torch.from_numpy(one).cuda()[:, None, None, None], snap, dec["state"])
+    want_hist = torch.where(torch.from_numpy(one).cuda()[:, None, None], hsnap, dec["hist"])
+    assert torch.equal(dev["state"], want_state)
+    assert torch.equal(dev["hist"], want_hist)
+
+
+def test_commit_ignores_other_accept_values():
+    shape = synth.Shape(B=4, T=2, Hq=1, Hv=2, warm=True)
+    inp = synth.make_inputs(shape, seed=9)
+    dev = device_inputs(shape, inp)
+    snap = torch.zeros_like(dev["state"])
+    hsnap = torch.zeros_like(dev["hist"])
+    before = dev["state"].clone(), dev["hist"].clone()
+    acc = torch.tensor([0, 2, 3, -1], dtype=torch.int32, device="cuda")
+    gdn.verify_commit(dev["state"], dev["hist"], snap, hsnap, acc, dims_of(shape))
+    torch.cuda.synchronize()
+    assert torch.equal(dev["state"], before[0]) and torch.equal(dev["hist"], before[1])
+
+
+# ------------------------------------------------------------------ standalone parts
+def test_standalone_parts_match_oracle_and_fused():
+    shape = synth.Shape(B=3, T=1, Hq=4, Hv=8, warm=True)
+    inp = synth.make_inputs(shape, seed=21)
+    ref = run_oracle(shape, inp, intermediates=True)
+    dev = device_inputs(shape, inp)
+    dims = dims_of(shape)
+    B, Hq, Hv, d, cd = shape.B, shape.Hq, shape.Hv, shape.d, shape.conv_dim
+    # conv + SiLU + L2
+    hist = dev["hist"].clone()
+    conv = torch.empty(B, 1, cd, device="cuda")
+    gdn.conv_update(hist, dev["x"], dev["conv_w"], conv, dims, 1, 1e-6)
+    # gate
+    g = torch.empty(B, Hv, device="cuda")
+    gdn.decay_gate(dev["alpha"], dev["dt"], dev["A_log"], g, B, Hv)
+    torch.cuda.synchronize()
+    assert max_rel(conv.cpu().numpy(), ref["conv"], 1) <= 1e-5
+    assert np.array_equal(hist.cpu().numpy(), ref["hist"].astype(np.float32))
+    assert max_rel(g.cpu().numpy(), ref["g"][:, 0], 1) <= 1e-5
+    # recurrence fed the GPU conv + gate outputs, beta from torch
+    beta = torch.sigmoid(dev["beta_logit"][:, 0].float()).contiguous()
+    state = dev["state"].clone()
+    y = torch.empty(B, Hv, d, device="cuda")
+    c0 = conv[:, 0]
+    gdn.recurrence_decode(state, c0, c0[:, Hq * d:], c0[:, 2 * Hq * d:], cd, g, beta, y, dims,
+                          1 / math.sqrt(d))
+    out = torch.empty_like(y)
+    gdn.gated_norm(y, dev["norm_w"], dev["z"][:, 0], out, B, Hv, d, Hv * d, 1e-6)
+    torch.cuda.synchronize()
+    assert max_rel(y.cpu().numpy(), ref["y"][:, 0], 1) <= OUT_TOL
+    assert max_rel(out.cpu().numpy(), ref["out"][:, 0], 1) <= OUT_TOL
+    assert max_rel(state.cpu().numpy(), ref["state"], 2) <= STATE_TOL
+    # the fused step agrees with the composition (beta differs only in its sigmoid rounding)
+    fused = torch.empty_like(y)
+    fstate = dev["state"].clone()
+    fhist = dev["hist"].clone()
+    gdn.decode_step(fstate, fhist, dev["x"], dev["z"], dev["alpha"], dev["beta_logit"],
+                    params_of(dev), fused, dims)
+    torch.cuda.synchronize()
+    assert torch.equal(fhist, hist)
+    assert max_rel(fused.cpu().numpy(), out.cpu().numpy(), 1) <= 1e-5
+    assert max_rel(fstate.cpu().numpy(), state.cpu().numpy(), 2) <= 1e-5
+
+
+def test_recurrence_fed_oracle_inputs():
+    # the recurrence alone, fed the oracle's own prepared q^, k^, v, g, beta (fp32-rounded)
+    shape = synth.Shape(B=2, T=1, Hq=2, Hv=6, warm=True)
+    inp = synth.make_inputs(shape, seed=22)
+    ref = run_oracle(shape, inp, intermediates=True)
+    B, Hq, Hv, d, cd = shape.B, shape.Hq, shape.Hv, shape.d, shape.conv_dim
+    conv = to_dev(ref["conv"][:, 0].astype(np.float32))
+    g = to_dev(ref["g"][:, 0].astype(np.float32))
+    beta = to_dev(ref["beta"][:, 0].astype(np.float32))
+    state = to_dev(inp["state"])
+    y = torch.empty(B, Hv, d, device="cuda")
+    gdn.recurrence_decode(state, conv, conv[:, Hq * d:], conv[:, 2 * Hq * d:], cd, g, beta, y,
+                          dims_of(shape), 1 / math.sqrt(d))
+    torch.cuda.synchronize()
+    assert max_rel(y.cpu().numpy(), ref["y"][:, 0], 1) <= 1e-4
+    assert max_rel(state.cpu().numpy(), ref["state"], 2) <= 1e-5
+
+
+def test_gated_norm_aliases_and_bf16_z():
+    shape = synth.Shape(B=5, T=1, Hq=1, Hv=4, warm=True)
+    inp = synth.make_inputs(shape, seed=23)
+    ref = run_oracle(shape, inp, intermediates=True)
+    y = to_dev(ref["y"][:, 0].astype(np.float32))
+    z = to_dev(inp["z"][:, 0], "bf16")
+    w = to_dev(inp["norm_w"])
+    gdn.gated_norm(y, w, z, y, shape.B, shape.Hv, 128, shape.Hv * 128, 1e-6)   # in place
+    torch.cuda.synchronize()
+    assert max_rel(y.cpu().numpy(), ref["out"][:, 0], 1) <= 1e-5
+
+
+def test_conv_scan_equals_single_steps_bitwise():
+    shape = synth.Shape(B=2, T=7, Hq=2, Hv=4, W=4, warm=True)
+    inp = synth.make_inputs(shape, seed=24)
+    dev = device_inputs(shape, inp)
+    dims = dims_of(shape)
+    cd = shape.conv_dim
+    h1 = dev["hist"].clone()
+    full = torch.empty(shape.B, shape.T, cd, device="cuda")
+    gdn.conv_update(h1, dev["x"], dev["conv_w"], full, dims, shape.T, 1e-6)
+    h2 = dev["hist"].clone()
+    steps = torch.empty_like(full)
+    one = torch.empty(shape.B, 1, cd, device="cuda")
+    for t in range(shape.T):
+        xt = dev["x"][:, t:t + 1].contiguous()
+        gdn.conv_update(h2, xt, dev["conv_w"], one, dims, 1, 1e-6)
+        steps[:, t] = one[:, 0]
+    torch.cuda.synchronize()
+    assert torch.equal(full, steps) and torch.equal(h1, h2)
+    ref = run_oracle(shape, inp, intermediates=True)
+    assert max_rel(full.cpu().numpy(), ref["conv"], 1) <= 1e-5
+
+
+def test_result_independent_of_batch_split():
+    # the same sequence decoded alone (few CTAs: row-split clusters) and inside a
+    # large batch (one CTA per head) gives identical bits
+    big = synth.Shape(B=64, T=1, Hq=16, Hv=32, warm=True)
+    inp = synth.make_inputs(big, seed=25)
+    dev = device_inputs(big, inp)
+    out_big = torch.empty(64, 32, 128, device="cuda")
+    st_big = dev["state"].clone()
+    gdn.decode_step(st_big, dev["hist"].clone(), dev["x"], dev["z"], dev["alpha"],
+                    dev["beta_logit"], params_of(dev), out_big, dims_of(big))
+    small = synth.Shape(B=1, T=1, Hq=16, Hv=32, warm=True)
+    b = 17
+    st1 = dev["state"][b:b + 1].clone()
+    out1 = torch.empty(1, 32, 128, device="cuda")
+    gdn.decode_step(st1, dev["hist"][b:b + 1].clone(), dev["x"][b:b + 1], dev["z"][b:b + 1],
+                    dev["alpha"][b:b + 1], dev["beta_logit"][b:b + 1], params_of(dev), out1,
+                    dims_of(small))
+    torch.cuda.synchronize()
+    assert torch.equal(out1[0], out_big[b])
+    assert torch.equal(st1[0], st_big[b])
+
+
+def test_repeat_runs_are_deterministic():
+    shape = synth.WORKLOADS["decode_b64"]
+    inp = synth.make_inputs(shape, seed=26)
+    dev = device_inputs(shape, inp)
+    res = []
+    for _ in range(2):
+        st, hi = dev["state"].clone(), dev["hist"].clone()
+        out = torch.empty(shape.B, shape.Hv, shape.d, device="cuda")
+        gdn.decode_step(st, hi, dev["x"], dev["z"], dev["alpha"], dev["beta_logit"],
+                        params_of(dev), out, dims_of(shape))
+        torch.cuda.synchronize()
+        res.append((out, st, hi))
+    assert all(torch.equal(a, b) for a, b in zip(res[0], res[1]))
