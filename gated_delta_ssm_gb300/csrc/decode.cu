@@ -77,6 +77,9 @@ __global__ void __launch_bounds__(256, 2) recurrence_decode_kernel(RecArgs a)
     const int h = blockIdx.x / NSPLIT, split = blockIdx.x % NSPLIT;
     const int hk = h / (a.Hv / a.Hq);
     const int row0 = split * ROWS;
+    float *rows = a.state + (((size_t)b * a.Hv + h) * kD + row0 + warp * RPW) * kD;
+    float4 r[NG][4];
+    load_rows<NG>(rows, r);
     if (tid < kD)
         sq[tid] = __ldg(a.q + (int64_t)b * a.qkv_stride + hk * kD + tid);
     else
@@ -88,9 +91,8 @@ __global__ void __launch_bounds__(256, 2) recurrence_decode_kernel(RecArgs a)
         sbeta[0] = __ldg(a.beta + (size_t)b * a.Hv + h);
     }
     __syncthreads();
-    float *rows = a.state + (((size_t)b * a.Hv + h) * kD + row0 + warp * RPW) * kD;
-    recurrence_rows<NG, 1, false>(rows, nullptr, sk, sq, sv, ROWS, sdecay, sbeta, sy, warp * RPW,
-                                  a.scale);
+    step_rows<NG, 1, false>(r, rows, nullptr, sk, sq, sv, ROWS, sdecay, sbeta, sy, warp * RPW,
+                            a.scale);
     __syncthreads();
     if (tid < ROWS)
         a.y[((size_t)b * a.Hv + h) * kD + row0 + tid] = sy[tid];
@@ -156,6 +158,12 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
     const TIn *xb = static_cast<const TIn *>(a.x) + tok0 * a.x_stride;
     float *histb = a.conv_state + (size_t)b * cd * (W - 1);
 
+    // ---- this warp's state rows: loads in flight during the prologue
+    const size_t head_off = ((size_t)b * a.Hv + h) * kD * kD;
+    const size_t warp_off = (size_t)(row0 + warp * RPW) * kD;
+    float4 st[NG][4];
+    load_rows<NG>(a.state + head_off + warp_off, st);
+
     // ---- Q / K conv + SiLU + per-head L2 (threads 0..127: Q head, 128..255: K head)
     const bool is_k = tid >= kD;
     const int c_qk = (is_k ? a.Hq * kD : 0) + hk * kD + (tid & (kD - 1));
@@ -198,11 +206,9 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
     __syncthreads();
 
     // ---- recurrence over this CTA's rows, state read once and written once
-    const size_t head_off = ((size_t)b * a.Hv + h) * kD * kD;
-    const size_t warp_off = (size_t)(row0 + warp * RPW) * kD;
-    recurrence_rows<NG, NTOK, SNAP>(a.state + head_off + warp_off,
-                                    SNAP ? a.state_snap + head_off + warp_off : nullptr, sk, sq,
-                                    sv, ROWS, sdecay, sbeta, sy, warp * RPW, a.scale);
+    step_rows<NG, NTOK, SNAP>(st, a.state + head_off + warp_off,
+                              SNAP ? a.state_snap + head_off + warp_off : nullptr, sk, sq, sv,
+                              ROWS, sdecay, sbeta, sy, warp * RPW, a.scale);
     __syncthreads();
 
     // ---- gated RMSNorm: 32-row block partials, combined in block order

@@ -171,6 +171,8 @@ __device__ __forceinline__ float gated_out(float y, float inv, float w, float z)
 // which is the page's read-after-write readout, expanded so that both dot
 // products share one reduction.
 //
+// load_rows issues the warp's loads (callers issue them before their
+// prologue so the HBM latency overlaps it); step_rows consumes them:
 //   rows       first row of this warp's block in global memory (row stride kD)
 //   snap_rows  same rows in the snapshot buffer (used when SNAP)
 //   sk, sq     shared [NTOK][kD] normalised k, q
@@ -178,22 +180,28 @@ __device__ __forceinline__ float gated_out(float y, float inv, float w, float z)
 //   sdecay, sbeta shared [NTOK]
 //   sy         shared [NTOK][v_stride] readout y (written by one lane per row)
 //   local_row0 local index of this warp's first row
-template <int NG, int NTOK, bool SNAP>
-__device__ __forceinline__ void recurrence_rows(float *rows, float *snap_rows, const float *sk,
-                                                const float *sq, const float *sv, int v_stride,
-                                                const float *sdecay, const float *sbeta,
-                                                float *sy, int local_row0, float scale)
+template <int NG>
+__device__ __forceinline__ void load_rows(const float *rows, float4 (&r)[NG][4])
 {
     const int lane = threadIdx.x & 31;
     const int rg = lane >> 3;
     const int sub = lane & 7;
-    float4 r[NG][4];
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi)
 #pragma unroll
         for (int m = 0; m < 4; ++m)
             r[gi][m] = ld_stream(rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4);
+}
 
+template <int NG, int NTOK, bool SNAP>
+__device__ __forceinline__ void step_rows(float4 (&r)[NG][4], float *rows, float *snap_rows,
+                                          const float *sk, const float *sq, const float *sv,
+                                          int v_stride, const float *sdecay, const float *sbeta,
+                                          float *sy, int local_row0, float scale)
+{
+    const int lane = threadIdx.x & 31;
+    const int rg = lane >> 3;
+    const int sub = lane & 7;
 #pragma unroll
     for (int p = 0; p < NTOK; ++p) {
         float4 k4[4], q4[4];

@@ -1,0 +1,97 @@
+"""GPU parity of the chunked prefill against the fp64 sequential-scan oracle."""
+import numpy as np
+import pytest
+
+from gated_delta_ssm_gb300 import synth
+from tests._util import OUT_TOL, STATE_TOL, device_inputs, dims_of, max_rel, params_of, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import gated_delta_ssm_gb300 as gdn  # noqa: E402
+
+PREFILL_STATE_TOL = STATE_TOL
+
+
+def _prefill(shape, dev, T=None):
+    T = shape.T if T is None else T
+    out = torch.empty(shape.B, T, shape.Hv, shape.d, device="cuda")
+    gdn.prefill_chunked(dev["state"], dev["hist"], dev["x"], dev["z"], dev["alpha"],
+                        dev["beta_logit"], params_of(dev), out, dims_of(shape), T, 64)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 200])
+@pytest.mark.parametrize("warm", [False, True])
+def test_prefill_ragged_lengths_match_oracle(T, warm):
+    shape = synth.Shape(B=2, T=T, Hq=2, Hv=4, warm=warm)
+    inp = synth.make_inputs(shape, seed=300 + T)
+    ref = run_oracle(shape, inp)
+    dev = device_inputs(shape, inp)
+    out = _prefill(shape, dev).cpu().numpy()
+    assert max_rel(out, ref["out"], 1) <= OUT_TOL
+    assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= PREFILL_STATE_TOL
+    assert np.array_equal(dev["hist"].cpu().numpy(), ref["hist"].astype(np.float32))
+
+
+@pytest.mark.parametrize("W,Hq,Hv", [(2, 1, 3), (8, 2, 2), (4, 1, 8)])
+def test_prefill_edge_shapes(W, Hq, Hv):
+    shape = synth.Shape(B=1, T=150, Hq=Hq, Hv=Hv, W=W, warm=True)
+    inp = synth.make_inputs(shape, seed=400 + W)
+    ref = run_oracle(shape, inp)
+    dev = device_inputs(shape, inp)
+    out = _prefill(shape, dev).cpu().numpy()
+    assert max_rel(out, ref["out"], 1) <= OUT_TOL
+    assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= PREFILL_STATE_TOL
+    assert np.array_equal(dev["hist"].cpu().numpy(), ref["hist"].astype(np.float32))
+
+
+def test_prefill_fp32_activations():
+    shape = synth.Shape(B=1, T=130, Hq=4, Hv=4, act_dtype="f32", warm=True)
+    inp = synth.make_inputs(shape, seed=31)
+    ref = run_oracle(shape, inp)
+    dev = device_inputs(shape, inp)
+    out = _prefill(shape, dev).cpu().numpy()
+    assert max_rel(out, ref["out"], 1) <= OUT_TOL
+    assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= PREFILL_STATE_TOL
+
+
+def test_prefill_then_decode_continues_the_sequence():
+    # prefill T tokens then decode one more == oracle over T + 1 tokens
+    shape = synth.Shape(B=2, T=97, Hq=2, Hv=4, warm=True)
+    inp = synth.make_inputs(shape, seed=32)
+    ref = run_oracle(shape, inp)
+    dev = device_inputs(shape, inp)
+    T = shape.T - 1
+    xs = {k: dev[k][:, :T].contiguous() for k in ("x", "z", "alpha", "beta_logit")}
+    out = torch.empty(shape.B, T, shape.Hv, shape.d, device="cuda")
+    gdn.prefill_chunked(dev["state"], dev["hist"], xs["x"], xs["z"], xs["alpha"], xs["beta_logit"],
+                        params_of(dev), out, dims_of(shape), T, 64)
+    step = torch.empty(shape.B, shape.Hv, shape.d, device="cuda")
+    last = {k: dev[k][:, T].contiguous() for k in ("x", "z", "alpha", "beta_logit")}
+    gdn.decode_step(dev["state"], dev["hist"], last["x"], last["z"], last["alpha"],
+                    last["beta_logit"], params_of(dev), step, dims_of(shape))
+    torch.cuda.synchronize()
+    assert max_rel(out.cpu().numpy(), ref["out"][:, :T], 1) <= OUT_TOL
+    assert max_rel(step.cpu().numpy(), ref["out"][:, T], 1) <= OUT_TOL
+    assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= PREFILL_STATE_TOL
+    assert np.array_equal(dev["hist"].cpu().numpy(), ref["hist"].astype(np.float32))
+
+
+def test_prefill_full_size_4x8192():
+    # the full prefill workload; the oracle scans every token for the final state and
+    # its outputs are compared on each sequence's first 512 tokens and last chunk
+    shape = synth.WORKLOADS["prefill"]
+    inp = synth.make_inputs(shape, seed=4)
+    dev = device_inputs(shape, inp)
+    out = _prefill(shape, dev)
+    ref = run_oracle(shape, inp)
+    o = out.cpu().numpy()
+    assert max_rel(o[:, :512], ref["out"][:, :512], 1) <= OUT_TOL
+    assert max_rel(o[:, -64:], ref["out"][:, -64:], 1) <= OUT_TOL
+    assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= PREFILL_STATE_TOL
+    assert np.array_equal(dev["hist"].cpu().numpy(), ref["hist"].astype(np.float32))
