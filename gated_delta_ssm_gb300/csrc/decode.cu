@@ -91,8 +91,8 @@ __global__ void __launch_bounds__(256, 2) recurrence_decode_kernel(RecArgs a)
         sbeta[0] = __ldg(a.beta + (size_t)b * a.Hv + h);
     }
     __syncthreads();
-    step_rows<NG, 1, false>(r, rows, nullptr, sk, sq, sv, ROWS, sdecay, sbeta, sy, warp * RPW,
-                            a.scale);
+    step_rows<NG, 1, false>(r, nullptr, sk, sq, sv, ROWS, sdecay, sbeta, sy, warp * RPW, a.scale);
+    store_rows<NG>(r, rows);
     __syncthreads();
     if (tid < ROWS)
         a.y[((size_t)b * a.Hv + h) * kD + row0 + tid] = sy[tid];
@@ -129,7 +129,28 @@ __global__ void __launch_bounds__(256) gated_norm_kernel(const float *y, const f
 }
 
 // ------------------------------------------------------------------ fused step
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // NTOK = 1: one decode step. NTOK = 2: K=2 verify, snapshot after token 0.
+//
+// Order of a CTA's work, chosen so that no fence ever waits on the state
+// stores: (1) state-row loads, (2) conv-window and gate loads, one memory
+// round trip; (3) conv + SiLU, then cluster arrive (every read of the shared
+// Q/K history is done); (4) L2, gates; (5) recurrence in registers; (6) gated
+// norm (row slices of a head exchange partial sums through distributed
+// shared memory when NSPLIT > 1); (7) state stores; (8) cluster wait, then the
+// single owner of each Q/K channel rewrites its history.
 template <typename TIn, int NTOK, int NSPLIT>
 __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
 {
@@ -158,75 +179,85 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
     const TIn *xb = static_cast<const TIn *>(a.x) + tok0 * a.x_stride;
     float *histb = a.conv_state + (size_t)b * cd * (W - 1);
 
-    // ---- this warp's state rows: loads in flight during the prologue
+    // (1) this warp's state rows: loads in flight during the prologue
     const size_t head_off = ((size_t)b * a.Hv + h) * kD * kD;
     const size_t warp_off = (size_t)(row0 + warp * RPW) * kD;
     float4 st[NG][4];
     load_rows<NG>(a.state + head_off + warp_off, st);
 
-    // ---- Q / K conv + SiLU + per-head L2 (threads 0..127: Q head, 128..255: K head)
+    // (2) conv windows: Q/K channel (every thread), V channel (threads < ROWS); gate inputs
     const bool is_k = tid >= kD;
     const int c_qk = (is_k ? a.Hq * kD : 0) + hk * kD + (tid & (kD - 1));
-    {
-        const float *hist_c = histb + (size_t)c_qk * (W - 1);
-        const float *w_c = a.conv_w + (size_t)c_qk * W;
-        float vals[NTOK];
-#pragma unroll
-        for (int p = 0; p < NTOK; ++p)
-            vals[p] = silu_f(conv_pre<TIn>(hist_c, xb + c_qk, a.x_stride, w_c, W, p));
-#pragma unroll
-        for (int p = 0; p < NTOK; ++p) {
-            const float inv = head_l2_inv(vals[p], a.l2_eps, &sred[p][is_k ? 4 : 0], warp & 3, lane);
-            (is_k ? sk : sq)[p * kD + (tid & (kD - 1))] = __fmul_rn(vals[p], inv);
-        }
+    const int c_v = 2 * a.Hq * kD + h * kD + row0 + tid;
+    ConvWindow<NTOK> wqk, wv;
+    conv_window_load<TIn, NTOK>(histb + (size_t)c_qk * (W - 1), xb + c_qk, a.x_stride,
+                                a.conv_w + (size_t)c_qk * W, W, wqk);
+    if (tid < ROWS)
+        conv_window_load<TIn, NTOK>(histb + (size_t)c_v * (W - 1), xb + c_v, a.x_stride,
+                                    a.conv_w + (size_t)c_v * W, W, wv);
+    float g_alpha = 0.0f, g_bl = 0.0f, g_dt = 0.0f, g_alog = 0.0f;
+    const bool gate_thread = tid >= ROWS && tid < ROWS + NTOK;
+    if (gate_thread) {
+        const int64_t row = tok0 + (tid - ROWS);
+        g_alpha = load_act<TIn>(static_cast<const TIn *>(a.alpha) + row * a.gate_stride + h);
+        g_bl = load_act<TIn>(static_cast<const TIn *>(a.beta_logit) + row * a.gate_stride + h);
+        g_dt = __ldg(a.dt + h);
+        g_alog = __ldg(a.A_log + h);
     }
-    // ---- V conv + SiLU for this CTA's rows (exclusively owned), gates
+
+    // (3) conv + SiLU; every read of the shared Q/K history is now complete
+    float vals[NTOK];
+#pragma unroll
+    for (int p = 0; p < NTOK; ++p)
+        vals[p] = silu_f(conv_window_pre<NTOK>(wqk, W, p));
+    if (csize > 1)
+        cluster_arrive_release();
+
+    // (4) V rows (exclusively owned: history rewritten at once), gates, Q/K L2
     if (tid < ROWS) {
-        const int c = 2 * a.Hq * kD + h * kD + row0 + tid;
-        float *hist_c = histb + (size_t)c * (W - 1);
-        const float *w_c = a.conv_w + (size_t)c * W;
 #pragma unroll
         for (int p = 0; p < NTOK; ++p)
-            sv[p * ROWS + tid] = silu_f(conv_pre<TIn>(hist_c, xb + c, a.x_stride, w_c, W, p));
+            sv[p * ROWS + tid] = silu_f(conv_window_pre<NTOK>(wv, W, p));
         float nh[kMaxW - 1];
         if (SNAP) {
-            conv_history_after<TIn>(hist_c, xb + c, a.x_stride, W, 1, nh);
-            store_history(a.conv_snap + ((size_t)b * cd + c) * (W - 1), W, nh);
+            conv_window_history<NTOK>(wv, W, 1, nh);
+            store_history(a.conv_snap + ((size_t)b * cd + c_v) * (W - 1), W, nh);
         }
-        conv_history_after<TIn>(hist_c, xb + c, a.x_stride, W, NTOK, nh);
-        store_history(hist_c, W, nh);
-    } else if (tid < ROWS + NTOK) {
+        conv_window_history<NTOK>(wv, W, NTOK, nh);
+        store_history(histb + (size_t)c_v * (W - 1), W, nh);
+    } else if (gate_thread) {
         const int p = tid - ROWS;
-        const int64_t row = tok0 + p;
-        const float g = decay_gate_f(load_act<TIn>(static_cast<const TIn *>(a.alpha) + row * a.gate_stride + h),
-                                     __ldg(a.dt + h), __ldg(a.A_log + h));
-        sdecay[p] = expf(g);
-        sbeta[p] = sigmoid_f(load_act<TIn>(static_cast<const TIn *>(a.beta_logit) + row * a.gate_stride + h));
+        sdecay[p] = expf(decay_gate_f(g_alpha, g_dt, g_alog));
+        sbeta[p] = sigmoid_f(g_bl);
+    }
+#pragma unroll
+    for (int p = 0; p < NTOK; ++p) {
+        const float inv = head_l2_inv(vals[p], a.l2_eps, &sred[p][is_k ? 4 : 0], warp & 3, lane);
+        (is_k ? sk : sq)[p * kD + (tid & (kD - 1))] = __fmul_rn(vals[p], inv);
     }
     __syncthreads();
 
-    // ---- recurrence over this CTA's rows, state read once and written once
-    step_rows<NG, NTOK, SNAP>(st, a.state + head_off + warp_off,
-                              SNAP ? a.state_snap + head_off + warp_off : nullptr, sk, sq, sv,
+    // (5) recurrence over this CTA's rows, in registers
+    step_rows<NG, NTOK, SNAP>(st, SNAP ? a.state_snap + head_off + warp_off : nullptr, sk, sq, sv,
                               ROWS, sdecay, sbeta, sy, warp * RPW, a.scale);
     __syncthreads();
 
-    // ---- gated RMSNorm: 32-row block partials, combined in block order
+    // (6) gated RMSNorm: 32-row block partials, combined in block order
     if (warp < NTOK * NBLK) {
         const int p = warp / NBLK, bl = warp % NBLK;
         const float s = norm_block_partial(sy[p * ROWS + bl * 32 + lane]);
         if (lane == 0)
             spart[p * NBLK + bl] = s;
     }
-    // One cluster barrier serves two purposes: every CTA of the cluster has
-    // finished reading the shared Q/K history (read in the first phase), and
-    // every CTA's norm partials are visible to its peers.
     cg::cluster_group cluster = cg::this_cluster();
-    if (csize > 1)
-        cluster.sync();
-    else
+    if (NSPLIT > 1) {
+        // phase 0 (history reads) has long completed; phase 1 publishes the partials
+        cluster_wait_acquire();
+        cluster_arrive_release();
+        cluster_wait_acquire();
+    } else {
         __syncthreads();
-
+    }
     if (tid < ROWS) {
 #pragma unroll
         for (int p = 0; p < NTOK; ++p) {
@@ -248,21 +279,29 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
             a.out[((size_t)row * a.Hv + h) * kD + j] = gated_out(sy[p * ROWS + tid], inv, __ldg(a.norm_w + j), zj);
         }
     }
+    if (NSPLIT > 1)
+        cluster_arrive_relaxed();   // this CTA no longer reads its peers' shared memory
 
-    // ---- Q / K history: each channel rewritten by exactly one CTA of the cluster
+    // (7) state rows back to HBM
+    store_rows<NG>(st, a.state + head_off + warp_off);
+
+    // (8) Q/K history: each channel rewritten by exactly one CTA of the cluster,
+    // after every CTA of the cluster has read it
+    if (csize > 1 && NSPLIT == 1)
+        cluster_wait_acquire();
     if (tid % csize == crank) {
         float *hist_c = histb + (size_t)c_qk * (W - 1);
         float nh[kMaxW - 1];
         if (SNAP) {
-            conv_history_after<TIn>(hist_c, xb + c_qk, a.x_stride, W, 1, nh);
+            conv_window_history<NTOK>(wqk, W, 1, nh);
             store_history(a.conv_snap + ((size_t)b * cd + c_qk) * (W - 1), W, nh);
         }
-        conv_history_after<TIn>(hist_c, xb + c_qk, a.x_stride, W, NTOK, nh);
+        conv_window_history<NTOK>(wqk, W, NTOK, nh);
         store_history(hist_c, W, nh);
     }
     // peers may still be reading this CTA's norm partials
     if (NSPLIT > 1)
-        cluster.sync();
+        cluster_wait_acquire();
 }
 
 // ------------------------------------------------------------------ commit
@@ -286,10 +325,14 @@ __global__ void __launch_bounds__(256) verify_commit_kernel(float *state, float 
 }
 
 // ------------------------------------------------------------------ host launchers
+#ifndef GDN_DECODE_TARGET_CTAS
+#define GDN_DECODE_TARGET_CTAS (4 * 152)
+#endif
+
 static int pick_nsplit(int B, int Hv, int r)
 {
     // Enough CTAs to keep every SM streaming, within an 8-CTA cluster.
-    const int target = 4 * 152;
+    const int target = GDN_DECODE_TARGET_CTAS;
     int ns = 1;
     while (ns < 4 && (int64_t)B * Hv * ns < target && r * ns * 2 <= 8)
         ns *= 2;

@@ -104,6 +104,61 @@ __device__ __forceinline__ void store_history(float *dst_c, int W, const float (
             dst_c[tau] = nh[tau];
 }
 
+// The same tap sum from a register window, for kernels that step NTOK tokens
+// of one channel: win[e] holds the channel's stream at index e - (W-1)
+// (history first, then the NTOK raw inputs), w[tau] its taps. Every load is
+// independent (one memory round trip), and the arithmetic order is conv_pre's.
+template <int NTOK>
+struct ConvWindow {
+    float win[kMaxW - 1 + NTOK];
+    float w[kMaxW];
+};
+
+template <typename TIn, int NTOK>
+__device__ __forceinline__ void conv_window_load(const float *hist_c, const TIn *x_c,
+                                                 int64_t x_stride, const float *w_c, int W,
+                                                 ConvWindow<NTOK> &cw)
+{
+#pragma unroll
+    for (int e = 0; e < kMaxW - 1 + NTOK; ++e) {
+        if (e < W - 1)
+            cw.win[e] = hist_c[e];
+        else if (e < W - 1 + NTOK)
+            cw.win[e] = load_act<TIn>(x_c + (int64_t)(e - (W - 1)) * x_stride);
+        else
+            cw.win[e] = 0.0f;
+    }
+#pragma unroll
+    for (int tau = 0; tau < kMaxW; ++tau)
+        cw.w[tau] = tau < W ? __ldg(w_c + tau) : 0.0f;
+}
+
+template <int NTOK>
+__device__ __forceinline__ float conv_window_pre(const ConvWindow<NTOK> &cw, int W, int p)
+{
+    float acc = __fmul_rn(cw.win[p], cw.w[0]);
+#pragma unroll
+    for (int tau = 1; tau < kMaxW; ++tau)
+        if (tau < W && p + tau < kMaxW - 1 + NTOK)
+            acc = __fmaf_rn(cw.win[p + tau], cw.w[tau], acc);
+    return acc;
+}
+
+// History after the first n tokens: win[n .. n+W-2].
+template <int NTOK>
+__device__ __forceinline__ void conv_window_history(const ConvWindow<NTOK> &cw, int W, int n,
+                                                    float (&nh)[kMaxW - 1])
+{
+#pragma unroll
+    for (int tau = 0; tau < kMaxW - 1; ++tau) {
+        nh[tau] = 0.0f;
+#pragma unroll
+        for (int nn = 0; nn <= NTOK; ++nn)
+            if (nn == n && tau < W - 1 && nn + tau < kMaxW - 1 + NTOK)
+                nh[tau] = cw.win[nn + tau];
+    }
+}
+
 // ------------------------------------------------------------------ reductions
 __device__ __forceinline__ float warp_sum32(float v)
 {
@@ -172,7 +227,8 @@ __device__ __forceinline__ float gated_out(float y, float inv, float w, float z)
 // products share one reduction.
 //
 // load_rows issues the warp's loads (callers issue them before their
-// prologue so the HBM latency overlaps it); step_rows consumes them:
+// prologue so the HBM latency overlaps it); step_rows advances them in
+// registers; store_rows writes them back:
 //   rows       first row of this warp's block in global memory (row stride kD)
 //   snap_rows  same rows in the snapshot buffer (used when SNAP)
 //   sk, sq     shared [NTOK][kD] normalised k, q
@@ -194,7 +250,7 @@ __device__ __forceinline__ void load_rows(const float *rows, float4 (&r)[NG][4])
 }
 
 template <int NG, int NTOK, bool SNAP>
-__device__ __forceinline__ void step_rows(float4 (&r)[NG][4], float *rows, float *snap_rows,
+__device__ __forceinline__ void step_rows(float4 (&r)[NG][4], float *snap_rows,
                                           const float *sk, const float *sq, const float *sv,
                                           int v_stride, const float *sdecay, const float *sbeta,
                                           float *sy, int local_row0, float scale)
@@ -263,6 +319,16 @@ __device__ __forceinline__ void step_rows(float4 (&r)[NG][4], float *rows, float
                     st_stream(snap_rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4, r[gi][m]);
         }
     }
+}
+
+// Write the advanced rows back (callers issue this late, after any cluster
+// barrier, so no release fence waits on these stores).
+template <int NG>
+__device__ __forceinline__ void store_rows(const float4 (&r)[NG][4], float *rows)
+{
+    const int lane = threadIdx.x & 31;
+    const int rg = lane >> 3;
+    const int sub = lane & 7;
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi)
 #pragma unroll
