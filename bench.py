@@ -431,6 +431,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--only", choices=["decode_b1", "verify_k2", "prefill"],
+                    help="run one secondary workload alone and print its figures (for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -439,6 +441,12 @@ def main(argv=None):
         return run_reference(args)
 
     world, rank, local = dist_env()
+    if args.only:
+        gpu = Gpu(local)
+        fn = {"decode_b1": lambda: gpu.decode_b1(), "verify_k2": lambda: gpu.verify_k2(args.steps, args.warmup),
+              "prefill": lambda: gpu.prefill(args.steps, args.warmup)}[args.only]
+        print(json.dumps({"workload": args.only, **fn()}), flush=True)
+        return 0
     dist = init_dist(world, "nccl")
     gpu = Gpu(local)
     shape = synth.WORKLOADS[HEADLINE]

@@ -253,8 +253,9 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
     if (!state || !conv_state || !x || !z || !alpha || !beta_logit || !out)
         return GDN_ERR_INVALID_ARG;
     const size_t es = act_size(act_dtype);
-    if (!aligned(state, 16) || !aligned(x, es) || !aligned(z, es) || !aligned(alpha, es) ||
-        !aligned(beta_logit, es) || !aligned(out, 16))
+    // the chunk kernel reads 8 channels of a token row per 16-byte load
+    if (!aligned(state, 16) || !aligned(x, 16) || (dims->x_stride * (int64_t)es) % 16 != 0 ||
+        !aligned(z, es) || !aligned(alpha, es) || !aligned(beta_logit, es) || !aligned(out, 16))
         return GDN_ERR_INVALID_ARG;
     if (chunk != 64)
         return GDN_ERR_UNSUPPORTED;

@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(PrefillArgs 
 // (or the older history when the call had fewer tokens). Runs after the chunk
 // kernel, which reads the old history.
 template <typename TIn>
-__global__ void __launch_bounds__(256) prefill_history_kernel(float *conv_state, const TIn *x,
+__global__ void __launch_bounds__(256) prefill_history_kernel_simt(float *conv_state, const TIn *x,
                                                               int64_t x_stride, int conv_dim, int W,
                                                               int T)
 {
@@ -427,16 +427,25 @@ cudaError_t prefill_typed(const PrefillArgs &a, cudaStream_t s)
     prefill_chunk_kernel<TIn><<<dim3(a.Hv, a.B, 1), kThreads, smem, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
-    prefill_history_kernel<TIn><<<dim3((a.conv_dim + 255) / 256, a.B, 1), 256, 0, s>>>(
+    prefill_history_kernel_simt<TIn><<<dim3((a.conv_dim + 255) / 256, a.B, 1), 256, 0, s>>>(
         a.conv_state, static_cast<const TIn *>(a.x), a.x_stride, a.conv_dim, a.W, a.T);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s)
+cudaError_t launch_prefill_simt(const PrefillArgs &a, bool bf16, cudaStream_t s)
 {
     return bf16 ? prefill_typed<__nv_bfloat16>(a, s) : prefill_typed<float>(a, s);
+}
+
+cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s)
+{
+#ifdef GDN_PREFILL_SIMT
+    return launch_prefill_simt(a, bf16, s);
+#else
+    return launch_prefill_tc(a, bf16, s);
+#endif
 }
 
 }  // namespace gdn

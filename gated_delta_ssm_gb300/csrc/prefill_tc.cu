@@ -1,0 +1,790 @@
+// prefill_tc.cu -- chunked prefill on the tcgen05 tensor cores.
+//
+// One CTA (8 warps) per (sequence, V head) walks the sequence in 64-token
+// chunks. Per chunk, with Gam the in-chunk cumulative decay, S_0 the entering
+// state in the plain orientation S[i][j] and the chunk algebra derived from the
+// recurrence of "fm_kernel_ssm.h" section "Delta-rule recurrence" (64-token
+// chunks with ceil(T/64) sequential links as in the "Mamba-2 SSD chunked
+// prefill scan" note of "ssm_mamba.rs"):
+//   G   = [Q; K] K^T                         tensor core   (QK^T and KK^T)
+//   P   = e^{Gam_t-Gam_s} (QK^T)[t][s], s<=t  CUDA cores
+//   A   = beta_t e^{Gam_t-Gam_s} (KK^T)[t][s], s<t;  T = (I + A)^{-1}  CUDA cores
+//   KS  = S_0^T [Q; K]^T                     tensor core   ((Q S_0)^T, (K S_0)^T)
+//   X^T = (beta V - beta e^{Gam} K S_0)^T     CUDA cores
+//   U^T = X^T T^T                            tensor core
+//   O^T = e^{Gam} (Q S_0)^T + U^T P^T        tensor core (accumulates onto KS)
+//   S^T <- e^{Gam_C} S^T + U^T (diag(e^{Gam_C-Gam}) K)   tensor core (state in TMEM)
+// then the gated RMSNorm of each token's O row. Every product is arranged
+// so that M = 128 (the value index j, or the stacked [Q; K] token index),
+// each TMEM lane holding one row of the result.
+//
+// Precision: operands are fp32 values split into bf16 parts. Every product on
+// the path to the readout (G, KS, U, O) splits its operands three ways
+// (x = x1 + x2 + x3, ~24 bits) and forms x1 y1 + x1 y2 + x2 y1 + x1 y3 +
+// x2 y2 + x3 y1: the readout of a token can be orders of magnitude smaller
+// than its terms (q_t . k_t and the sum over earlier tokens cancel), and the
+// gated RMSNorm rescales it to unit RMS, so it needs float32-class accuracy.
+// The state update alone uses two parts (x1 y1 + x1 y2 + x2 y1, ~16 bits),
+// enough for the 1e-4 state tolerance. Accumulation is fp32 in TMEM.
+//
+// Shared-memory operand tiles use the no-swizzle K-major core-matrix layout
+// of tc_ptx.cuh. The conv + SiLU + L2 and the gates of the chunk's tokens are
+// computed in the CTA from the raw inputs; the conv history is rewritten by
+// a second small kernel after every CTA has read it.
+#include "gdn_device.cuh"
+#include "gdn_kernels.h"
+#include "tc_ptx.cuh"
+
+namespace gdn {
+
+__device__ int g_device_error;   // set by a kernel whose bounded wait ran out
+
+namespace {
+
+constexpr int kC = 64;
+constexpr int kThreads = 256;
+
+// byte offsets in dynamic shared memory
+// Tiles whose live ranges do not overlap share space: the third parts of
+// [Q; K] and S^T are only read by the G and KS products, before T, P and
+// (e^{Gam_C-Gam} K)^T are written.
+constexpr uint32_t QK_HI = 0, QK_LO = 32768;        // [128 t'][128 i]  (Q rows, then K rows)
+constexpr uint32_t ST_HI = 65536, ST_LO = 98304;    // [128 j][128 i]   S^T
+constexpr uint32_t KT_HI = 131072, KT_LO = 147456;  // [128 i][64 t]    (e^{Gam_C-Gam} K)^T
+constexpr uint32_t ST_3 = 131072;                   // third part of S^T (in KT's space)
+constexpr uint32_t XU_HI = 163840, XU_LO = 180224;  // [128 j][64 t]    X^T, then U^T; V^T and O staging
+constexpr uint32_t TT_HI = 196608, TT_LO = 204800;  // [64 t][64 s]     T; A staging
+constexpr uint32_t PP_HI = 212992, PP_LO = 221184;  // [64 t][64 s]     P
+constexpr uint32_t QK_3 = 196608;                   // third part of [Q; K] (in TT and PP's space)
+// third parts of X^T/U^T, T and P, in the Q rows of [Q; K] (dead once G and KS are formed)
+constexpr uint32_t XU_3 = QK_HI, TT_3 = QK_LO, PP_3 = QK_LO + 8192;
+constexpr uint32_t SC_G = 229376, SC_BETA = SC_G + 256, SC_GAM = SC_BETA + 256,
+                   SC_GAML = SC_GAM + 256, SC_EG = SC_GAML + 256, SC_EGC = SC_EG + 256,
+                   SC_EGCC = SC_EGC + 256, SC_MBAR = SC_EGCC + 8, SC_TMEM = SC_MBAR + 32,
+                   SC_ERR = SC_TMEM + 4, SMEM_BYTES = SC_ERR + 4;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// TMEM columns
+constexpr uint32_t TM_G = 0, TM_KS = 64, TM_U = 192, TM_S = 256, TM_COLS = 512;
+constexpr int kWaitLimit = 1 << 26;
+
+__device__ __forceinline__ void split8(const float (&v)[8], uint4 &hi, uint4 &lo)
+{
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+        const float2 hf = __bfloat1622float2(hh);
+        const __nv_bfloat162 ll = __floats2bfloat162_rn(v[2 * e] - hf.x, v[2 * e + 1] - hf.y);
+        h[e] = *reinterpret_cast<const uint32_t *>(&hh);
+        l[e] = *reinterpret_cast<const uint32_t *>(&ll);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ void split8x3(const float (&v)[8], uint4 &p1, uint4 &p2, uint4 &p3)
+{
+    uint32_t a[4], b[4], c[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+        const float2 f1 = __bfloat1622float2(h1);
+        const float r0 = v[2 * e] - f1.x, r1 = v[2 * e + 1] - f1.y;
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(r0, r1);
+        const float2 f2 = __bfloat1622float2(h2);
+        const __nv_bfloat162 h3 = __floats2bfloat162_rn(r0 - f2.x, r1 - f2.y);
+        a[e] = *reinterpret_cast<const uint32_t *>(&h1);
+        b[e] = *reinterpret_cast<const uint32_t *>(&h2);
+        c[e] = *reinterpret_cast<const uint32_t *>(&h3);
+    }
+    p1 = make_uint4(a[0], a[1], a[2], a[3]);
+    p2 = make_uint4(b[0], b[1], b[2], b[3]);
+    p3 = make_uint4(c[0], c[1], c[2], c[3]);
+}
+
+__device__ __forceinline__ void split1x3(float v, __nv_bfloat16 &p1, __nv_bfloat16 &p2,
+                                         __nv_bfloat16 &p3)
+{
+    p1 = __float2bfloat16_rn(v);
+    const float r = v - __bfloat162float(p1);
+    p2 = __float2bfloat16_rn(r);
+    p3 = __float2bfloat16_rn(r - __bfloat162float(p2));
+}
+
+// Two-float arithmetic for the in-chunk cumulative decay Gam: its values reach
+// hundreds while the decays exp(Gam_t - Gam_s) need the differences to full
+// float precision, so Gam is carried as hi + lo (Knuth's TwoSum keeps the
+// rounding error of every addition).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ void two_add(float &h, float &l, float bh, float bl)
+{
+    float s, e;
+    two_sum(h, bh, s, e);
+    const float t = __fadd_rn(__fadd_rn(l, bl), e);
+    h = __fadd_rn(s, t);
+    l = __fsub_rn(t, __fsub_rn(h, s));
+}
+
+// exp((ah + al) - (bh + bl)) with the difference formed exactly before rounding
+__device__ __forceinline__ float exp_diff(float ah, float al, float bh, float bl)
+{
+    float dh, de;
+    two_sum(ah, -bh, dh, de);
+    const float dl = __fadd_rn(de, __fsub_rn(al, bl));
+    return __fmul_rn(expf(dh), __fadd_rn(1.0f, dl));
+}
+
+// 8 consecutive channels of one input row as floats (16-byte aligned rows).
+template <typename TIn>
+__device__ __forceinline__ void load8(const TIn *p, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[8])
+{
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        v[2 * e] = __uint_as_float(w[e] << 16);
+        v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float *p, float (&v)[8])
+{
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// conv + SiLU of 8 channels (cb .. cb+7) for 8 tokens (t0 .. t0+7 of the call);
+// tokens at or past T give 0.
+template <typename TIn>
+__device__ __forceinline__ void conv8x8(const PrefillArgs &a, int b, int cb, int t0,
+                                        float (&out)[8][8])
+{
+    const int W = a.W, T = a.T;
+    const TIn *xb = static_cast<const TIn *>(a.x) + (int64_t)b * T * a.x_stride + cb;
+    const float *hist = a.conv_state + ((size_t)b * a.conv_dim + cb) * (W - 1);
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            out[t][e] = 0.0f;
+    for (int tau = 0; tau < W; ++tau) {
+        float w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            w[e] = __ldg(a.conv_w + (size_t)(cb + e) * W + tau);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int s = t0 + t - (W - 1) + tau;    // stream index of this tap
+            float v[8];
+            if (s >= 0 && s < T) {
+                load8<TIn>(xb + (int64_t)s * a.x_stride, v);
+            } else if (s < 0) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    v[e] = hist[(size_t)e * (W - 1) + (W - 1 + s)];
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    v[e] = 0.0f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                out[t][e] = __fmaf_rn(v[e], w[e], out[t][e]);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            out[t][e] = t0 + t < T ? silu_f(out[t][e]) : 0.0f;
+}
+
+// One column c of T = (I + A)^{-1} (unit lower triangular) by forward
+// substitution, T[t][c] = [t == c] - sum_{s<t} A[t][s] T[s][c], one thread per
+// column. A is read from the fp32 staging rows (16 float4 chunks per row,
+// XOR-swizzled by the row index so that the row writes are conflict-free).
+__device__ __forceinline__ void tri_inverse_column(const uint8_t *smem, int c, float (&Tc)[kC])
+{
+#pragma unroll
+    for (int t = 0; t < kC; ++t) {
+        const float *row = reinterpret_cast<const float *>(smem + TT_HI + t * 256);
+        float acc0 = 0.0f, acc1 = 0.0f;
+#pragma unroll
+        for (int s = 0; s < t; ++s) {
+            const float av = row[(((s >> 2) ^ (t & 15)) << 2) + (s & 3)];
+            if (s & 1)
+                acc1 = __fmaf_rn(av, Tc[s], acc1);
+            else
+                acc0 = __fmaf_rn(av, Tc[s], acc0);
+        }
+        Tc[t] = (t == c ? 1.0f : 0.0f) - (acc0 + acc1);
+    }
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.y, h = blockIdx.x;
+    const int hk = h / (a.Hv / a.Hq);
+    const int T = a.T;
+    const uint32_t sbase = tc::smem_addr(smem);
+    float *sg = reinterpret_cast<float *>(smem + SC_G);
+    float *sbeta = reinterpret_cast<float *>(smem + SC_BETA);
+    float *sgam = reinterpret_cast<float *>(smem + SC_GAM);     // Gam, high part
+    float *sgaml = reinterpret_cast<float *>(smem + SC_GAML);   // Gam, low part
+    float *seg = reinterpret_cast<float *>(smem + SC_EG);
+    float *segc = reinterpret_cast<float *>(smem + SC_EGC);
+    float *segC = reinterpret_cast<float *>(smem + SC_EGCC);
+    int *serr = reinterpret_cast<int *>(smem + SC_ERR);
+    const uint32_t mbar = sbase + SC_MBAR;   // four barriers, 8 bytes apart
+    float *state_h = a.state + ((size_t)b * a.Hv + h) * kD * kD;
+
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i)
+            tc::mbar_init(mbar + 8 * i, 1);
+        *serr = 0;
+    }
+    if (warp == 0)
+        tc::tmem_alloc(sbase + SC_TMEM, TM_COLS);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<const uint32_t *>(smem + SC_TMEM);
+    const uint32_t lane_q = (uint32_t)(32 * (warp & 3)) << 16;    // this warp's TMEM lane quarter
+    const int jrow = 32 * (warp & 3) + lane;                       // TMEM lane = row index
+
+    // ---- entering state: S^T rows into TMEM (fp32 master) and the bf16 hi/lo tile
+    if (warp < 4) {
+        const float *src = state_h + (size_t)jrow * kD;
+#pragma unroll 1
+        for (int c = 0; c < kD; c += 16) {
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const float4 f = __ldg(reinterpret_cast<const float4 *>(src + c + e));
+                v[e] = f.x; v[e + 1] = f.y; v[e + 2] = f.z; v[e + 3] = f.w;
+            }
+            tc::tmem_st16(tmem + lane_q + TM_S + c, v);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float w8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    w8[e] = v[8 * half + e];
+                uint4 p1, p2, p3;
+                split8x3(w8, p1, p2, p3);
+                const uint32_t off = tc::km_offset(jrow, c + 8 * half, kD);
+                *reinterpret_cast<uint4 *>(smem + ST_HI + off) = p1;
+                *reinterpret_cast<uint4 *>(smem + ST_LO + off) = p2;
+                *reinterpret_cast<uint4 *>(smem + ST_3 + off) = p3;
+            }
+        }
+    }
+
+    const float dtv = __ldg(a.dt + h), alog = __ldg(a.A_log + h);
+    const TIn *alb = static_cast<const TIn *>(a.alpha) + (int64_t)b * T * a.gate_stride + h;
+    const TIn *blb = static_cast<const TIn *>(a.beta_logit) + (int64_t)b * T * a.gate_stride + h;
+    const uint32_t id_g = tc::idesc_bf16(128, 64), id_128 = tc::idesc_bf16(128, 128);
+    int chunk = 0;
+
+    for (int c0 = 0; c0 < T; c0 += kC, ++chunk) {
+        const int n = min(kC, T - c0);
+        const uint32_t par = chunk & 1;
+
+        // ---- gates and in-chunk cumulative decay (warp 7)
+        if (warp == 7) {
+            float gv[2], bv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = 2 * lane + u;
+                gv[u] = bv[u] = 0.0f;
+                if (t < n) {
+                    const int64_t row = c0 + t;
+                    gv[u] = decay_gate_f(load_act<TIn>(alb + row * a.gate_stride), dtv, alog);
+                    bv[u] = sigmoid_f(load_act<TIn>(blb + row * a.gate_stride));
+                }
+                sg[t] = gv[u];
+                sbeta[t] = bv[u];
+            }
+            // inclusive scan of the token pairs in two-float arithmetic
+            float ph, pl;
+            two_sum(gv[0], gv[1], ph, pl);
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float yh = __shfl_up_sync(0xffffffffu, ph, off);
+                const float yl = __shfl_up_sync(0xffffffffu, pl, off);
+                if (lane >= off)
+                    two_add(ph, pl, yh, yl);
+            }
+            float exh = __shfl_up_sync(0xffffffffu, ph, 1);
+            float exl = __shfl_up_sync(0xffffffffu, pl, 1);
+            if (lane == 0)
+                exh = exl = 0.0f;
+            float g0h = exh, g0l = exl;
+            two_add(g0h, g0l, gv[0], 0.0f);
+            float g1h = g0h, g1l = g0l;
+            two_add(g1h, g1l, gv[1], 0.0f);
+            const float gch = __shfl_sync(0xffffffffu, g1h, 31);
+            const float gcl = __shfl_sync(0xffffffffu, g1l, 31);
+            sgam[2 * lane] = g0h;
+            sgaml[2 * lane] = g0l;
+            sgam[2 * lane + 1] = g1h;
+            sgaml[2 * lane + 1] = g1l;
+            seg[2 * lane] = exp_diff(g0h, g0l, 0.0f, 0.0f);
+            seg[2 * lane + 1] = exp_diff(g1h, g1l, 0.0f, 0.0f);
+            segc[2 * lane] = 2 * lane < n ? exp_diff(gch, gcl, g0h, g0l) : 0.0f;
+            segc[2 * lane + 1] = 2 * lane + 1 < n ? exp_diff(gch, gcl, g1h, g1l) : 0.0f;
+            if (lane == 0)
+                *segC = exp_diff(gch, gcl, 0.0f, 0.0f);
+        }
+        __syncthreads();
+
+        // ---- Q and K rows: conv + SiLU + L2 -> [Q; K] tile, and (e^{Gam_C-Gam} K)^T tile
+        {
+            const int part = warp >> 2;                         // 0: Q, 1: K
+            const int t0 = 16 * (warp & 3) + 8 * (lane >> 4);   // first token (in chunk)
+            const int grp = lane & 15;                          // 8-channel group of the head
+            const int cb = (part ? a.Hq * kD : 0) + hk * kD + 8 * grp;
+            float v[8][8];
+            conv8x8<TIn>(a, b, cb, c0 + t0, v);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                float ss = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    ss = __fmaf_rn(v[t][e], v[t][e], ss);
+#pragma unroll
+                for (int m = 1; m < 16; m <<= 1)
+                    ss += __shfl_xor_sync(0xffffffffu, ss, m);
+                const float inv = t0 + t < n ? rsqrtf(ss + a.l2_eps) : 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    v[t][e] *= inv;
+                uint4 p1, p2, p3;
+                split8x3(v[t], p1, p2, p3);
+                const uint32_t off = tc::km_offset(part * kC + t0 + t, 8 * grp, kD);
+                *reinterpret_cast<uint4 *>(smem + QK_HI + off) = p1;
+                *reinterpret_cast<uint4 *>(smem + QK_LO + off) = p2;
+                *reinterpret_cast<uint4 *>(smem + QK_3 + off) = p3;
+            }
+        }
+        // ---- V rows: conv + SiLU -> fp32 V^T staged in each value row's X^T footprint
+        if (warp < 4) {
+            const int t0 = 16 * warp + 8 * (lane >> 4);
+            const int grp = lane & 15;
+            const int cb = 2 * a.Hq * kD + h * kD + 8 * grp;
+            float v[8][8];
+            conv8x8<TIn>(a, b, cb, c0 + t0, v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j = 8 * grp + e;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int chunk4 = t0 / 4 + q;     // float4 chunk of the row (0..15)
+                    const uint32_t off = (chunk4 < 8 ? XU_HI : XU_LO) + (j >> 3) * 1024 +
+                                         (chunk4 & 7) * 128 + (j & 7) * 16;
+                    *reinterpret_cast<float4 *>(smem + off) =
+                        make_float4(v[4 * q][e], v[4 * q + 1][e], v[4 * q + 2][e], v[4 * q + 3][e]);
+                }
+            }
+        }
+        tc::fence_smem_to_async();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+
+        // ---- G = [Q; K] K^T and KS = S^T [Q; K]^T on the tensor core
+        if (tid == 0) {
+#pragma unroll 1
+            for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint32_t ko = kk * 256;
+                const uint64_t a1 = tc::sdesc(sbase + QK_HI + ko, 128, 2048);
+                const uint64_t a2 = tc::sdesc(sbase + QK_LO + ko, 128, 2048);
+                const uint64_t a3 = tc::sdesc(sbase + QK_3 + ko, 128, 2048);
+                const uint64_t b1 = tc::sdesc(sbase + QK_HI + 16384 + ko, 128, 2048);
+                const uint64_t b2 = tc::sdesc(sbase + QK_LO + 16384 + ko, 128, 2048);
+                const uint64_t b3 = tc::sdesc(sbase + QK_3 + 16384 + ko, 128, 2048);
+                tc::mma_bf16(tmem + TM_G, a1, b1, id_g, kk > 0);
+                tc::mma_bf16(tmem + TM_G, a1, b2, id_g, 1);
+                tc::mma_bf16(tmem + TM_G, a2, b1, id_g, 1);
+                tc::mma_bf16(tmem + TM_G, a1, b3, id_g, 1);
+                tc::mma_bf16(tmem + TM_G, a2, b2, id_g, 1);
+                tc::mma_bf16(tmem + TM_G, a3, b1, id_g, 1);
+            }
+            tc::mma_commit(mbar + 0);
+#pragma unroll 1
+            for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint32_t ko = kk * 256;
+                const uint64_t a1 = tc::sdesc(sbase + ST_HI + ko, 128, 2048);
+                const uint64_t a2 = tc::sdesc(sbase + ST_LO + ko, 128, 2048);
+                const uint64_t a3 = tc::sdesc(sbase + ST_3 + ko, 128, 2048);
+                const uint64_t b1 = tc::sdesc(sbase + QK_HI + ko, 128, 2048);
+                const uint64_t b2 = tc::sdesc(sbase + QK_LO + ko, 128, 2048);
+                const uint64_t b3 = tc::sdesc(sbase + QK_3 + ko, 128, 2048);
+                tc::mma_bf16(tmem + TM_KS, a1, b1, id_128, kk > 0);
+                tc::mma_bf16(tmem + TM_KS, a1, b2, id_128, 1);
+                tc::mma_bf16(tmem + TM_KS, a2, b1, id_128, 1);
+                tc::mma_bf16(tmem + TM_KS, a1, b3, id_128, 1);
+                tc::mma_bf16(tmem + TM_KS, a2, b2, id_128, 1);
+                tc::mma_bf16(tmem + TM_KS, a3, b1, id_128, 1);
+            }
+            tc::mma_commit(mbar + 8);
+        }
+
+        // ---- P and A from G (both products must be done: their third parts share
+        // the space P, T and (e^{Gam_C-Gam} K)^T are written to)
+        if (!tc::mbar_wait(mbar + 0, par, kWaitLimit))
+            atomicOr(serr, 1);
+        if (!tc::mbar_wait(mbar + 8, par, kWaitLimit))
+            atomicOr(serr, 2);
+        tc::fence_after_sync();
+        if (warp < 4) {
+            const int t = jrow & (kC - 1);
+            const bool krow = jrow >= kC;
+            const float gt = sgam[t], gtl = sgaml[t];
+            const float bt = sbeta[t];
+#pragma unroll 1
+            for (int c = 0; c < kC; c += 16) {
+                float gv[16];
+                tc::tmem_ld16(tmem + lane_q + TM_G + c, gv);
+                float o[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int s = c + e;
+                    const bool keep = t < n && (krow ? s < t : s <= t);
+                    const float dec = keep ? exp_diff(gt, gtl, sgam[s], sgaml[s]) : 0.0f;
+                    o[e] = krow ? bt * dec * gv[e] : dec * gv[e];
+                }
+                if (krow) {
+                    // A, fp32, rows of 16 float4 chunks XOR-swizzled by the row index
+                    float *row = reinterpret_cast<float *>(smem + TT_HI + t * 256);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<float4 *>(row + ((((c >> 2) + q) ^ (t & 15)) << 2)) =
+                            make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                } else {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        float w8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            w8[e] = o[8 * half + e];
+                        uint4 p1, p2, p3;
+                        split8x3(w8, p1, p2, p3);
+                        const uint32_t off = tc::km_offset(t, c + 8 * half, kC);
+                        *reinterpret_cast<uint4 *>(smem + PP_HI + off) = p1;
+                        *reinterpret_cast<uint4 *>(smem + PP_LO + off) = p2;
+                        *reinterpret_cast<uint4 *>(smem + PP_3 + off) = p3;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+
+        if (warp >= 4) {
+            // ---- T = (I + A)^{-1}: warps 4-5, one thread per column
+            float Tc[kC];
+            const int c = tid - 128;
+            if (warp < 6) {
+                tri_inverse_column(smem, c, Tc);
+            } else {
+                // (e^{Gam_C-Gam} K)^T from the first two parts of the K rows: two key rows i per thread
+#pragma unroll 1
+                for (int i = c - 64; i < kD; i += 64) {
+#pragma unroll
+                    for (int t0 = 0; t0 < kC; t0 += 8) {
+                        float col[8];
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) {
+                            const uint32_t off = tc::km_offset(kC + t0 + t, i, kD);
+                            const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + QK_HI + off)) +
+                                             __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + QK_LO + off));
+                            col[t] = kv * segc[t0 + t];
+                        }
+                        uint4 hi, lo;
+                        split8(col, hi, lo);
+                        const uint32_t off = tc::km_offset(i, t0, kC);
+                        *reinterpret_cast<uint4 *>(smem + KT_HI + off) = hi;
+                        *reinterpret_cast<uint4 *>(smem + KT_LO + off) = lo;
+                    }
+                }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");   // every read of A is done
+            if (warp < 6) {
+#pragma unroll
+                for (int t = 0; t < kC; ++t) {
+                    __nv_bfloat16 p1, p2, p3;
+                    split1x3(Tc[t], p1, p2, p3);
+                    const uint32_t off = tc::km_offset(t, c, kC);
+                    *reinterpret_cast<__nv_bfloat16 *>(smem + TT_HI + off) = p1;
+                    *reinterpret_cast<__nv_bfloat16 *>(smem + TT_LO + off) = p2;
+                    *reinterpret_cast<__nv_bfloat16 *>(smem + TT_3 + off) = p3;
+                }
+            }
+            // ---- state accumulator scaled by e^{Gam_C} ahead of this chunk's update
+            const float egC = *segC;
+#pragma unroll 1
+            for (int c2 = 0; c2 < kD; c2 += 16) {
+                float sv[16];
+                tc::tmem_ld16(tmem + lane_q + TM_S + c2, sv);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    sv[e] *= egC;
+                tc::tmem_st16(tmem + lane_q + TM_S + c2, sv);
+            }
+        } else {
+            // ---- (Q S_0)^T scaled by e^{Gam}; X^T = beta V^T - beta e^{Gam} (K S_0)^T
+#pragma unroll 1
+            for (int c = 0; c < kC; c += 16) {
+                float qv[16];
+                tc::tmem_ld16(tmem + lane_q + TM_KS + c, qv);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    qv[e] *= seg[c + e];
+                tc::tmem_st16(tmem + lane_q + TM_KS + c, qv);
+            }
+            float vt[kC];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const uint32_t off = (q < 8 ? XU_HI : XU_LO) + (jrow >> 3) * 1024 + (q & 7) * 128 +
+                                     (jrow & 7) * 16;
+                const float4 f = *reinterpret_cast<const float4 *>(smem + off);
+                vt[4 * q] = f.x; vt[4 * q + 1] = f.y; vt[4 * q + 2] = f.z; vt[4 * q + 3] = f.w;
+            }
+#pragma unroll
+            for (int c = 0; c < kC; c += 16) {
+                float kv[16];
+                tc::tmem_ld16(tmem + lane_q + TM_KS + kC + c, kv);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float x8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int t = c + 8 * half + e;
+                        const float bt = sbeta[t];
+                        x8[e] = bt * vt[t] - bt * seg[t] * kv[8 * half + e];
+                    }
+                    uint4 p1, p2, p3;
+                    split8x3(x8, p1, p2, p3);
+                    const uint32_t off = tc::km_offset(jrow, c + 8 * half, kC);
+                    *reinterpret_cast<uint4 *>(smem + XU_HI + off) = p1;
+                    *reinterpret_cast<uint4 *>(smem + XU_LO + off) = p2;
+                    *reinterpret_cast<uint4 *>(smem + XU_3 + off) = p3;
+                }
+            }
+        }
+        tc::fence_smem_to_async();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+
+        // ---- U^T = X^T T^T
+        if (tid == 0) {
+#pragma unroll 1
+            for (int kk = 0; kk < kC / 16; ++kk) {
+                const uint32_t ko = kk * 256;
+                const uint64_t a1 = tc::sdesc(sbase + XU_HI + ko, 128, 1024);
+                const uint64_t a2 = tc::sdesc(sbase + XU_LO + ko, 128, 1024);
+                const uint64_t a3 = tc::sdesc(sbase + XU_3 + ko, 128, 1024);
+                const uint64_t b1 = tc::sdesc(sbase + TT_HI + ko, 128, 1024);
+                const uint64_t b2 = tc::sdesc(sbase + TT_LO + ko, 128, 1024);
+                const uint64_t b3 = tc::sdesc(sbase + TT_3 + ko, 128, 1024);
+                tc::mma_bf16(tmem + TM_U, a1, b1, id_g, kk > 0);
+                tc::mma_bf16(tmem + TM_U, a1, b2, id_g, 1);
+                tc::mma_bf16(tmem + TM_U, a2, b1, id_g, 1);
+                tc::mma_bf16(tmem + TM_U, a1, b3, id_g, 1);
+                tc::mma_bf16(tmem + TM_U, a2, b2, id_g, 1);
+                tc::mma_bf16(tmem + TM_U, a3, b1, id_g, 1);
+            }
+            tc::mma_commit(mbar + 16);
+        }
+        if (!tc::mbar_wait(mbar + 16, par, kWaitLimit))
+            atomicOr(serr, 4);
+        tc::fence_after_sync();
+        if (warp < 4) {
+#pragma unroll 1
+            for (int c = 0; c < kC; c += 16) {
+                float uv[16];
+                tc::tmem_ld16(tmem + lane_q + TM_U + c, uv);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float u8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        u8[e] = uv[8 * half + e];
+                    uint4 p1, p2, p3;
+                    split8x3(u8, p1, p2, p3);
+                    const uint32_t off = tc::km_offset(jrow, c + 8 * half, kC);
+                    *reinterpret_cast<uint4 *>(smem + XU_HI + off) = p1;
+                    *reinterpret_cast<uint4 *>(smem + XU_LO + off) = p2;
+                    *reinterpret_cast<uint4 *>(smem + XU_3 + off) = p3;
+                }
+            }
+        }
+        tc::fence_smem_to_async();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+
+        // ---- O^T += U^T P^T;  S^T += U^T (e^{Gam_C-Gam} K)
+        if (tid == 0) {
+#pragma unroll 1
+            for (int kk = 0; kk < kC / 16; ++kk) {
+                const uint32_t ko = kk * 256;
+                const uint64_t ah = tc::sdesc(sbase + XU_HI + ko, 128, 1024);
+                const uint64_t al = tc::sdesc(sbase + XU_LO + ko, 128, 1024);
+                const uint64_t a3 = tc::sdesc(sbase + XU_3 + ko, 128, 1024);
+                const uint64_t ph = tc::sdesc(sbase + PP_HI + ko, 128, 1024);
+                const uint64_t pl = tc::sdesc(sbase + PP_LO + ko, 128, 1024);
+                const uint64_t p3 = tc::sdesc(sbase + PP_3 + ko, 128, 1024);
+                const uint64_t kh = tc::sdesc(sbase + KT_HI + ko, 128, 1024);
+                const uint64_t kl = tc::sdesc(sbase + KT_LO + ko, 128, 1024);
+                tc::mma_bf16(tmem + TM_KS, ah, ph, id_g, 1);
+                tc::mma_bf16(tmem + TM_KS, ah, pl, id_g, 1);
+                tc::mma_bf16(tmem + TM_KS, al, ph, id_g, 1);
+                tc::mma_bf16(tmem + TM_KS, ah, p3, id_g, 1);
+                tc::mma_bf16(tmem + TM_KS, al, pl, id_g, 1);
+                tc::mma_bf16(tmem + TM_KS, a3, ph, id_g, 1);
+                tc::mma_bf16(tmem + TM_S, ah, kh, id_128, 1);
+                tc::mma_bf16(tmem + TM_S, ah, kl, id_128, 1);
+                tc::mma_bf16(tmem + TM_S, al, kh, id_128, 1);
+            }
+            tc::mma_commit(mbar + 24);
+        }
+        if (!tc::mbar_wait(mbar + 24, par, kWaitLimit))
+            atomicOr(serr, 8);
+        tc::fence_after_sync();
+        if (warp < 4) {
+            // O (fp32, [t][j]) into the XU region for the row-wise norm
+            float *O = reinterpret_cast<float *>(smem + XU_HI);
+#pragma unroll 1
+            for (int c = 0; c < kC; c += 16) {
+                float ov[16];
+                tc::tmem_ld16(tmem + lane_q + TM_KS + c, ov);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    O[(c + e) * kD + jrow] = ov[e];
+            }
+        } else {
+            // next chunk's S^T operand (three parts) from the updated state
+#pragma unroll 1
+            for (int c = 0; c < kD; c += 16) {
+                float sv[16];
+                tc::tmem_ld16(tmem + lane_q + TM_S + c, sv);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float s8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        s8[e] = sv[8 * half + e];
+                    uint4 p1, p2, p3;
+                    split8x3(s8, p1, p2, p3);
+                    const uint32_t off = tc::km_offset(jrow, c + 8 * half, kD);
+                    *reinterpret_cast<uint4 *>(smem + ST_HI + off) = p1;
+                    *reinterpret_cast<uint4 *>(smem + ST_LO + off) = p2;
+                    *reinterpret_cast<uint4 *>(smem + ST_3 + off) = p3;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- gated RMSNorm of each token's output row
+        {
+            const float *O = reinterpret_cast<const float *>(smem + XU_HI);
+            const TIn *zb = static_cast<const TIn *>(a.z) + (int64_t)b * T * a.z_stride + (int64_t)h * kD;
+            for (int t = warp; t < n; t += 8) {
+                float yv[4], bp[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    yv[m] = O[t * kD + 32 * m + lane] * a.scale;
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    bp[m] = norm_block_partial(yv[m]);
+                const float inv = norm_inv(bp[0], bp[1], bp[2], bp[3], a.rms_eps);
+                const int64_t row = (int64_t)c0 + t;
+                const TIn *zr = zb + row * a.z_stride;
+                float *outr = a.out + (((size_t)b * T + row) * a.Hv + h) * kD;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int j = 32 * m + lane;
+                    outr[j] = gated_out(yv[m], inv, __ldg(a.norm_w + j), load_act<TIn>(zr + j));
+                }
+            }
+        }
+        __syncthreads();
+        if (*serr)
+            break;
+    }
+
+    // ---- final state back to HBM (S^T rows = the library layout)
+    tc::fence_after_sync();
+    if (warp < 4 && *serr == 0) {
+        float *dst = state_h + (size_t)jrow * kD;
+#pragma unroll 1
+        for (int c = 0; c < kD; c += 16) {
+            float v[16];
+            tc::tmem_ld16(tmem + lane_q + TM_S + c, v);
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4 *>(dst + c + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+    }
+    if (tid == 0 && *serr)
+        atomicOr(&g_device_error, *serr);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0)
+        tc::tmem_dealloc(tmem, TM_COLS);
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(256) prefill_history_kernel(float *conv_state, const TIn *x,
+                                                              int64_t x_stride, int conv_dim, int W,
+                                                              int T)
+{
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    const int b = blockIdx.y;
+    if (c >= conv_dim)
+        return;
+    float *hist_c = conv_state + ((size_t)b * conv_dim + c) * (W - 1);
+    float nh[kMaxW - 1];
+    conv_history_after<TIn>(hist_c, x + (int64_t)b * T * x_stride + c, x_stride, W, T, nh);
+    store_history(hist_c, W, nh);
+}
+
+template <typename TIn>
+cudaError_t prefill_typed(const PrefillArgs &a, cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<TIn>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess)
+        return e;
+    prefill_tc_kernel<TIn><<<dim3(a.Hv, a.B, 1), kThreads, SMEM_BYTES, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    prefill_history_kernel<TIn><<<dim3((a.conv_dim + 255) / 256, a.B, 1), 256, 0, s>>>(
+        a.conv_state, static_cast<const TIn *>(a.x), a.x_stride, a.conv_dim, a.W, a.T);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, bool bf16, cudaStream_t s)
+{
+    return bf16 ? prefill_typed<__nv_bfloat16>(a, s) : prefill_typed<float>(a, s);
+}
+
+}  // namespace gdn

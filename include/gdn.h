@@ -217,9 +217,11 @@ gdn_status gdn_verify_commit(float *state, float *conv_state, const float *state
  *   state, conv_state updated in place (state after the last token);
  *   x, z, alpha, beta_logit as in LAYOUTS with T = n_tokens;
  *   out float [B][n_tokens][Hv][d].
- * chunk must be 64. Agrees with the sequential scan within float32 rounding,
- * not bit for bit.
- * Errors: INVALID_ARG (null, n_tokens < 1, bad dims), UNSUPPORTED (d, W, chunk != 64).
+ * chunk must be 64. x must be 16-byte aligned with rows a multiple of 16 bytes
+ * apart (x_stride * element size). Agrees with the sequential scan within
+ * float32 rounding, not bit for bit.
+ * Errors: INVALID_ARG (null, n_tokens < 1, bad dims, x alignment), UNSUPPORTED
+ * (d, W, chunk != 64).
  */
 gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, const void *z,
                                const void *alpha, const void *beta_logit, gdn_dtype act_dtype,

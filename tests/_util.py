@@ -70,6 +70,20 @@ def run_oracle(shape: synth.Shape, inp: dict, T=None, seqs=None, **kw):
                         inp["hist"], Hq=shape.Hq, W=shape.W, seqs=seqs, **kw)
 
 
+def out_rel(x, ref):
+    """Normwise relative error of layer outputs, one slice per (sequence, V head):
+    max over slices of max|x - ref| / max|ref| over that head's tokens and
+    channels. Outputs are [B][T][Hv][d] or [B][Hv][d] (one token)."""
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if x.ndim == 3:
+        x, ref = x[:, None], ref[:, None]
+    num = np.abs(x - ref).max(axis=(1, 3))
+    den = np.abs(ref).max(axis=(1, 3))
+    den = np.where(den == 0, 1.0, den)
+    return float((num / den).max())
+
+
 def max_rel(x, ref, slice_axes: int):
     """Normwise relative error: max over slices (the trailing `slice_axes` axes form one
     slice) of max|x - ref| / max|ref| within the slice."""

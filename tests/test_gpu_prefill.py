@@ -3,7 +3,8 @@ import numpy as np
 import pytest
 
 from gated_delta_ssm_gb300 import synth
-from tests._util import OUT_TOL, STATE_TOL, device_inputs, dims_of, max_rel, params_of, run_oracle
+from tests._util import (OUT_TOL, STATE_TOL, device_inputs, dims_of, max_rel, out_rel, params_of,
+                         run_oracle)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +34,7 @@ def test_prefill_ragged_lengths_match_oracle(T, warm):
     ref = run_oracle(shape, inp)
     dev = device_inputs(shape, inp)
     out = _prefill(shape, dev).cpu().numpy()
-    assert max_rel(out, ref["out"], 1) <= OUT_TOL
+    assert out_rel(out, ref["out"]) <= OUT_TOL
     assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= PREFILL_STATE_TOL
     assert np.array_equal(dev["hist"].cpu().numpy(), ref["hist"].astype(np.float32))
 
@@ -45,7 +46,7 @@ def test_prefill_edge_shapes(W, Hq, Hv):
     ref = run_oracle(shape, inp)
     dev = device_inputs(shape, inp)
     out = _prefill(shape, dev).cpu().numpy()
-    assert max_rel(out, ref["out"], 1) <= OUT_TOL
+    assert out_rel(out, ref["out"]) <= OUT_TOL
     assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= PREFILL_STATE_TOL
     assert np.array_equal(dev["hist"].cpu().numpy(), ref["hist"].astype(np.float32))
 
@@ -56,7 +57,7 @@ def test_prefill_fp32_activations():
     ref = run_oracle(shape, inp)
     dev = device_inputs(shape, inp)
     out = _prefill(shape, dev).cpu().numpy()
-    assert max_rel(out, ref["out"], 1) <= OUT_TOL
+    assert out_rel(out, ref["out"]) <= OUT_TOL
     assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= PREFILL_STATE_TOL
 
 
@@ -76,8 +77,8 @@ def test_prefill_then_decode_continues_the_sequence():
     gdn.decode_step(dev["state"], dev["hist"], last["x"], last["z"], last["alpha"],
                     last["beta_logit"], params_of(dev), step, dims_of(shape))
     torch.cuda.synchronize()
-    assert max_rel(out.cpu().numpy(), ref["out"][:, :T], 1) <= OUT_TOL
-    assert max_rel(step.cpu().numpy(), ref["out"][:, T], 1) <= OUT_TOL
+    assert out_rel(out.cpu().numpy(), ref["out"][:, :T]) <= OUT_TOL
+    assert out_rel(step.cpu().numpy(), ref["out"][:, T]) <= OUT_TOL
     assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= PREFILL_STATE_TOL
     assert np.array_equal(dev["hist"].cpu().numpy(), ref["hist"].astype(np.float32))
 
@@ -91,7 +92,7 @@ def test_prefill_full_size_4x8192():
     out = _prefill(shape, dev)
     ref = run_oracle(shape, inp)
     o = out.cpu().numpy()
-    assert max_rel(o[:, :512], ref["out"][:, :512], 1) <= OUT_TOL
-    assert max_rel(o[:, -64:], ref["out"][:, -64:], 1) <= OUT_TOL
+    assert out_rel(o[:, :512], ref["out"][:, :512]) <= OUT_TOL
+    assert out_rel(o[:, -64:], ref["out"][:, -64:]) <= OUT_TOL
     assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= PREFILL_STATE_TOL
     assert np.array_equal(dev["hist"].cpu().numpy(), ref["hist"].astype(np.float32))
