@@ -19,7 +19,7 @@ import threading as _th
 __all__ = [
     "Dims", "Params", "GdnError", "load", "library_path",
     "decay_gate", "conv_update", "recurrence_decode", "gated_norm",
-    "decode_step", "verify_k2", "verify_commit", "prefill_chunked", "version",
+    "decode_step", "verify_k2", "verify_commit", "prefill_chunked", "check_device", "version",
 ]
 
 _PKG = _os.path.dirname(_os.path.abspath(__file__))
@@ -27,14 +27,15 @@ _LIB_PATH = _os.path.join(_PKG, "libgdn.so")
 _lib = None
 _lock = _th.Lock()
 
-GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE = 0, 1, 2, 3, 4
 GDN_F32, GDN_BF16 = 0, 1
 
 
 class GdnError(RuntimeError):
     def __init__(self, status: int, fn: str, detail: str = ""):
         self.status = status
-        names = {1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_CUDA"}
+        names = {1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_CUDA",
+                 4: "GDN_ERR_DEVICE"}
         super().__init__(f"{fn}: {names.get(status, status)}" + (f" ({detail})" if detail else ""))
 
 
@@ -119,10 +120,21 @@ def load():
         for name in ("gdn_last_cuda_error", "gdn_version"):
             getattr(L, name).restype = _ct.c_char_p
             getattr(L, name).argtypes = []
+        L.gdn_check_device.restype = _ct.c_int
+        L.gdn_check_device.argtypes = [_ct.POINTER(_ct.c_int32)]
         L.gdn_status_string.restype = _ct.c_char_p
         L.gdn_status_string.argtypes = [_ct.c_int]
         _lib = L
     return _lib
+
+
+def check_device() -> int:
+    """Synchronise, then read and clear the device-side error word (0 = no kernel gave up a wait)."""
+    code = _ct.c_int32(0)
+    st = load().gdn_check_device(_ct.byref(code))
+    if st not in (GDN_OK, GDN_ERR_DEVICE):
+        _check(st, "gdn_check_device")
+    return int(code.value)
 
 
 def version() -> str:

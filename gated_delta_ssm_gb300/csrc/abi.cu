@@ -286,6 +286,19 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
     return from_cuda(gdn::launch_prefill(a, act_dtype == GDN_BF16, as_cuda(stream)));
 }
 
+gdn_status gdn_check_device(int32_t *code)
+{
+    int a = 0, b = 0;
+    gdn_status st = from_cuda(gdn::take_decode_device_error(&a));
+    if (st == GDN_OK)
+        st = from_cuda(gdn::take_prefill_device_error(&b));
+    if (code)
+        *code = a | b;
+    if (st != GDN_OK)
+        return st;
+    return (a | b) ? GDN_ERR_DEVICE : GDN_OK;
+}
+
 const char *gdn_last_cuda_error(void) { return g_last_cuda_error; }
 
 const char *gdn_status_string(gdn_status s)
@@ -295,6 +308,7 @@ const char *gdn_status_string(gdn_status s)
     case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
     case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_DEVICE: return "GDN_ERR_DEVICE";
     }
     return "unknown gdn_status";
 }

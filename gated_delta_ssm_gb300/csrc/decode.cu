@@ -145,12 +145,13 @@ __device__ __forceinline__ void cluster_wait_acquire()
 // NTOK = 1: one decode step. NTOK = 2: K=2 verify, snapshot after token 0.
 //
 // Order of a CTA's work, chosen so that no fence ever waits on the state
-// stores: (1) state-row loads, (2) conv-window and gate loads, one memory
-// round trip; (3) conv + SiLU, then cluster arrive (every read of the shared
-// Q/K history is done); (4) L2, gates; (5) recurrence in registers; (6) gated
-// norm (row slices of a head exchange partial sums through distributed
-// shared memory when NSPLIT > 1); (7) state stores; (8) cluster wait, then the
-// single owner of each Q/K channel rewrites its history.
+// loads or stores: (1) state-row loads, (2) conv-window, gate, z and norm-gain
+// loads, one memory round trip; (3) conv + SiLU, then cluster arrive (every
+// read of the shared Q/K history is done); (4) L2, gates; (5) recurrence in
+// registers; (6) gated norm (row slices of a head exchange partial sums
+// through distributed shared memory when NSPLIT > 1); (7) state stores; (8)
+// cluster wait, then the single owner of each Q/K channel rewrites its
+// history.
 template <typename TIn, int NTOK, int NSPLIT>
 __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
 {
@@ -195,6 +196,14 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
     if (tid < ROWS)
         conv_window_load<TIn, NTOK>(histb + (size_t)c_v * (W - 1), xb + c_v, a.x_stride,
                                     a.conv_w + (size_t)c_v * W, W, wv);
+    float zj[NTOK], nw = 0.0f;
+    if (tid < ROWS) {
+#pragma unroll
+        for (int p = 0; p < NTOK; ++p)
+            zj[p] = load_act<TIn>(static_cast<const TIn *>(a.z) + (tok0 + p) * a.z_stride +
+                                  (int64_t)h * kD + row0 + tid);
+        nw = __ldg(a.norm_w + row0 + tid);
+    }
     float g_alpha = 0.0f, g_bl = 0.0f, g_dt = 0.0f, g_alog = 0.0f;
     const bool gate_thread = tid >= ROWS && tid < ROWS + NTOK;
     if (gate_thread) {
@@ -205,13 +214,16 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
         g_alog = __ldg(a.A_log + h);
     }
 
-    // (3) conv + SiLU; every read of the shared Q/K history is now complete
+    // (3) conv + SiLU; every read of the shared Q/K history is now complete: the
+    // arrive below issues after the arithmetic that consumed those loads (a
+    // warp issues in order), so it needs no release fence, which would also
+    // wait for this warp's state loads still in flight
     float vals[NTOK];
 #pragma unroll
     for (int p = 0; p < NTOK; ++p)
         vals[p] = silu_f(conv_window_pre<NTOK>(wqk, W, p));
     if (csize > 1)
-        cluster_arrive_release();
+        cluster_arrive_relaxed();
 
     // (4) V rows (exclusively owned: history rewritten at once), gates, Q/K L2
     if (tid < ROWS) {
@@ -275,8 +287,7 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
             const float inv = norm_inv(bp[0], bp[1], bp[2], bp[3], a.rms_eps);
             const int j = row0 + tid;
             const int64_t row = tok0 + p;
-            const float zj = load_act<TIn>(static_cast<const TIn *>(a.z) + row * a.z_stride + (int64_t)h * kD + j);
-            a.out[((size_t)row * a.Hv + h) * kD + j] = gated_out(sy[p * ROWS + tid], inv, __ldg(a.norm_w + j), zj);
+            a.out[((size_t)row * a.Hv + h) * kD + j] = gated_out(sy[p * ROWS + tid], inv, nw, zj[p]);
         }
     }
     if (NSPLIT > 1)
@@ -427,6 +438,13 @@ cudaError_t launch_gated_norm(const float *y, const float *w, const void *z, boo
         gated_norm_kernel<<<blocks, 256, 0, s>>>(y, w, static_cast<const float *>(z), z_stride,
                                                  out, rows, Hv, eps);
     return cudaGetLastError();
+}
+
+cudaError_t take_decode_device_error(int *code)
+{
+    // no kernel in this file waits on anything but hardware barriers
+    *code = 0;
+    return cudaSuccess;
 }
 
 cudaError_t launch_verify_commit(float *state, float *conv_state, const float *state_snap,

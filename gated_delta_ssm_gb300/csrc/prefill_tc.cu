@@ -37,7 +37,9 @@
 
 namespace gdn {
 
-__device__ int g_device_error;   // set by a kernel whose bounded wait ran out
+// Set when a bounded wait of a kernel in this file gives up; read and cleared
+// by take_prefill_device_error.
+static __device__ int g_device_error;
 
 namespace {
 
@@ -742,8 +744,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 *reinterpret_cast<float4 *>(dst + c + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         }
     }
-    if (tid == 0 && *serr)
-        atomicOr(&g_device_error, *serr);
+    if (*serr) {
+        if (tid == 0)
+            atomicOr(&g_device_error, *serr);
+        // MMAs may still be in flight: a second bounded chance for every barrier
+        // before TMEM is released
+        for (int i = 0; i < 4; ++i)
+            tc::mbar_wait(mbar + 8 * i, (chunk & 1), kWaitLimit);
+    }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0)
@@ -781,6 +789,18 @@ cudaError_t prefill_typed(const PrefillArgs &a, cudaStream_t s)
 }
 
 }  // namespace
+
+cudaError_t take_prefill_device_error(int *code)
+{
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int));
+    if (e == cudaSuccess && v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    }
+    *code = v;
+    return e;
+}
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, bool bf16, cudaStream_t s)
 {

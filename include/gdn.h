@@ -14,9 +14,10 @@
  *               call that returns anything but GDN_OK has enqueued nothing,
  *               except GDN_ERR_CUDA, where the launch itself failed;
  *               gdn_last_cuda_error() then names the CUDA error.
- *   Reentrancy  The library holds no mutable global state (the last-error
- *               text is per thread): calls from several host threads and
- *               streams are safe as long as their buffers do not overlap.
+ *   Reentrancy  The library holds no mutable global state besides the
+ *               last-error text (per host thread) and one device-side error
+ *               word (see gdn_check_device): calls from several host threads
+ *               and streams are safe as long as their buffers do not overlap.
  *   Precision   Parameters, recurrent state, conv history and all outputs are
  *               float32; activations are float32 or bf16 (gdn_dtype). All
  *               arithmetic is float32.
@@ -61,7 +62,8 @@ typedef enum gdn_status {
     GDN_OK = 0,
     GDN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, stride too small, misalignment */
     GDN_ERR_UNSUPPORTED = 2,  /* a valid shape this build has no kernel for (d != 128, W > 8, r > 8) */
-    GDN_ERR_CUDA = 3          /* the launch failed; see gdn_last_cuda_error() */
+    GDN_ERR_CUDA = 3,         /* the launch failed; see gdn_last_cuda_error() */
+    GDN_ERR_DEVICE = 4        /* a kernel's bounded wait gave up (see gdn_check_device) */
 } gdn_status;
 
 typedef enum gdn_dtype {
@@ -227,6 +229,16 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
                                const void *alpha, const void *beta_logit, gdn_dtype act_dtype,
                                const gdn_params *params, float *out, const gdn_dims *dims,
                                int32_t n_tokens, int32_t chunk, gdn_stream_t stream);
+
+/*
+ * Every wait inside a kernel (on a bulk copy or a tensor-core operation) is
+ * bounded; a kernel whose wait gives up sets a bit in a device-side error word
+ * and skips the rest of its work instead of hanging. This call waits for all
+ * work on the device (it synchronises), reads the word into *code (may be
+ * NULL) and clears it. Returns GDN_OK when no wait gave up, GDN_ERR_DEVICE when
+ * one did, GDN_ERR_CUDA if the read failed.
+ */
+gdn_status gdn_check_device(int32_t *code);
 
 /* Text of the last CUDA error seen by a call on this host thread ("" if none). */
 const char *gdn_last_cuda_error(void);
