@@ -167,12 +167,13 @@ __device__ __forceinline__ void load8<float>(const float *p, float (&v)[8])
 }
 
 // conv + SiLU of 8 channels (cb .. cb+7) for 8 tokens (t0 .. t0+7 of the call);
-// tokens at or past T give 0.
-template <typename TIn>
+// tokens at or past T give 0. WC > 0 fixes the tap count at compile time so
+// that all window loads issue together; WC == 0 reads it from the arguments.
+template <typename TIn, int WC>
 __device__ __forceinline__ void conv8x8(const PrefillArgs &a, int b, int cb, int t0,
                                         float (&out)[8][8])
 {
-    const int W = a.W, T = a.T;
+    const int W = WC > 0 ? WC : a.W, T = a.T;
     const TIn *xb = static_cast<const TIn *>(a.x) + (int64_t)b * T * a.x_stride + cb;
     const float *hist = a.conv_state + ((size_t)b * a.conv_dim + cb) * (W - 1);
 #pragma unroll
@@ -180,7 +181,10 @@ __device__ __forceinline__ void conv8x8(const PrefillArgs &a, int b, int cb, int
 #pragma unroll
         for (int e = 0; e < 8; ++e)
             out[t][e] = 0.0f;
-    for (int tau = 0; tau < W; ++tau) {
+#pragma unroll
+    for (int tau = 0; tau < (WC > 0 ? WC : kMaxW); ++tau) {
+        if (tau >= W)
+            break;
         float w[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e)
@@ -361,7 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
             const int grp = lane & 15;                          // 8-channel group of the head
             const int cb = (part ? a.Hq * kD : 0) + hk * kD + 8 * grp;
             float v[8][8];
-            conv8x8<TIn>(a, b, cb, c0 + t0, v);
+            if (a.W == 4)
+                conv8x8<TIn, 4>(a, b, cb, c0 + t0, v);
+            else
+                conv8x8<TIn, 0>(a, b, cb, c0 + t0, v);
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 float ss = 0.0f;
@@ -389,7 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
             const int grp = lane & 15;
             const int cb = 2 * a.Hq * kD + h * kD + 8 * grp;
             float v[8][8];
-            conv8x8<TIn>(a, b, cb, c0 + t0, v);
+            if (a.W == 4)
+                conv8x8<TIn, 4>(a, b, cb, c0 + t0, v);
+            else
+                conv8x8<TIn, 0>(a, b, cb, c0 + t0, v);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int j = 8 * grp + e;
@@ -703,11 +713,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
         }
         __syncthreads();
 
-        // ---- gated RMSNorm of each token's output row
+        // ---- gated RMSNorm of each token's output row (warp w: tokens w, w+8, ...;
+        // every z value is requested before the first is used)
         {
             const float *O = reinterpret_cast<const float *>(smem + XU_HI);
             const TIn *zb = static_cast<const TIn *>(a.z) + (int64_t)b * T * a.z_stride + (int64_t)h * kD;
-            for (int t = warp; t < n; t += 8) {
+            float zv[kC / 8][4];
+#pragma unroll
+            for (int i = 0; i < kC / 8; ++i) {
+                const int t = warp + 8 * i;
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    zv[i][m] = t < n ? load_act<TIn>(zb + ((int64_t)c0 + t) * a.z_stride + 32 * m + lane) : 0.0f;
+            }
+            float nwv[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                nwv[m] = __ldg(a.norm_w + 32 * m + lane);
+#pragma unroll
+            for (int i = 0; i < kC / 8; ++i) {
+                const int t = warp + 8 * i;
+                if (t >= n)
+                    break;
                 float yv[4], bp[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m)
@@ -716,14 +743,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 for (int m = 0; m < 4; ++m)
                     bp[m] = norm_block_partial(yv[m]);
                 const float inv = norm_inv(bp[0], bp[1], bp[2], bp[3], a.rms_eps);
-                const int64_t row = (int64_t)c0 + t;
-                const TIn *zr = zb + row * a.z_stride;
-                float *outr = a.out + (((size_t)b * T + row) * a.Hv + h) * kD;
+                float *outr = a.out + (((size_t)b * T + c0 + t) * a.Hv + h) * kD;
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int j = 32 * m + lane;
-                    outr[j] = gated_out(yv[m], inv, __ldg(a.norm_w + j), load_act<TIn>(zr + j));
-                }
+                for (int m = 0; m < 4; ++m)
+                    outr[32 * m + lane] = gated_out(yv[m], inv, nwv[m], zv[i][m]);
             }
         }
         __syncthreads();
