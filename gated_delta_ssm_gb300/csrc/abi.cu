@@ -255,6 +255,7 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
     const size_t es = act_size(act_dtype);
     // the chunk kernel reads 8 channels of a token row per 16-byte load
     if (!aligned(state, 16) || !aligned(x, 16) || (dims->x_stride * (int64_t)es) % 16 != 0 ||
+        !aligned(params->conv_w, 16) ||
         !aligned(z, es) || !aligned(alpha, es) || !aligned(beta_logit, es) || !aligned(out, 16))
         return GDN_ERR_INVALID_ARG;
     if (chunk != 64)

@@ -216,26 +216,54 @@ __device__ __forceinline__ void conv8x8(const PrefillArgs &a, int b, int cb, int
             out[t][e] = t0 + t < T ? silu_f(out[t][e]) : 0.0f;
 }
 
-// One column c of T = (I + A)^{-1} (unit lower triangular) by forward
-// substitution, T[t][c] = [t == c] - sum_{s<t} A[t][s] T[s][c], one thread per
-// column. A is read from the fp32 staging rows (16 float4 chunks per row,
-// XOR-swizzled by the row index so that the row writes are conflict-free).
-__device__ __forceinline__ void tri_inverse_column(const uint8_t *smem, int c, float (&Tc)[kC])
+// The four-tap conv for a block whose window lies inside the call (every
+// 8-token block but the first of a sequence): each of the 11 input rows is
+// read once with a branch-free load (rows past the end of the call read the
+// last row and are masked), so all loads issue together; SiLU uses the fast
+// exponential.
+template <typename TIn>
+__device__ __forceinline__ void conv8x8_w4_inner(const PrefillArgs &a, int b, int cb, int t0,
+                                                 float (&out)[8][8])
 {
+    const int T = a.T;
+    const TIn *xb = static_cast<const TIn *>(a.x) + (int64_t)b * T * a.x_stride + cb;
+    float w[8][4];
 #pragma unroll
-    for (int t = 0; t < kC; ++t) {
-        const float *row = reinterpret_cast<const float *>(smem + TT_HI + t * 256);
-        float acc0 = 0.0f, acc1 = 0.0f;
-#pragma unroll
-        for (int s = 0; s < t; ++s) {
-            const float av = row[(((s >> 2) ^ (t & 15)) << 2) + (s & 3)];
-            if (s & 1)
-                acc1 = __fmaf_rn(av, Tc[s], acc1);
-            else
-                acc0 = __fmaf_rn(av, Tc[s], acc0);
-        }
-        Tc[t] = (t == c ? 1.0f : 0.0f) - (acc0 + acc1);
+    for (int e = 0; e < 8; ++e) {
+        const float4 f = __ldg(reinterpret_cast<const float4 *>(a.conv_w + (size_t)(cb + e) * 4));
+        w[e][0] = f.x; w[e][1] = f.y; w[e][2] = f.z; w[e][3] = f.w;
     }
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            out[t][e] = 0.0f;
+#pragma unroll
+    for (int rr = 0; rr < 11; ++rr) {
+        const int sidx = t0 - 3 + rr;                 // >= 0 on this path
+        float v[8];
+        load8<TIn>(xb + (int64_t)min(sidx, T - 1) * a.x_stride, v);
+        const bool live = sidx < T;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            v[e] = live ? v[e] : 0.0f;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int tau = rr - t;                   // tap that row rr feeds for token t
+            if (tau >= 0 && tau < 4) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    out[t][e] = __fmaf_rn(v[e], w[e][tau], out[t][e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float x = out[t][e];
+            out[t][e] = t0 + t < T ? __fdividef(x, 1.0f + __expf(-x)) : 0.0f;
+        }
 }
 
 template <typename TIn>
@@ -365,7 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
             const int grp = lane & 15;                          // 8-channel group of the head
             const int cb = (part ? a.Hq * kD : 0) + hk * kD + 8 * grp;
             float v[8][8];
-            if (a.W == 4)
+            if (a.W == 4 && c0 + t0 >= 3)
+                conv8x8_w4_inner<TIn>(a, b, cb, c0 + t0, v);
+            else if (a.W == 4)
                 conv8x8<TIn, 4>(a, b, cb, c0 + t0, v);
             else
                 conv8x8<TIn, 0>(a, b, cb, c0 + t0, v);
@@ -396,7 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
             const int grp = lane & 15;
             const int cb = 2 * a.Hq * kD + h * kD + 8 * grp;
             float v[8][8];
-            if (a.W == 4)
+            if (a.W == 4 && c0 + t0 >= 3)
+                conv8x8_w4_inner<TIn>(a, b, cb, c0 + t0, v);
+            else if (a.W == 4)
                 conv8x8<TIn, 4>(a, b, cb, c0 + t0, v);
             else
                 conv8x8<TIn, 0>(a, b, cb, c0 + t0, v);
@@ -507,44 +539,119 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
         __syncthreads();
 
         if (warp >= 4) {
-            // ---- T = (I + A)^{-1}: warps 4-5, one thread per column
-            float Tc[kC];
-            const int c = tid - 128;
-            if (warp < 6) {
-                tri_inverse_column(smem, c, Tc);
-            } else {
-                // (e^{Gam_C-Gam} K)^T from the first two parts of the K rows: two key rows i per thread
-#pragma unroll 1
-                for (int i = c - 64; i < kD; i += 64) {
+            const int tq = tid - 128;
+            // ---- (e^{Gam_C-Gam} K)^T from the first two parts of the K rows: key row tq
+            for (int t0 = 0; t0 < kC; t0 += 8) {
+                float col[8];
 #pragma unroll
-                    for (int t0 = 0; t0 < kC; t0 += 8) {
-                        float col[8];
+                for (int t = 0; t < 8; ++t) {
+                    const uint32_t off = tc::km_offset(kC + t0 + t, tq, kD);
+                    const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + QK_HI + off)) +
+                                     __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + QK_LO + off));
+                    col[t] = kv * segc[t0 + t];
+                }
+                uint4 hi, lo;
+                split8(col, hi, lo);
+                const uint32_t off = tc::km_offset(tq, t0, kC);
+                *reinterpret_cast<uint4 *>(smem + KT_HI + off) = hi;
+                *reinterpret_cast<uint4 *>(smem + KT_LO + off) = lo;
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");   // the K rows are free now
+
+            // ---- T = (I + A)^{-1} by 16x16 blocks: the diagonal blocks by forward
+            // substitution, then T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj for i > j in
+            // order of i - j. T (fp32, rows XOR-swizzled like A) and the products
+            // A_ik T_kj use the dead K rows of the [Q; K] tile.
+            float *Tf = reinterpret_cast<float *>(smem + QK_HI + 16384);
+            float *Yb = reinterpret_cast<float *>(smem + QK_LO + 16384);   // [3][16][16]
+            const float *Af = reinterpret_cast<const float *>(smem + TT_HI);
+            auto sw = [](int t, int c) { return t * kC + ((((c >> 2) ^ (t & 15)) << 2) | (c & 3)); };
+            if (tq < kC) {
+                const int blk = tq >> 4, c = tq & 15, o = 16 * blk;
+                float tcol[16];
 #pragma unroll
-                        for (int t = 0; t < 8; ++t) {
-                            const uint32_t off = tc::km_offset(kC + t0 + t, i, kD);
-                            const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + QK_HI + off)) +
-                                             __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + QK_LO + off));
-                            col[t] = kv * segc[t0 + t];
-                        }
-                        uint4 hi, lo;
-                        split8(col, hi, lo);
-                        const uint32_t off = tc::km_offset(i, t0, kC);
-                        *reinterpret_cast<uint4 *>(smem + KT_HI + off) = hi;
-                        *reinterpret_cast<uint4 *>(smem + KT_LO + off) = lo;
-                    }
+                for (int t = 0; t < 16; ++t) {
+                    float acc = 0.0f;
+#pragma unroll
+                    for (int s2 = 0; s2 < t; ++s2)
+                        acc = __fmaf_rn(Af[sw(o + t, o + s2)], tcol[s2], acc);
+                    tcol[t] = (t == c ? 1.0f : 0.0f) - acc;
+                    Tf[sw(o + t, o + c)] = tcol[t];
                 }
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");   // every read of A is done
-            if (warp < 6) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll 1
+            for (int d = 1; d < 4; ++d) {
+                const int nb = 4 - d;
+                const int ne = nb * 2;                       // output elements per thread
+                // Y_ij = sum_{k=j}^{i-1} A_ik T_kj; this thread's elements e = tq + 128 m
+                float acc[6];
+                int rowA[6], colT[6];
 #pragma unroll
-                for (int t = 0; t < kC; ++t) {
-                    __nv_bfloat16 p1, p2, p3;
-                    split1x3(Tc[t], p1, p2, p3);
-                    const uint32_t off = tc::km_offset(t, c, kC);
-                    *reinterpret_cast<__nv_bfloat16 *>(smem + TT_HI + off) = p1;
-                    *reinterpret_cast<__nv_bfloat16 *>(smem + TT_LO + off) = p2;
-                    *reinterpret_cast<__nv_bfloat16 *>(smem + TT_3 + off) = p3;
+                for (int m = 0; m < 6; ++m) {
+                    const int e = tq + 128 * m;
+                    const int bb = e >> 8, ra = (e >> 4) & 15, bc = e & 15;
+                    rowA[m] = 16 * (d + bb) + ra;
+                    colT[m] = 16 * bb + bc;
+                    acc[m] = 0.0f;
                 }
+#pragma unroll 1
+                for (int kb = 0; kb < d; ++kb) {
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) {
+#pragma unroll
+                        for (int m = 0; m < 6; ++m) {
+                            if (m < ne) {
+                                const int kcol = colT[m] - (colT[m] & 15) + 16 * kb + kk;
+                                acc[m] = __fmaf_rn(Af[sw(rowA[m], kcol)], Tf[sw(kcol, colT[m])], acc[m]);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < 6; ++m)
+                    if (m < ne)
+                        Yb[tq + 128 * m] = acc[m];
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                // T_ij = -T_ii Y_ij
+#pragma unroll
+                for (int m = 0; m < 6; ++m)
+                    acc[m] = 0.0f;
+#pragma unroll
+                for (int c2 = 0; c2 < 16; ++c2) {
+#pragma unroll
+                    for (int m = 0; m < 6; ++m) {
+                        if (m < ne) {
+                            const int e = tq + 128 * m;
+                            const int bb = e >> 8, bc = e & 15;
+                            const int ti = rowA[m] - (rowA[m] & 15);
+                            acc[m] = __fmaf_rn(Tf[sw(rowA[m], ti + c2)], Yb[bb * 256 + c2 * 16 + bc], acc[m]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < 6; ++m)
+                    if (m < ne)
+                        Tf[sw(rowA[m], colT[m])] = -acc[m];
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            }
+            // ---- T as the three-part bf16 operand tile (every read of A is done)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int q = tq + 128 * m;
+                const int t = q & (kC - 1), cg = q >> 6;
+                float v8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int sc = 8 * cg + e;
+                    v8[e] = sc <= t ? Tf[sw(t, sc)] : 0.0f;
+                }
+                uint4 p1, p2, p3;
+                split8x3(v8, p1, p2, p3);
+                const uint32_t off = tc::km_offset(t, 8 * cg, kC);
+                *reinterpret_cast<uint4 *>(smem + TT_HI + off) = p1;
+                *reinterpret_cast<uint4 *>(smem + TT_LO + off) = p2;
+                *reinterpret_cast<uint4 *>(smem + TT_3 + off) = p3;
             }
             // ---- state accumulator scaled by e^{Gam_C} ahead of this chunk's update
             const float egC = *segC;

@@ -219,8 +219,8 @@ gdn_status gdn_verify_commit(float *state, float *conv_state, const float *state
  *   state, conv_state updated in place (state after the last token);
  *   x, z, alpha, beta_logit as in LAYOUTS with T = n_tokens;
  *   out float [B][n_tokens][Hv][d].
- * chunk must be 64. x must be 16-byte aligned with rows a multiple of 16 bytes
- * apart (x_stride * element size). Agrees with the sequential scan within
+ * chunk must be 64. x and params->conv_w must be 16-byte aligned, with x rows
+ * a multiple of 16 bytes apart (x_stride * element size). Agrees with the sequential scan within
  * float32 rounding, not bit for bit.
  * Errors: INVALID_ARG (null, n_tokens < 1, bad dims, x alignment), UNSUPPORTED
  * (d, W, chunk != 64).
