@@ -8,10 +8,10 @@
 // prefill scan" note of "ssm_mamba.rs"):
 //   G   = [Q; K] K^T                         tensor core   (QK^T and KK^T)
 //   P   = e^{Gam_t-Gam_s} (QK^T)[t][s], s<=t  CUDA cores
-//   A   = beta_t e^{Gam_t-Gam_s} (KK^T)[t][s], s<t;  T = (I + A)^{-1}  CUDA cores
+//   A   = beta_t e^{Gam_t-Gam_s} (KK^T)[t][s], s<t      CUDA cores
 //   KS  = S_0^T [Q; K]^T                     tensor core   ((Q S_0)^T, (K S_0)^T)
-//   X^T = (beta V - beta e^{Gam} K S_0)^T     CUDA cores
-//   U^T = X^T T^T                            tensor core
+//   X   = beta V - beta e^{Gam} K S_0;  U = (I + A)^{-1} X by forward substitution,
+//         one value column per thread, in registers            CUDA cores
 //   O^T = e^{Gam} (Q S_0)^T + U^T P^T        tensor core (accumulates onto KS)
 //   S^T <- e^{Gam_C} S^T + U^T (diag(e^{Gam_C-Gam}) K)   tensor core (state in TMEM)
 // then the gated RMSNorm of each token's O row. Every product is arranged
@@ -19,7 +19,7 @@
 // each TMEM lane holding one row of the result.
 //
 // Precision: operands are fp32 values split into bf16 parts. Every product on
-// the path to the readout (G, KS, U, O) splits its operands three ways
+// the path to the readout (G, KS, O) splits its operands three ways
 // (x = x1 + x2 + x3, ~24 bits) and forms x1 y1 + x1 y2 + x2 y1 + x1 y3 +
 // x2 y2 + x3 y1: the readout of a token can be orders of magnitude smaller
 // than its terms (q_t . k_t and the sum over earlier tokens cancel), and the
@@ -54,12 +54,12 @@ constexpr uint32_t QK_HI = 0, QK_LO = 32768;        // [128 t'][128 i]  (Q rows,
 constexpr uint32_t ST_HI = 65536, ST_LO = 98304;    // [128 j][128 i]   S^T
 constexpr uint32_t KT_HI = 131072, KT_LO = 147456;  // [128 i][64 t]    (e^{Gam_C-Gam} K)^T
 constexpr uint32_t ST_3 = 131072;                   // third part of S^T (in KT's space)
-constexpr uint32_t XU_HI = 163840, XU_LO = 180224;  // [128 j][64 t]    X^T, then U^T; V^T and O staging
-constexpr uint32_t TT_HI = 196608, TT_LO = 204800;  // [64 t][64 s]     T; A staging
+constexpr uint32_t XU_HI = 163840, XU_LO = 180224;  // [128 j][64 t]    U^T; V^T and O staging
+constexpr uint32_t TT_HI = 196608;                  // [64 t][64 s]     A (fp32, 16 KB)
 constexpr uint32_t PP_HI = 212992, PP_LO = 221184;  // [64 t][64 s]     P
 constexpr uint32_t QK_3 = 196608;                   // third part of [Q; K] (in TT and PP's space)
-// third parts of X^T/U^T, T and P, in the Q rows of [Q; K] (dead once G and KS are formed)
-constexpr uint32_t XU_3 = QK_HI, TT_3 = QK_LO, PP_3 = QK_LO + 8192;
+// third parts of U^T and P, in the Q rows of [Q; K] (dead once G and KS are formed)
+constexpr uint32_t XU_3 = QK_HI, PP_3 = QK_LO + 8192;
 constexpr uint32_t SC_G = 229376, SC_BETA = SC_G + 256, SC_GAM = SC_BETA + 256,
                    SC_GAML = SC_GAM + 256, SC_EG = SC_GAML + 256, SC_EGC = SC_EG + 256,
                    SC_EGCC = SC_EGC + 256, SC_MBAR = SC_EGCC + 8, SC_TMEM = SC_MBAR + 32,
@@ -67,7 +67,7 @@ constexpr uint32_t SC_G = 229376, SC_BETA = SC_G + 256, SC_GAM = SC_BETA + 256,
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // TMEM columns
-constexpr uint32_t TM_G = 0, TM_KS = 64, TM_U = 192, TM_S = 256, TM_COLS = 512;
+constexpr uint32_t TM_G = 0, TM_KS = 64, TM_S = 256, TM_COLS = 512;
 constexpr int kWaitLimit = 1 << 26;
 
 __device__ __forceinline__ void split8(const float (&v)[8], uint4 &hi, uint4 &lo)
@@ -556,103 +556,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 *reinterpret_cast<uint4 *>(smem + KT_HI + off) = hi;
                 *reinterpret_cast<uint4 *>(smem + KT_LO + off) = lo;
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");   // the K rows are free now
-
-            // ---- T = (I + A)^{-1} by 16x16 blocks: the diagonal blocks by forward
-            // substitution, then T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj for i > j in
-            // order of i - j. T (fp32, rows XOR-swizzled like A) and the products
-            // A_ik T_kj use the dead K rows of the [Q; K] tile.
-            float *Tf = reinterpret_cast<float *>(smem + QK_HI + 16384);
-            float *Yb = reinterpret_cast<float *>(smem + QK_LO + 16384);   // [3][16][16]
-            const float *Af = reinterpret_cast<const float *>(smem + TT_HI);
-            auto sw = [](int t, int c) { return t * kC + ((((c >> 2) ^ (t & 15)) << 2) | (c & 3)); };
-            if (tq < kC) {
-                const int blk = tq >> 4, c = tq & 15, o = 16 * blk;
-                float tcol[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    float acc = 0.0f;
-#pragma unroll
-                    for (int s2 = 0; s2 < t; ++s2)
-                        acc = __fmaf_rn(Af[sw(o + t, o + s2)], tcol[s2], acc);
-                    tcol[t] = (t == c ? 1.0f : 0.0f) - acc;
-                    Tf[sw(o + t, o + c)] = tcol[t];
-                }
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-#pragma unroll 1
-            for (int d = 1; d < 4; ++d) {
-                const int nb = 4 - d;
-                const int ne = nb * 2;                       // output elements per thread
-                // Y_ij = sum_{k=j}^{i-1} A_ik T_kj; this thread's elements e = tq + 128 m
-                float acc[6];
-                int rowA[6], colT[6];
-#pragma unroll
-                for (int m = 0; m < 6; ++m) {
-                    const int e = tq + 128 * m;
-                    const int bb = e >> 8, ra = (e >> 4) & 15, bc = e & 15;
-                    rowA[m] = 16 * (d + bb) + ra;
-                    colT[m] = 16 * bb + bc;
-                    acc[m] = 0.0f;
-                }
-#pragma unroll 1
-                for (int kb = 0; kb < d; ++kb) {
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-#pragma unroll
-                        for (int m = 0; m < 6; ++m) {
-                            if (m < ne) {
-                                const int kcol = colT[m] - (colT[m] & 15) + 16 * kb + kk;
-                                acc[m] = __fmaf_rn(Af[sw(rowA[m], kcol)], Tf[sw(kcol, colT[m])], acc[m]);
-                            }
-                        }
-                    }
-                }
-#pragma unroll
-                for (int m = 0; m < 6; ++m)
-                    if (m < ne)
-                        Yb[tq + 128 * m] = acc[m];
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                // T_ij = -T_ii Y_ij
-#pragma unroll
-                for (int m = 0; m < 6; ++m)
-                    acc[m] = 0.0f;
-#pragma unroll
-                for (int c2 = 0; c2 < 16; ++c2) {
-#pragma unroll
-                    for (int m = 0; m < 6; ++m) {
-                        if (m < ne) {
-                            const int e = tq + 128 * m;
-                            const int bb = e >> 8, bc = e & 15;
-                            const int ti = rowA[m] - (rowA[m] & 15);
-                            acc[m] = __fmaf_rn(Tf[sw(rowA[m], ti + c2)], Yb[bb * 256 + c2 * 16 + bc], acc[m]);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int m = 0; m < 6; ++m)
-                    if (m < ne)
-                        Tf[sw(rowA[m], colT[m])] = -acc[m];
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-            }
-            // ---- T as the three-part bf16 operand tile (every read of A is done)
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int q = tq + 128 * m;
-                const int t = q & (kC - 1), cg = q >> 6;
-                float v8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int sc = 8 * cg + e;
-                    v8[e] = sc <= t ? Tf[sw(t, sc)] : 0.0f;
-                }
-                uint4 p1, p2, p3;
-                split8x3(v8, p1, p2, p3);
-                const uint32_t off = tc::km_offset(t, 8 * cg, kC);
-                *reinterpret_cast<uint4 *>(smem + TT_HI + off) = p1;
-                *reinterpret_cast<uint4 *>(smem + TT_LO + off) = p2;
-                *reinterpret_cast<uint4 *>(smem + TT_3 + off) = p3;
-            }
             // ---- state accumulator scaled by e^{Gam_C} ahead of this chunk's update
             const float egC = *segC;
 #pragma unroll 1
@@ -675,82 +578,61 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                     qv[e] *= seg[c + e];
                 tc::tmem_st16(tmem + lane_q + TM_KS + c, qv);
             }
-            float vt[kC];
+            // X^T row j = beta V^T - beta e^{Gam} (K S_0)^T, in registers (V^T was staged in
+            // this thread's own footprint of the X^T/U^T tile)
+            float xv[kC];
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
                 const uint32_t off = (q < 8 ? XU_HI : XU_LO) + (jrow >> 3) * 1024 + (q & 7) * 128 +
                                      (jrow & 7) * 16;
                 const float4 f = *reinterpret_cast<const float4 *>(smem + off);
-                vt[4 * q] = f.x; vt[4 * q + 1] = f.y; vt[4 * q + 2] = f.z; vt[4 * q + 3] = f.w;
+                xv[4 * q] = f.x; xv[4 * q + 1] = f.y; xv[4 * q + 2] = f.z; xv[4 * q + 3] = f.w;
             }
 #pragma unroll
             for (int c = 0; c < kC; c += 16) {
                 float kv[16];
                 tc::tmem_ld16(tmem + lane_q + TM_KS + kC + c, kv);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float x8[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int t = c + 8 * half + e;
-                        const float bt = sbeta[t];
-                        x8[e] = bt * vt[t] - bt * seg[t] * kv[8 * half + e];
-                    }
-                    uint4 p1, p2, p3;
-                    split8x3(x8, p1, p2, p3);
-                    const uint32_t off = tc::km_offset(jrow, c + 8 * half, kC);
-                    *reinterpret_cast<uint4 *>(smem + XU_HI + off) = p1;
-                    *reinterpret_cast<uint4 *>(smem + XU_LO + off) = p2;
-                    *reinterpret_cast<uint4 *>(smem + XU_3 + off) = p3;
+                for (int e = 0; e < 16; ++e) {
+                    const float bt = sbeta[c + e];
+                    xv[c + e] = bt * xv[c + e] - bt * seg[c + e] * kv[e];
                 }
             }
-        }
-        tc::fence_smem_to_async();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-
-        // ---- U^T = X^T T^T
-        if (tid == 0) {
-#pragma unroll 1
-            for (int kk = 0; kk < kC / 16; ++kk) {
-                const uint32_t ko = kk * 256;
-                const uint64_t a1 = tc::sdesc(sbase + XU_HI + ko, 128, 1024);
-                const uint64_t a2 = tc::sdesc(sbase + XU_LO + ko, 128, 1024);
-                const uint64_t a3 = tc::sdesc(sbase + XU_3 + ko, 128, 1024);
-                const uint64_t b1 = tc::sdesc(sbase + TT_HI + ko, 128, 1024);
-                const uint64_t b2 = tc::sdesc(sbase + TT_LO + ko, 128, 1024);
-                const uint64_t b3 = tc::sdesc(sbase + TT_3 + ko, 128, 1024);
-                tc::mma_bf16(tmem + TM_U, a1, b1, id_g, kk > 0);
-                tc::mma_bf16(tmem + TM_U, a1, b2, id_g, 1);
-                tc::mma_bf16(tmem + TM_U, a2, b1, id_g, 1);
-                tc::mma_bf16(tmem + TM_U, a1, b3, id_g, 1);
-                tc::mma_bf16(tmem + TM_U, a2, b2, id_g, 1);
-                tc::mma_bf16(tmem + TM_U, a3, b1, id_g, 1);
-            }
-            tc::mma_commit(mbar + 16);
-        }
-        if (!tc::mbar_wait(mbar + 16, par, kWaitLimit))
-            atomicOr(serr, 4);
-        tc::fence_after_sync();
-        if (warp < 4) {
-#pragma unroll 1
-            for (int c = 0; c < kC; c += 16) {
-                float uv[16];
-                tc::tmem_ld16(tmem + lane_q + TM_U + c, uv);
+            // U = (I + A)^{-1} X column by column: (I + A) is unit lower triangular,
+            // so u_t = x_t - sum_{s<t} A[t][s] u_s, with the rows of A (fp32, XOR-swizzled
+            // float4 chunks) read as broadcasts
+            const float *Af = reinterpret_cast<const float *>(smem + TT_HI);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float u8[8];
+            for (int t = 1; t < kC; ++t) {
+                const float *arow = Af + t * kC;
+                float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        u8[e] = uv[8 * half + e];
-                    uint4 p1, p2, p3;
-                    split8x3(u8, p1, p2, p3);
-                    const uint32_t off = tc::km_offset(jrow, c + 8 * half, kC);
-                    *reinterpret_cast<uint4 *>(smem + XU_HI + off) = p1;
-                    *reinterpret_cast<uint4 *>(smem + XU_LO + off) = p2;
-                    *reinterpret_cast<uint4 *>(smem + XU_3 + off) = p3;
+                for (int q = 0; q < (t + 3) / 4; ++q) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(arow + ((q ^ (t & 15)) << 2));
+                    if (4 * q + 0 < t)
+                        acc0 = __fmaf_rn(a4.x, xv[4 * q + 0], acc0);
+                    if (4 * q + 1 < t)
+                        acc1 = __fmaf_rn(a4.y, xv[4 * q + 1], acc1);
+                    if (4 * q + 2 < t)
+                        acc0 = __fmaf_rn(a4.z, xv[4 * q + 2], acc0);
+                    if (4 * q + 3 < t)
+                        acc1 = __fmaf_rn(a4.w, xv[4 * q + 3], acc1);
                 }
+                xv[t] = __fsub_rn(xv[t], __fadd_rn(acc0, acc1));
+            }
+            // U^T row j as the three-part operand of the O and state products
+#pragma unroll
+            for (int c = 0; c < kC; c += 8) {
+                float u8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    u8[e] = xv[c + e];
+                uint4 p1, p2, p3;
+                split8x3(u8, p1, p2, p3);
+                const uint32_t off = tc::km_offset(jrow, c, kC);
+                *reinterpret_cast<uint4 *>(smem + XU_HI + off) = p1;
+                *reinterpret_cast<uint4 *>(smem + XU_LO + off) = p2;
+                *reinterpret_cast<uint4 *>(smem + XU_3 + off) = p3;
             }
         }
         tc::fence_smem_to_async();
@@ -880,7 +762,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
         // MMAs may still be in flight: a second bounded chance for every barrier
         // before TMEM is released
         for (int i = 0; i < 4; ++i)
-            tc::mbar_wait(mbar + 8 * i, (chunk & 1), kWaitLimit);
+            if (i != 2)   // barrier 2 is not used
+                tc::mbar_wait(mbar + 8 * i, (chunk & 1), kWaitLimit);
     }
     tc::fence_before_sync();
     __syncthreads();
