@@ -19,7 +19,8 @@ import threading as _th
 __all__ = [
     "Dims", "Params", "GdnError", "load", "library_path",
     "decay_gate", "conv_update", "recurrence_decode", "gated_norm",
-    "decode_step", "verify_k2", "verify_commit", "prefill_chunked", "check_device", "version",
+    "decode_step", "verify_k2", "verify_commit", "prefill_chunked", "recurrence_scan",
+    "layer_scan", "verify_kn", "verify_commit_kn", "check_device", "version",
 ]
 
 _PKG = _os.path.dirname(_os.path.abspath(__file__))
@@ -112,6 +113,10 @@ def load():
             "gdn_verify_k2": [vp, vp, vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, vp],
             "gdn_verify_commit": [vp, vp, vp, vp, vp, pd, vp],
             "gdn_prefill_chunked": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, i32, i32, vp],
+            "gdn_recurrence_scan": [vp, vp, vp, vp, i64, vp, vp, vp, pd, i32, f32, vp],
+            "gdn_layer_scan": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, i32, vp],
+            "gdn_verify_kn": [vp, vp, vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, i32, vp],
+            "gdn_verify_commit_kn": [vp, vp, vp, vp, vp, pd, i32, vp],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -239,3 +244,40 @@ def prefill_chunked(state, conv_state, x, z, alpha, beta_logit, params: Params, 
                                       _ptr(beta_logit), _dtype(x), _ct.byref(cp), _ptr(out),
                                       _ct.byref(cd), n_tokens, chunk, _stream(stream)),
            "gdn_prefill_chunked")
+
+
+def recurrence_scan(state, q, k, v, qkv_stride: int, g, beta, y, dims: Dims, n_tokens: int,
+                    scale: float, stream=None):
+    cd = dims.c()
+    _check(load().gdn_recurrence_scan(_ptr(state), _ptr(q), _ptr(k), _ptr(v), qkv_stride,
+                                      _ptr(g), _ptr(beta), _ptr(y), _ct.byref(cd), n_tokens,
+                                      scale, _stream(stream)),
+           "gdn_recurrence_scan")
+
+
+def layer_scan(state, conv_state, x, z, alpha, beta_logit, params: Params, out, dims: Dims,
+               n_tokens: int, stream=None):
+    cd, cp = dims.c(), params.c()
+    _check(load().gdn_layer_scan(_ptr(state), _ptr(conv_state), _ptr(x), _ptr(z), _ptr(alpha),
+                                 _ptr(beta_logit), _dtype(x), _ct.byref(cp), _ptr(out),
+                                 _ct.byref(cd), n_tokens, _stream(stream)),
+           "gdn_layer_scan")
+
+
+def verify_kn(state, conv_state, state_snap, conv_snap, x, z, alpha, beta_logit, params: Params,
+              out, dims: Dims, n_draft: int, stream=None):
+    cd, cp = dims.c(), params.c()
+    _check(load().gdn_verify_kn(_ptr(state), _ptr(conv_state), _ptr(state_snap), _ptr(conv_snap),
+                                _ptr(x), _ptr(z), _ptr(alpha), _ptr(beta_logit), _dtype(x),
+                                _ct.byref(cp), _ptr(out), _ct.byref(cd), n_draft,
+                                _stream(stream)),
+           "gdn_verify_kn")
+
+
+def verify_commit_kn(state, conv_state, state_snap, conv_snap, n_accept, dims: Dims, n_draft: int,
+                     stream=None):
+    cd = dims.c()
+    _check(load().gdn_verify_commit_kn(_ptr(state), _ptr(conv_state), _ptr(state_snap),
+                                       _ptr(conv_snap), _ptr(n_accept), _ct.byref(cd), n_draft,
+                                       _stream(stream)),
+           "gdn_verify_commit_kn")

@@ -119,6 +119,55 @@ gdn_status fused_common(float *state, float *conv_state, float *state_snap, floa
     return from_cuda(gdn::launch_decode_fused(a, act_dtype == GDN_BF16, ntok, as_cuda(stream)));
 }
 
+gdn_status layer_scan_common(float *state, float *conv_state, float *state_snap, float *conv_snap,
+                             const void *x, const void *z, const void *alpha,
+                             const void *beta_logit, gdn_dtype act_dtype,
+                             const gdn_params *params, float *out, const gdn_dims *dims,
+                             int32_t n_tokens, gdn_stream_t stream)
+{
+    gdn_status st = check_dims(dims, 7);
+    if (st != GDN_OK)
+        return st;
+    if ((st = check_params(params)) != GDN_OK)
+        return st;
+    if (!valid_dtype(act_dtype) || n_tokens < 1)
+        return GDN_ERR_INVALID_ARG;
+    if (!state || !conv_state || !x || !z || !alpha || !beta_logit || !out)
+        return GDN_ERR_INVALID_ARG;
+    const size_t es = act_size(act_dtype);
+    if (!aligned(state, 16) || (state_snap && !aligned(state_snap, 16)) || !aligned(x, es) ||
+        !aligned(z, es) || !aligned(alpha, es) || !aligned(beta_logit, es) || !aligned(out, 4) ||
+        !aligned(conv_state, 4) || (conv_snap && !aligned(conv_snap, 4)))
+        return GDN_ERR_INVALID_ARG;
+    gdn::LayerScanArgs a;
+    a.state = state;
+    a.conv_state = conv_state;
+    a.state_snap = n_tokens > 1 ? state_snap : nullptr;
+    a.conv_snap = conv_snap;
+    a.x = x;
+    a.z = z;
+    a.alpha = alpha;
+    a.beta_logit = beta_logit;
+    a.conv_w = params->conv_w;
+    a.dt = params->dt;
+    a.A_log = params->A_log;
+    a.norm_w = params->norm_w;
+    a.out = out;
+    a.x_stride = dims->x_stride;
+    a.z_stride = dims->z_stride;
+    a.gate_stride = dims->gate_stride;
+    a.B = dims->n_seq;
+    a.Hq = dims->n_qk_heads;
+    a.Hv = dims->n_v_heads;
+    a.W = dims->d_conv;
+    a.conv_dim = conv_dim_of(dims);
+    a.T = n_tokens;
+    a.l2_eps = params->l2_eps;
+    a.rms_eps = params->rms_eps;
+    a.scale = 1.0f / sqrtf((float)dims->head_dim);
+    return from_cuda(gdn::launch_layer_scan(a, act_dtype == GDN_BF16, as_cuda(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -238,6 +287,75 @@ gdn_status gdn_verify_commit(float *state, float *conv_state, const float *state
                                                as_cuda(stream)));
 }
 
+gdn_status gdn_recurrence_scan(float *state, const float *q, const float *k, const float *v,
+                               int64_t qkv_stride, const float *g, const float *beta, float *y,
+                               const gdn_dims *dims, int32_t n_tokens, float scale,
+                               gdn_stream_t stream)
+{
+    gdn_status st = check_dims(dims, 0);
+    if (st != GDN_OK)
+        return st;
+    if (!state || !q || !k || !v || !g || !beta || !y || !aligned(state, 16) || n_tokens < 1)
+        return GDN_ERR_INVALID_ARG;
+    if ((int64_t)dims->n_seq * n_tokens > 1 &&
+        qkv_stride < (int64_t)dims->n_v_heads * dims->head_dim)
+        return GDN_ERR_INVALID_ARG;
+    gdn::RecScanArgs a;
+    a.state = state;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.qkv_stride = qkv_stride;
+    a.g = g;
+    a.beta = beta;
+    a.y = y;
+    a.B = dims->n_seq;
+    a.Hq = dims->n_qk_heads;
+    a.Hv = dims->n_v_heads;
+    a.T = n_tokens;
+    a.scale = scale;
+    return from_cuda(gdn::launch_recurrence_scan(a, as_cuda(stream)));
+}
+
+gdn_status gdn_layer_scan(float *state, float *conv_state, const void *x, const void *z,
+                          const void *alpha, const void *beta_logit, gdn_dtype act_dtype,
+                          const gdn_params *params, float *out, const gdn_dims *dims,
+                          int32_t n_tokens, gdn_stream_t stream)
+{
+    return layer_scan_common(state, conv_state, nullptr, nullptr, x, z, alpha, beta_logit,
+                             act_dtype, params, out, dims, n_tokens, stream);
+}
+
+gdn_status gdn_verify_kn(float *state, float *conv_state, float *state_snap, float *conv_snap,
+                         const void *x, const void *z, const void *alpha, const void *beta_logit,
+                         gdn_dtype act_dtype, const gdn_params *params, float *out,
+                         const gdn_dims *dims, int32_t n_draft, gdn_stream_t stream)
+{
+    if (!conv_snap || (n_draft > 1 && !state_snap) || state_snap == state ||
+        conv_snap == conv_state)
+        return GDN_ERR_INVALID_ARG;
+    return layer_scan_common(state, conv_state, state_snap, conv_snap, x, z, alpha, beta_logit,
+                             act_dtype, params, out, dims, n_draft, stream);
+}
+
+gdn_status gdn_verify_commit_kn(float *state, float *conv_state, const float *state_snap,
+                                const float *conv_snap, const int32_t *n_accept,
+                                const gdn_dims *dims, int32_t n_draft, gdn_stream_t stream)
+{
+    gdn_status st = check_dims(dims, 0);
+    if (st != GDN_OK)
+        return st;
+    if (n_draft < 1 || !state || !conv_state || !conv_snap || !n_accept ||
+        (n_draft > 1 && !state_snap) || !aligned(state, 16) ||
+        (state_snap && !aligned(state_snap, 16)))
+        return GDN_ERR_INVALID_ARG;
+    const int64_t d = dims->head_dim;
+    return from_cuda(gdn::launch_verify_commit_kn(
+        state, conv_state, state_snap, conv_snap, n_accept, dims->n_seq, n_draft,
+        (int64_t)dims->n_v_heads * d * d, (int64_t)conv_dim_of(dims) * (dims->d_conv - 1),
+        as_cuda(stream)));
+}
+
 gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, const void *z,
                                const void *alpha, const void *beta_logit, gdn_dtype act_dtype,
                                const gdn_params *params, float *out, const gdn_dims *dims,
@@ -289,15 +407,17 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
 
 gdn_status gdn_check_device(int32_t *code)
 {
-    int a = 0, b = 0;
+    int a = 0, b = 0, c = 0;
     gdn_status st = from_cuda(gdn::take_decode_device_error(&a));
     if (st == GDN_OK)
         st = from_cuda(gdn::take_prefill_device_error(&b));
+    if (st == GDN_OK)
+        st = from_cuda(gdn::take_sequential_device_error(&c));
     if (code)
-        *code = a | b;
+        *code = a | b | c;
     if (st != GDN_OK)
         return st;
-    return (a | b) ? GDN_ERR_DEVICE : GDN_OK;
+    return (a | b | c) ? GDN_ERR_DEVICE : GDN_OK;
 }
 
 const char *gdn_last_cuda_error(void) { return g_last_cuda_error; }

@@ -13,6 +13,7 @@
 // slices of a head through distributed shared memory.
 #include <cooperative_groups.h>
 
+#include "cluster.cuh"
 #include "gdn_device.cuh"
 #include "gdn_kernels.h"
 
@@ -129,19 +130,6 @@ __global__ void __launch_bounds__(256) gated_norm_kernel(const float *y, const f
 }
 
 // ------------------------------------------------------------------ fused step
-__device__ __forceinline__ void cluster_arrive_release()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait_acquire()
-{
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // NTOK = 1: one decode step. NTOK = 2: K=2 verify, snapshot after token 0.
 //
 // Order of a CTA's work, chosen so that no fence ever waits on the state
@@ -348,24 +336,6 @@ static int pick_nsplit(int B, int Hv, int r)
     while (ns < 4 && (int64_t)B * Hv * ns < target && r * ns * 2 <= 8)
         ns *= 2;
     return ns;
-}
-
-template <typename K, typename A>
-static cudaError_t launch_cluster(K kernel, dim3 grid, int csize, cudaStream_t s, const A &args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(256, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = csize > 1 ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
 template <typename TIn, int NTOK>

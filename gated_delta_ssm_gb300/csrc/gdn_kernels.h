@@ -40,6 +40,30 @@ struct RecArgs {
     float scale;
 };
 
+struct RecScanArgs {
+    float *state;          // [B][Hv][d][d]
+    const float *q, *k, *v;// token (b, t) at row b*T + t, qkv_stride apart
+    int64_t qkv_stride;
+    const float *g, *beta; // [B][T][Hv]
+    float *y;              // [B][T][Hv][d]
+    int B, Hq, Hv, T;
+    float scale;
+};
+
+// The fused layer stepped token by token over T tokens of every sequence.
+struct LayerScanArgs {
+    float *state;          // [B][Hv][d][d]
+    float *conv_state;     // [B][conv_dim][W-1]
+    float *state_snap;     // [B][T-1][Hv][d][d] or null
+    float *conv_snap;      // [B][T][conv_dim][W-1] or null
+    const void *x, *z, *alpha, *beta_logit;
+    const float *conv_w, *dt, *A_log, *norm_w;
+    float *out;            // [B][T][Hv][d]
+    int64_t x_stride, z_stride, gate_stride;
+    int B, Hq, Hv, W, conv_dim, T;
+    float l2_eps, rms_eps, scale;
+};
+
 struct PrefillArgs {
     float *state;
     float *conv_state;
@@ -64,6 +88,12 @@ cudaError_t launch_verify_commit(float *state, float *conv_state, const float *s
                                  int64_t state_elems, int64_t hist_elems, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s);
 cudaError_t take_decode_device_error(int *code);
+cudaError_t launch_recurrence_scan(const RecScanArgs &a, cudaStream_t s);
+cudaError_t launch_layer_scan(const LayerScanArgs &a, bool bf16, cudaStream_t s);
+cudaError_t launch_verify_commit_kn(float *state, float *conv_state, const float *state_snap,
+                                    const float *conv_snap, const int32_t *n_accept, int B, int K,
+                                    int64_t state_elems, int64_t hist_elems, cudaStream_t s);
+cudaError_t take_sequential_device_error(int *code);
 cudaError_t take_prefill_device_error(int *code);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, bool bf16, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs &a, bool bf16, cudaStream_t s);

@@ -210,6 +210,81 @@ gdn_status gdn_verify_commit(float *state, float *conv_state, const float *state
                              const gdn_dims *dims, gdn_stream_t stream);
 
 /*
+ * Sequential scan of the recurrence over n_tokens tokens of every sequence
+ * ("fm_kernel_ssm.h", "Delta-rule recurrence": the naive sequential scan,
+ * kept as the permanent correctness reference for the chunked path). Each
+ * state row stays in registers across the tokens and is written back once;
+ * per token the arithmetic is gdn_recurrence_decode's, so the result equals
+ * n_tokens gdn_recurrence_decode calls bit for bit.
+ *   q, k, v  token t of sequence b is row b*n_tokens + t: its QK head hk at
+ *            q + row*qkv_stride + hk*d (same for k), V head h at
+ *            v + row*qkv_stride + h*d
+ *   g, beta  float [B][n_tokens][Hv] (g pre-exp, beta already a sigmoid)
+ *   y        float [B][n_tokens][Hv][d]
+ * Errors: INVALID_ARG (null, n_tokens < 1, bad dims, qkv_stride too small),
+ * UNSUPPORTED (d, r).
+ */
+gdn_status gdn_recurrence_scan(float *state, const float *q, const float *k, const float *v,
+                               int64_t qkv_stride, const float *g, const float *beta, float *y,
+                               const gdn_dims *dims, int32_t n_tokens, float scale,
+                               gdn_stream_t stream);
+
+/*
+ * The fused layer step applied to n_tokens tokens of every sequence one token
+ * at a time, in ONE launch, with the state rows held in registers throughout:
+ * equal bit for bit to n_tokens gdn_decode_step calls. It is the on-device
+ * sequential reference for gdn_prefill_chunked at lengths beyond a CPU
+ * check ("fm_kernel_ssm.h", "Delta-rule recurrence").
+ *   state, conv_state updated in place; x, z, alpha, beta_logit as in LAYOUTS
+ *   with T = n_tokens; out float [B][n_tokens][Hv][d].
+ * Errors: INVALID_ARG (null, n_tokens < 1, bad dims), UNSUPPORTED (d, W, r).
+ */
+gdn_status gdn_layer_scan(float *state, float *conv_state, const void *x, const void *z,
+                          const void *alpha, const void *beta_logit, gdn_dtype act_dtype,
+                          const gdn_params *params, float *out, const gdn_dims *dims,
+                          int32_t n_tokens, gdn_stream_t stream);
+
+/*
+ * Draft verification of K = n_draft positions per sequence, every sequence in
+ * ONE launch ("ssm_mamba.rs", gdn_verify_fused_conv_kn and
+ * gdn_verify_fused_conv_kn_batched: all positions in one launch, every
+ * per-position rollback snapshot written inline, the committed window
+ * duplicated as the last snapshot so the caller issues no copies; here the
+ * recurrent state is snapshotted as well). Positions are applied exactly as
+ * K gdn_decode_step calls would apply them, bit for bit.
+ *   state, conv_state <- after position K-1 (the committed result)
+ *   state_snap float [B][K-1][Hv][d][d]: entry p = state after position p,
+ *              p = 0..K-2 (the state after K-1 is `state` itself, so it is
+ *              not duplicated: that would cost a full extra state write);
+ *              may be NULL when K == 1
+ *   conv_snap  float [B][K][conv_dim][W-1]: entry p = conv window after
+ *              position p; entry K-1 duplicates the committed conv_state
+ *   out float [B][K][Hv][d]; inputs are [B][K] token rows (row b*K + p).
+ * The snapshot arrays may not overlap state, conv_state or each other.
+ * Errors: INVALID_ARG (null, n_draft < 1, bad dims), UNSUPPORTED (d, W, r).
+ */
+gdn_status gdn_verify_kn(float *state, float *conv_state, float *state_snap, float *conv_snap,
+                         const void *x, const void *z, const void *alpha,
+                         const void *beta_logit, gdn_dtype act_dtype,
+                         const gdn_params *params, float *out, const gdn_dims *dims,
+                         int32_t n_draft, gdn_stream_t stream);
+
+/*
+ * Commit or roll back after gdn_verify_kn with the same n_draft = K. Per
+ * sequence b with n = n_accept[b] (device int32 [B]), the number of
+ * positions kept:
+ *   n == K      nothing (state and conv_state already hold all K);
+ *   1 <= n < K  state[b] <- state_snap[b][n-1], conv_state[b] <- conv_snap[b][n-1]
+ *               (bit-exact state after n decode steps);
+ *   otherwise   sequence b is left unchanged and bit 16 is set in the
+ *               device-side error word (see gdn_check_device).
+ * Errors: INVALID_ARG (null, n_draft < 1, bad dims), UNSUPPORTED (d).
+ */
+gdn_status gdn_verify_commit_kn(float *state, float *conv_state, const float *state_snap,
+                                const float *conv_snap, const int32_t *n_accept,
+                                const gdn_dims *dims, int32_t n_draft, gdn_stream_t stream);
+
+/*
  * Chunked prefill over n_tokens tokens of every sequence: the same function
  * as n_tokens gdn_decode_step calls, evaluated chunk by chunk
  * ("fm_kernel_ssm.h", "Delta-rule recurrence": the sequential scan is the
@@ -233,10 +308,11 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
 /*
  * Every wait inside a kernel (on a bulk copy or a tensor-core operation) is
  * bounded; a kernel whose wait gives up sets a bit in a device-side error word
- * and skips the rest of its work instead of hanging. This call waits for all
+ * and skips the rest of its work instead of hanging. gdn_verify_commit_kn
+ * sets bit 16 for an accepted count outside 1..K. This call waits for all
  * work on the device (it synchronises), reads the word into *code (may be
- * NULL) and clears it. Returns GDN_OK when no wait gave up, GDN_ERR_DEVICE when
- * one did, GDN_ERR_CUDA if the read failed.
+ * NULL) and clears it. Returns GDN_OK when no bit was set, GDN_ERR_DEVICE when
+ * one was, GDN_ERR_CUDA if the read failed.
  */
 gdn_status gdn_check_device(int32_t *code);
 

@@ -30,7 +30,9 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("gdn_conv_update", "gdn_decay_gate", "gdn_recurrence_decode", "gdn_verify_k2",
                      "gdn_prefill_chunked", "gdn_gated_norm", "gdn_decode_step",
-                     "gdn_verify_commit", "gdn_last_cuda_error", "gdn_version"):
+                     "gdn_verify_commit", "gdn_recurrence_scan", "gdn_layer_scan",
+                     "gdn_verify_kn", "gdn_verify_commit_kn", "gdn_last_cuda_error",
+                     "gdn_version"):
         assert required in names
 
 
@@ -117,6 +119,36 @@ def test_other_entry_points_validate(lib):
     assert lib.gdn_verify_commit(FAKE, FAKE, FAKE, FAKE, None, ct.byref(cd), None) == gdn.GDN_ERR_INVALID_ARG
     assert lib.gdn_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 7, ct.byref(_params().c()), FAKE,
                                ct.byref(cd), None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_scan_entry_points_validate(lib):
+    cd, cp = _dims().c(), _params().c()
+    # recurrence scan: n_tokens < 1, qkv_stride too small, null y
+    rs = lambda stride, n, y=FAKE: lib.gdn_recurrence_scan(FAKE, FAKE, FAKE, FAKE, stride, FAKE,
+                                                           FAKE, y, ct.byref(cd), n, 1.0, None)
+    assert rs(1536, 0) == gdn.GDN_ERR_INVALID_ARG
+    assert rs(10, 4) == gdn.GDN_ERR_INVALID_ARG
+    assert rs(1536, 4, None) == gdn.GDN_ERR_INVALID_ARG
+    layer = [FAKE] * 6 + [gdn.GDN_BF16, ct.byref(cp), FAKE, ct.byref(cd)]
+    assert lib.gdn_layer_scan(*layer, 0, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_layer_scan(*([FAKE + 4] + layer[1:]), 3, None) == gdn.GDN_ERR_INVALID_ARG
+    bad_w = gdn.Dims(n_seq=2, n_qk_heads=2, n_v_heads=4, d_conv=9).c()
+    assert lib.gdn_layer_scan(*layer[:9], ct.byref(bad_w), 3, None) == gdn.GDN_ERR_UNSUPPORTED
+
+
+def test_verify_kn_requires_distinct_snapshots(lib):
+    cd, cp = _dims().c(), _params().c()
+    tail = [FAKE] * 4 + [gdn.GDN_F32, ct.byref(cp), FAKE, ct.byref(cd)]
+    st, conv, ss, cs = FAKE, FAKE + 64, FAKE + 128, FAKE + 192
+    assert lib.gdn_verify_kn(st, conv, None, cs, *tail, 3, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_verify_kn(st, conv, ss, None, *tail, 3, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_verify_kn(st, conv, st, cs, *tail, 3, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_verify_kn(st, conv, ss, conv, *tail, 3, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_verify_kn(st, conv, ss, cs, *tail, 0, None) == gdn.GDN_ERR_INVALID_ARG
+    commit = lambda ss_, n: lib.gdn_verify_commit_kn(st, conv, ss_, cs, FAKE, ct.byref(cd), n, None)
+    assert commit(ss, 0) == gdn.GDN_ERR_INVALID_ARG
+    assert commit(None, 3) == gdn.GDN_ERR_INVALID_ARG
+    assert commit(ss + 4, 3) == gdn.GDN_ERR_INVALID_ARG
 
 
 def test_binding_raises_loudly_on_bad_status(lib):
