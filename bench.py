@@ -338,6 +338,61 @@ class Gpu:
                 "commit_us": mc * 1e6, "commit_GBps": 2 * n_rb * (sb // shape.B) / mc / 1e9,
                 "rollbacks": n_rb}
 
+    # -- generic-K draft verification (K = 4) + commit, K=2 verify's batch
+    def verify_kn(self, steps, warmup, K=4):
+        torch, gdn = self.torch, self.gdn
+        shape = synth.Shape(B=32, T=K, Hq=16, Hv=32, warm=True)
+        inp = synth.make_inputs(shape, seed=5)
+        nbuf = 2
+        d = self.upload(shape, inp, copies=nbuf)
+        B, Hv, dd = shape.B, shape.Hv, shape.d
+        snaps = [torch.empty(B, K - 1, Hv, dd, dd, device=self.dev) for _ in range(nbuf)]
+        hsnaps = [torch.empty((B, K) + tuple(d["hists"][0].shape[1:]), device=self.dev)
+                  for _ in range(nbuf)]
+        dims, prm = self.dims(shape), self.params(d)
+        out = torch.empty(B, K, Hv, dd, device=self.dev)
+        accept = torch.arange(B, dtype=torch.int32, device=self.dev) % K + 1
+
+        def vstep(i):
+            j = i % nbuf
+            gdn.verify_kn(d["states"][j], d["hists"][j], snaps[j], hsnaps[j], d["x"], d["z"],
+                          d["alpha"], d["beta_logit"], prm, out, dims, K)
+
+        def cstep(i):
+            j = i % nbuf
+            gdn.verify_commit_kn(d["states"][j], d["hists"][j], snaps[j], hsnaps[j], accept, dims, K)
+
+        tv = self.time_steps(vstep, steps, warmup)
+        tc = self.time_steps(cstep, steps, warmup)
+        self.launches += 2 * steps
+        sb = B * Hv * dd * dd * 4
+        mv, mc = statistics.mean(tv), statistics.mean(tc)
+        n_rb = int((accept < K).sum())
+        # state bytes: read once, the K-1 snapshots and the committed state written
+        return {"K": K, "verify_us": mv * 1e6, "verify_state_GBps": (1 + K) * sb / mv / 1e9,
+                "commit_us": mc * 1e6, "commit_GBps": 2 * n_rb * (sb // B) / mc / 1e9,
+                "rollbacks": n_rb}
+
+    # -- token-parallel conv + SiLU + Q/K L2 over the prefill workload
+    def conv_tokens(self, steps, warmup):
+        torch, gdn = self.torch, self.gdn
+        shape = synth.WORKLOADS["prefill"]
+        inp = synth.make_inputs(shape, seed=6)
+        d = self.upload(shape, inp)
+        B, T, cd = shape.B, shape.T, shape.conv_dim
+        out = torch.empty(B, T, cd, device=self.dev)
+        dims = self.dims(shape)
+
+        def step(i):
+            gdn.conv_update(d["hists"][0], d["x"], d["conv_w"], out, dims, T, 1e-6)
+
+        t = self.time_steps(step, steps, warmup)
+        self.launches += steps
+        m = statistics.mean(t)
+        act = 2 if shape.act_dtype == "bf16" else 4
+        nbytes = B * T * cd * (act + 4) + 2 * B * cd * (shape.W - 1) * 4 + cd * shape.W * 4
+        return {"us": m * 1e6, "GBps": nbytes / m / 1e9, "algorithmic_bytes": nbytes}
+
     # -- chunked prefill
     def prefill(self, steps, warmup):
         torch, gdn = self.torch, self.gdn
@@ -431,7 +486,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-extra", action="store_true", help="headline workload only")
-    ap.add_argument("--only", choices=["decode_b1", "verify_k2", "prefill"],
+    ap.add_argument("--only", choices=["decode_b1", "verify_k2", "verify_kn", "conv_tokens",
+                                       "prefill"],
                     help="run one secondary workload alone and print its figures (for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -444,6 +500,8 @@ def main(argv=None):
     if args.only:
         gpu = Gpu(local)
         fn = {"decode_b1": lambda: gpu.decode_b1(), "verify_k2": lambda: gpu.verify_k2(args.steps, args.warmup),
+              "verify_kn": lambda: gpu.verify_kn(args.steps, args.warmup),
+              "conv_tokens": lambda: gpu.conv_tokens(args.steps, args.warmup),
               "prefill": lambda: gpu.prefill(args.steps, args.warmup)}[args.only]
         print(json.dumps({"workload": args.only, **fn()}), flush=True)
         return 0
@@ -465,6 +523,8 @@ def main(argv=None):
     if not args.skip_extra:
         extra["decode_b1"] = gpu.decode_b1()
         extra["verify_k2"] = gpu.verify_k2(max(5, args.steps // 2), args.warmup)
+        extra["verify_kn"] = gpu.verify_kn(max(5, args.steps // 2), args.warmup)
+        extra["conv_tokens"] = gpu.conv_tokens(max(5, args.steps // 2), args.warmup)
         extra["prefill"] = gpu.prefill(max(3, args.steps // 5), 3)
     if rank != 0:
         if dist is not None:

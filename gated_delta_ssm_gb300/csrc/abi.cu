@@ -407,17 +407,20 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
 
 gdn_status gdn_check_device(int32_t *code)
 {
-    int a = 0, b = 0, c = 0;
+    int a = 0, b = 0, c = 0, d = 0;
     gdn_status st = from_cuda(gdn::take_decode_device_error(&a));
     if (st == GDN_OK)
         st = from_cuda(gdn::take_prefill_device_error(&b));
     if (st == GDN_OK)
         st = from_cuda(gdn::take_sequential_device_error(&c));
+    if (st == GDN_OK)
+        st = from_cuda(gdn::take_conv_device_error(&d));
+    const int all = a | b | c | d;
     if (code)
-        *code = a | b | c;
+        *code = all;
     if (st != GDN_OK)
         return st;
-    return (a | b | c) ? GDN_ERR_DEVICE : GDN_OK;
+    return all ? GDN_ERR_DEVICE : GDN_OK;
 }
 
 const char *gdn_last_cuda_error(void) { return g_last_cuda_error; }

@@ -35,33 +35,6 @@ __global__ void __launch_bounds__(256) decay_gate_kernel(const TIn *alpha, int64
     g[i] = decay_gate_f(load_act<TIn>(alpha + r * alpha_stride + h), __ldg(dt + h), __ldg(A_log + h));
 }
 
-// ------------------------------------------------------------------ conv + L2
-// One CTA of 128 threads per (128-channel head, sequence); thread i owns
-// channel i of the head and scans the tokens of the call in order.
-template <typename TIn>
-__global__ void __launch_bounds__(kD) conv_update_kernel(ConvArgs a)
-{
-    __shared__ float red[2][4];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b = blockIdx.y;
-    const int c = blockIdx.x * kD + tid;
-    const bool is_qk = blockIdx.x < 2 * a.Hq;
-    const int W = a.W;
-    float *hist_c = a.conv_state + ((size_t)b * a.conv_dim + c) * (W - 1);
-    const TIn *x_c = static_cast<const TIn *>(a.x) + (int64_t)b * a.T * a.x_stride + c;
-    const float *w_c = a.conv_w + (size_t)c * W;
-    float *out_c = a.out + (size_t)b * a.T * a.conv_dim + c;
-    for (int t = 0; t < a.T; ++t) {
-        float v = silu_f(conv_pre<TIn>(hist_c, x_c, a.x_stride, w_c, W, t));
-        if (is_qk)
-            v = __fmul_rn(v, head_l2_inv(v, a.l2_eps, red[t & 1], warp, lane));
-        out_c[(size_t)t * a.conv_dim] = v;
-    }
-    float nh[kMaxW - 1];
-    conv_history_after<TIn>(hist_c, x_c, a.x_stride, W, a.T, nh);
-    store_history(hist_c, W, nh);
-}
-
 // ------------------------------------------------------------------ recurrence
 template <int NSPLIT>
 __global__ void __launch_bounds__(256, 2) recurrence_decode_kernel(RecArgs a)
@@ -369,16 +342,6 @@ cudaError_t launch_decay_gate(const void *alpha, bool bf16, int64_t alpha_stride
     else
         decay_gate_kernel<<<blocks, 256, 0, s>>>(static_cast<const float *>(alpha), alpha_stride,
                                                  dt, A_log, g, rows, H);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_conv_update(const ConvArgs &a, bool bf16, cudaStream_t s)
-{
-    const dim3 grid(a.conv_dim / kD, a.B, 1);
-    if (bf16)
-        conv_update_kernel<__nv_bfloat16><<<grid, kD, 0, s>>>(a);
-    else
-        conv_update_kernel<float><<<grid, kD, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -38,10 +38,14 @@ __device__ __forceinline__ void st_stream(float *p, float4 v)
 }
 
 // ------------------------------------------------------------------ scalar maps
-// silu(x) = x * sigmoid(x) = x / (1 + e^-x)
+// silu(x) = x * sigmoid(x) = x / (1 + e^-x), from the hardware exponential and
+// the fast divide: a few ulp (about 1e-6 relative for |x| < 20), cheap enough
+// for the multi-token conv paths, where the IEEE divide alone dominated the
+// instruction count. Large negative x gives e^-x = inf and a quotient of 0;
+// large positive x gives x.
 __device__ __forceinline__ float silu_f(float x)
 {
-    return __fdiv_rn(x, __fadd_rn(1.0f, expf(-x)));
+    return __fdividef(x, __fadd_rn(1.0f, __expf(-x)));
 }
 
 __device__ __forceinline__ float sigmoid_f(float x)
@@ -181,6 +185,13 @@ __device__ __forceinline__ float row8_sum(float v)
 // warps (thread i of the head = channel i). red4 is 4 floats of shared memory
 // private to this head. Returns 1 / sqrt(sum v^2 + eps) to every thread.
 // Caller must __syncthreads() between this and any reuse of red4.
+// The head's 1 / sqrt(sum v^2 + eps) from its four 32-channel warp sums, in order.
+__device__ __forceinline__ float l2_inv_of_partials(const float *red4, float eps)
+{
+    const float tot = __fadd_rn(__fadd_rn(__fadd_rn(red4[0], red4[1]), red4[2]), red4[3]);
+    return rsqrtf(__fadd_rn(tot, eps));
+}
+
 __device__ __forceinline__ float head_l2_inv(float v, float eps, float *red4, int warp_in_head,
                                              int lane)
 {
@@ -188,8 +199,7 @@ __device__ __forceinline__ float head_l2_inv(float v, float eps, float *red4, in
     if (lane == 0)
         red4[warp_in_head] = s;
     __syncthreads();
-    const float tot = __fadd_rn(__fadd_rn(__fadd_rn(red4[0], red4[1]), red4[2]), red4[3]);
-    return rsqrtf(__fadd_rn(tot, eps));
+    return l2_inv_of_partials(red4, eps);
 }
 
 // ------------------------------------------------------------------ gated norm

@@ -94,6 +94,7 @@ cudaError_t launch_verify_commit_kn(float *state, float *conv_state, const float
                                     const float *conv_snap, const int32_t *n_accept, int B, int K,
                                     int64_t state_elems, int64_t hist_elems, cudaStream_t s);
 cudaError_t take_sequential_device_error(int *code);
+cudaError_t take_conv_device_error(int *code);
 cudaError_t take_prefill_device_error(int *code);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, bool bf16, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs &a, bool bf16, cudaStream_t s);

@@ -121,8 +121,12 @@ gdn_status gdn_decay_gate(const void *alpha, gdn_dtype alpha_dtype, int64_t alph
  *   conv_state [B][conv_dim][W-1] updated in place (ends holding the last
  *              W-1 raw inputs); x as in LAYOUTS (dims->x_stride);
  *   out        float [B][n_tokens][conv_dim] dense: [Q^ | K^ | V].
- * dims->z_stride and gate_stride are not used.
- * Errors: INVALID_ARG (null, n_tokens < 1, bad dims), UNSUPPORTED (d, W).
+ * dims->z_stride and gate_stride are not used. With n_tokens > 1 the tokens
+ * are computed in parallel ("ssm_mamba.rs", token-parallel prefill conv1d:
+ * the window slides over inputs, so no output depends on another), bit for
+ * bit equal to n_tokens single-token calls. n_tokens <= 2,097,120.
+ * Errors: INVALID_ARG (null, n_tokens < 1, bad dims), UNSUPPORTED (d, W),
+ * CUDA (n_tokens above the limit).
  */
 gdn_status gdn_conv_update(float *conv_state, const void *x, gdn_dtype x_dtype,
                            const float *conv_w, float *out, const gdn_dims *dims,
@@ -308,8 +312,10 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
 /*
  * Every wait inside a kernel (on a bulk copy or a tensor-core operation) is
  * bounded; a kernel whose wait gives up sets a bit in a device-side error word
- * and skips the rest of its work instead of hanging. gdn_verify_commit_kn
- * sets bit 16 for an accepted count outside 1..K. This call waits for all
+ * and skips the rest of its work instead of hanging (bits 1, 2, 8: the chunked
+ * prefill's tensor-core and copy waits; bit 64: the multi-token conv's tile
+ * copy wait). gdn_verify_commit_kn sets bit 16 for an accepted count outside
+ * 1..K. This call waits for all
  * work on the device (it synchronises), reads the word into *code (may be
  * NULL) and clears it. Returns GDN_OK when no bit was set, GDN_ERR_DEVICE when
  * one was, GDN_ERR_CUDA if the read failed.

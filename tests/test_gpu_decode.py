@@ -240,6 +240,58 @@ def test_conv_scan_equals_single_steps_bitwise():
     assert max_rel(full.cpu().numpy(), ref["conv"], 1) <= 1e-5
 
 
+@pytest.mark.parametrize("B,T,W,act,pad", [(2, 100, 4, "bf16", 0), (1, 33, 8, "f32", 0),
+                                           (3, 64, 2, "bf16", 0), (2, 3, 8, "bf16", 0),
+                                           (2, 200, 4, "f32", 0), (2, 100, 4, "bf16", 4),
+                                           (1, 70, 3, "f32", 1)])
+def test_token_parallel_conv_equals_serial_steps(B, T, W, act, pad):
+    # several tiles with a ragged tail (and T < W-1): the multi-token kernels against
+    # T single-token calls of the serial kernel, bit for bit. Rows padded by a
+    # non-multiple of 16 bytes take the plain-load kernel instead of the tiled one.
+    base = synth.Shape(B=B, T=T, Hq=2, Hv=6, W=W, act_dtype=act, warm=True)
+    shape = synth.Shape(B=B, T=T, Hq=2, Hv=6, W=W, act_dtype=act, warm=True,
+                        x_stride=base.conv_dim + pad)
+    inp = synth.make_inputs(shape, seed=27 + T)
+    dev = device_inputs(shape, inp)
+    dims = dims_of(shape)
+    cd = shape.conv_dim
+    h1 = dev["hist"].clone()
+    full = torch.empty(B, T, cd, device="cuda")
+    gdn.conv_update(h1, dev["x"], dev["conv_w"], full, dims, T, 1e-6)
+    h2 = dev["hist"].clone()
+    steps = torch.empty_like(full)
+    one = torch.empty(B, 1, cd, device="cuda")
+    dims1 = dims_of(shape, rows_per_seq=T)
+    for t in range(T):
+        gdn.conv_update(h2, dev["x"][:, t:t + 1], dev["conv_w"], one, dims1, 1, 1e-6)
+        steps[:, t] = one[:, 0]
+    torch.cuda.synchronize()
+    assert torch.equal(full, steps) and torch.equal(h1, h2)
+    ref = run_oracle(shape, inp, intermediates=True)
+    assert max_rel(full.cpu().numpy(), ref["conv"], 1) <= 1e-5
+    assert np.array_equal(h1.cpu().numpy(), ref["hist"].astype(np.float32))
+
+
+def test_token_parallel_conv_full_prefill_size_equals_serial():
+    # 4 x 8192 tokens of the 8192-channel prefill layer, every element
+    shape = synth.WORKLOADS["prefill"]
+    inp = synth.make_inputs(shape, seed=28)
+    dev = device_inputs(shape, inp)
+    B, T, cd = shape.B, shape.T, shape.conv_dim
+    h1 = dev["hist"].clone()
+    full = torch.empty(B, T, cd, device="cuda")
+    gdn.conv_update(h1, dev["x"], dev["conv_w"], full, dims_of(shape), T, 1e-6)
+    h2 = dev["hist"].clone()
+    one = torch.empty(B, 1, cd, device="cuda")
+    dims1 = dims_of(shape, rows_per_seq=T)
+    same = True
+    for t in range(T):
+        gdn.conv_update(h2, dev["x"][:, t:t + 1], dev["conv_w"], one, dims1, 1, 1e-6)
+        same &= bool(torch.equal(one[:, 0], full[:, t]))
+    torch.cuda.synchronize()
+    assert same and torch.equal(h1, h2)
+
+
 def test_result_independent_of_batch_split():
     # the same sequence decoded alone (few CTAs: row-split clusters) and inside a
     # large batch (one CTA per head) gives identical bits
