@@ -39,7 +39,8 @@ from gated_delta_ssm_gb300 import synth  # noqa: E402
 
 METRIC = "GDN decode: state HBM GB/s (% of peak), seqs/s; prefill tokens/s"
 HEADLINE = "decode_b64"
-KERNEL_SOURCES = ["gated_delta_ssm_gb300/csrc/decode.cu", "gated_delta_ssm_gb300/csrc/gdn_device.cuh"]
+KERNEL_SOURCES = ["gated_delta_ssm_gb300/csrc/decode.cu", "gated_delta_ssm_gb300/csrc/gdn_device.cuh",
+                  "gated_delta_ssm_gb300/csrc/cluster.cuh"]
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -343,7 +344,7 @@ class Gpu:
         torch, gdn = self.torch, self.gdn
         shape = synth.Shape(B=32, T=K, Hq=16, Hv=32, warm=True)
         inp = synth.make_inputs(shape, seed=5)
-        nbuf = 2
+        nbuf = 3                                   # 3 x 64 MiB state (+ snapshots): beyond L2
         d = self.upload(shape, inp, copies=nbuf)
         B, Hv, dd = shape.B, shape.Hv, shape.d
         snaps = [torch.empty(B, K - 1, Hv, dd, dd, device=self.dev) for _ in range(nbuf)]
