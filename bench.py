@@ -308,6 +308,31 @@ class Gpu:
         return {"us_per_step": per * 1e6, "state_GBps": st / per / 1e9, "steps_in_graph": n_steps,
                 "state_buffers": nbuf}
 
+    # -- the batched decode with bf16 state and output (serving option)
+    def decode_b64_bf16_state(self, steps, warmup):
+        torch, gdn = self.torch, self.gdn
+        shape = synth.WORKLOADS["decode_b64"]
+        inp = synth.make_inputs(shape, seed=2)
+        d = self.upload(shape, inp)
+        bits = torch.from_numpy(synth.bf16_round(inp["state"]).view(np.int16)).view(torch.bfloat16)
+        nbuf = 3                                   # 3 x 96 MiB bf16 state: beyond L2
+        states = [bits.to(self.dev) for _ in range(nbuf)]
+        dims = self.dims(shape)
+        prm = self.params(d)
+        out = torch.empty(shape.B, shape.Hv, shape.d, device=self.dev, dtype=torch.bfloat16)
+
+        def step(i):
+            gdn.decode_step_bf16_state(states[i % nbuf], d["hists"][0], d["x"], d["z"], d["alpha"],
+                                       d["beta_logit"], prm, out, dims)
+
+        t = self.time_steps(step, steps, warmup)
+        self.launches += steps
+        m = statistics.mean(t)
+        sb = 2 * shape.B * shape.Hv * shape.d * shape.d * 2
+        hbm_peak, _, _ = measured_peaks()
+        return {"us_per_step": m * 1e6, "state_GBps": sb / m / 1e9,
+                "pct_of_peak": 100.0 * sb / m / 1e9 / hbm_peak, "seqs_per_s": shape.B / m}
+
     # -- K=2 verify + commit
     def verify_k2(self, steps, warmup):
         torch, gdn = self.torch, self.gdn
@@ -487,8 +512,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-extra", action="store_true", help="headline workload only")
-    ap.add_argument("--only", choices=["decode_b1", "verify_k2", "verify_kn", "conv_tokens",
-                                       "prefill"],
+    ap.add_argument("--only", choices=["decode_b1", "decode_b64_bf16_state", "verify_k2",
+                                       "verify_kn", "conv_tokens", "prefill"],
                     help="run one secondary workload alone and print its figures (for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -502,6 +527,7 @@ def main(argv=None):
         gpu = Gpu(local)
         fn = {"decode_b1": lambda: gpu.decode_b1(), "verify_k2": lambda: gpu.verify_k2(args.steps, args.warmup),
               "verify_kn": lambda: gpu.verify_kn(args.steps, args.warmup),
+              "decode_b64_bf16_state": lambda: gpu.decode_b64_bf16_state(args.steps, args.warmup),
               "conv_tokens": lambda: gpu.conv_tokens(args.steps, args.warmup),
               "prefill": lambda: gpu.prefill(args.steps, args.warmup)}[args.only]
         print(json.dumps({"workload": args.only, **fn()}), flush=True)
@@ -523,6 +549,7 @@ def main(argv=None):
     extra = {}
     if not args.skip_extra:
         extra["decode_b1"] = gpu.decode_b1()
+        extra["decode_b64_bf16_state"] = gpu.decode_b64_bf16_state(args.steps, args.warmup)
         extra["verify_k2"] = gpu.verify_k2(max(5, args.steps // 2), args.warmup)
         extra["verify_kn"] = gpu.verify_kn(max(5, args.steps // 2), args.warmup)
         extra["conv_tokens"] = gpu.conv_tokens(max(5, args.steps // 2), args.warmup)

@@ -20,7 +20,8 @@ __all__ = [
     "Dims", "Params", "GdnError", "load", "library_path",
     "decay_gate", "conv_update", "recurrence_decode", "gated_norm",
     "decode_step", "verify_k2", "verify_commit", "prefill_chunked", "recurrence_scan",
-    "layer_scan", "verify_kn", "verify_commit_kn", "check_device", "version",
+    "layer_scan", "verify_kn", "verify_commit_kn", "decode_step_bf16_state", "check_device",
+    "version",
 ]
 
 _PKG = _os.path.dirname(_os.path.abspath(__file__))
@@ -110,6 +111,7 @@ def load():
             "gdn_recurrence_decode": [vp, vp, vp, vp, i64, vp, vp, vp, pd, f32, vp],
             "gdn_gated_norm": [vp, vp, vp, _ct.c_int, i64, vp, i32, i32, i32, f32, vp],
             "gdn_decode_step": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, vp],
+            "gdn_decode_step_bf16_state": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, vp],
             "gdn_verify_k2": [vp, vp, vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, vp],
             "gdn_verify_commit": [vp, vp, vp, vp, vp, pd, vp],
             "gdn_prefill_chunked": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, i32, i32, vp],
@@ -218,6 +220,20 @@ def decode_step(state, conv_state, x, z, alpha, beta_logit, params: Params, out,
                                   _ptr(beta_logit), _dtype(x), _ct.byref(cp), _ptr(out),
                                   _ct.byref(cd), _stream(stream)),
            "gdn_decode_step")
+
+
+def decode_step_bf16_state(state, conv_state, x, z, alpha, beta_logit, params: Params, out,
+                           dims: Dims, stream=None):
+    """state and out are bfloat16 tensors; see gdn_decode_step_bf16_state."""
+    import torch
+    if state.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise TypeError("state and out must be bfloat16")
+    cd, cp = dims.c(), params.c()
+    _check(load().gdn_decode_step_bf16_state(_ptr(state), _ptr(conv_state), _ptr(x), _ptr(z),
+                                             _ptr(alpha), _ptr(beta_logit), _dtype(x),
+                                             _ct.byref(cp), _ptr(out), _ct.byref(cd),
+                                             _stream(stream)),
+           "gdn_decode_step_bf16_state")
 
 
 def verify_k2(state, conv_state, state_snap, conv_snap, x, z, alpha, beta_logit, params: Params,

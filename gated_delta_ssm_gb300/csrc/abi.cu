@@ -70,10 +70,11 @@ gdn_status check_params(const gdn_params *p)
 
 int conv_dim_of(const gdn_dims *d) { return (2 * d->n_qk_heads + d->n_v_heads) * d->head_dim; }
 
-gdn_status fused_common(float *state, float *conv_state, float *state_snap, float *conv_snap,
+// bf16_state: state and out are bf16 (single-token step only).
+gdn_status fused_common(void *state, float *conv_state, float *state_snap, float *conv_snap,
                         const void *x, const void *z, const void *alpha, const void *beta_logit,
-                        gdn_dtype act_dtype, const gdn_params *params, float *out,
-                        const gdn_dims *dims, int ntok, gdn_stream_t stream)
+                        gdn_dtype act_dtype, const gdn_params *params, void *out,
+                        const gdn_dims *dims, int ntok, bool bf16_state, gdn_stream_t stream)
 {
     gdn_status st = check_dims(dims, 7);
     if (st != GDN_OK)
@@ -88,8 +89,9 @@ gdn_status fused_common(float *state, float *conv_state, float *state_snap, floa
         return GDN_ERR_INVALID_ARG;
     const size_t es = act_size(act_dtype);
     if (!aligned(state, 16) || (state_snap && !aligned(state_snap, 16)) || !aligned(x, es) ||
-        !aligned(z, es) || !aligned(alpha, es) || !aligned(beta_logit, es) || !aligned(out, 4) ||
-        !aligned(conv_state, 4) || (conv_snap && !aligned(conv_snap, 4)))
+        !aligned(z, es) || !aligned(alpha, es) || !aligned(beta_logit, es) ||
+        !aligned(out, bf16_state ? 2 : 4) || !aligned(conv_state, 4) ||
+        (conv_snap && !aligned(conv_snap, 4)))
         return GDN_ERR_INVALID_ARG;
     gdn::FusedArgs a;
     a.state = state;
@@ -116,6 +118,9 @@ gdn_status fused_common(float *state, float *conv_state, float *state_snap, floa
     a.l2_eps = params->l2_eps;
     a.rms_eps = params->rms_eps;
     a.scale = 1.0f / sqrtf((float)dims->head_dim);
+    if (bf16_state)
+        return from_cuda(gdn::launch_decode_fused_bf16_state(a, act_dtype == GDN_BF16,
+                                                             as_cuda(stream)));
     return from_cuda(gdn::launch_decode_fused(a, act_dtype == GDN_BF16, ntok, as_cuda(stream)));
 }
 
@@ -256,7 +261,16 @@ gdn_status gdn_decode_step(float *state, float *conv_state, const void *x, const
                            gdn_stream_t stream)
 {
     return fused_common(state, conv_state, nullptr, nullptr, x, z, alpha, beta_logit, act_dtype,
-                        params, out, dims, 1, stream);
+                        params, out, dims, 1, false, stream);
+}
+
+gdn_status gdn_decode_step_bf16_state(void *state, float *conv_state, const void *x,
+                                      const void *z, const void *alpha, const void *beta_logit,
+                                      gdn_dtype act_dtype, const gdn_params *params, void *out,
+                                      const gdn_dims *dims, gdn_stream_t stream)
+{
+    return fused_common(state, conv_state, nullptr, nullptr, x, z, alpha, beta_logit, act_dtype,
+                        params, out, dims, 1, true, stream);
 }
 
 gdn_status gdn_verify_k2(float *state, float *conv_state, float *state_snap, float *conv_snap,
@@ -267,7 +281,7 @@ gdn_status gdn_verify_k2(float *state, float *conv_state, float *state_snap, flo
     if (state_snap == state || conv_snap == conv_state)
         return GDN_ERR_INVALID_ARG;
     return fused_common(state, conv_state, state_snap, conv_snap, x, z, alpha, beta_logit,
-                        act_dtype, params, out, dims, 2, stream);
+                        act_dtype, params, out, dims, 2, false, stream);
 }
 
 gdn_status gdn_verify_commit(float *state, float *conv_state, const float *state_snap,

@@ -113,9 +113,16 @@ __global__ void __launch_bounds__(256) gated_norm_kernel(const float *y, const f
 // through distributed shared memory when NSPLIT > 1); (7) state stores; (8)
 // cluster wait, then the single owner of each Q/K channel rewrites its
 // history.
-template <typename TIn, int NTOK, int NSPLIT>
+//
+// TS is the storage type of the state and the output: float, or bf16 for the
+// bf16-state decode (NTOK = 1 only), whose rows are widened to fp32 on load,
+// stepped in fp32 and rounded to nearest even on store.
+template <typename TIn, int NTOK, int NSPLIT, typename TS = float>
 __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
 {
+    static_assert(sizeof(TS) == 4 || NTOK == 1, "snapshots are float32");
+    TS *const state = static_cast<TS *>(a.state);
+    TS *const out = static_cast<TS *>(a.out);
     constexpr int ROWS = kD / NSPLIT;   // value rows of one head in this CTA
     constexpr int RPW = ROWS / 8;       // rows per warp
     constexpr int NG = RPW / 4;         // 4-row groups per warp
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
     const size_t head_off = ((size_t)b * a.Hv + h) * kD * kD;
     const size_t warp_off = (size_t)(row0 + warp * RPW) * kD;
     float4 st[NG][4];
-    load_rows<NG>(a.state + head_off + warp_off, st);
+    load_rows<NG>(state + head_off + warp_off, st);
 
     // (2) conv windows: Q/K channel (every thread), V channel (threads < ROWS); gate inputs
     const bool is_k = tid >= kD;
@@ -211,7 +218,9 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
     __syncthreads();
 
     // (5) recurrence over this CTA's rows, in registers
-    step_rows<NG, NTOK, SNAP>(st, SNAP ? a.state_snap + head_off + warp_off : nullptr, sk, sq, sv,
+    step_rows<NG, NTOK, SNAP>(st, SNAP ? static_cast<float *>(a.state_snap) + head_off + warp_off
+                                       : nullptr,
+                              sk, sq, sv,
                               ROWS, sdecay, sbeta, sy, warp * RPW, a.scale);
     __syncthreads();
 
@@ -248,14 +257,15 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
             const float inv = norm_inv(bp[0], bp[1], bp[2], bp[3], a.rms_eps);
             const int j = row0 + tid;
             const int64_t row = tok0 + p;
-            a.out[((size_t)row * a.Hv + h) * kD + j] = gated_out(sy[p * ROWS + tid], inv, nw, zj[p]);
+            store_out(out + ((size_t)row * a.Hv + h) * kD + j,
+                      gated_out(sy[p * ROWS + tid], inv, nw, zj[p]));
         }
     }
     if (NSPLIT > 1)
         cluster_arrive_relaxed();   // this CTA no longer reads its peers' shared memory
 
     // (7) state rows back to HBM
-    store_rows<NG>(st, a.state + head_off + warp_off);
+    store_rows<NG>(st, state + head_off + warp_off);
 
     // (8) Q/K history: each channel rewritten by exactly one CTA of the cluster,
     // after every CTA of the cluster has read it
@@ -311,17 +321,23 @@ static int pick_nsplit(int B, int Hv, int r)
     return ns;
 }
 
-template <typename TIn, int NTOK>
+template <typename TIn, int NTOK, typename TS = float>
 static cudaError_t fused_dispatch(const FusedArgs &a, cudaStream_t s)
 {
     const int r = a.Hv / a.Hq;
     const int ns = pick_nsplit(a.B, a.Hv, r);
     const dim3 grid(a.Hv * ns, a.B, 1);
     switch (ns) {
-    case 1: return launch_cluster(decode_fused_kernel<TIn, NTOK, 1>, grid, r, s, a);
-    case 2: return launch_cluster(decode_fused_kernel<TIn, NTOK, 2>, grid, r * 2, s, a);
-    default: return launch_cluster(decode_fused_kernel<TIn, NTOK, 4>, grid, r * 4, s, a);
+    case 1: return launch_cluster(decode_fused_kernel<TIn, NTOK, 1, TS>, grid, r, s, a);
+    case 2: return launch_cluster(decode_fused_kernel<TIn, NTOK, 2, TS>, grid, r * 2, s, a);
+    default: return launch_cluster(decode_fused_kernel<TIn, NTOK, 4, TS>, grid, r * 4, s, a);
     }
+}
+
+cudaError_t launch_decode_fused_bf16_state(const FusedArgs &a, bool bf16, cudaStream_t s)
+{
+    return bf16 ? fused_dispatch<__nv_bfloat16, 1, __nv_bfloat16>(a, s)
+                : fused_dispatch<float, 1, __nv_bfloat16>(a, s);
 }
 
 cudaError_t launch_decode_fused(const FusedArgs &a, bool bf16, int ntok, cudaStream_t s)

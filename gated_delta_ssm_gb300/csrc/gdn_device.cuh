@@ -346,4 +346,50 @@ __device__ __forceinline__ void store_rows(const float4 (&r)[NG][4], float *rows
             st_stream(rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4, r[gi][m]);
 }
 
+// bf16 storage of the same rows (the bf16-state decode): lane l holds the same
+// 16 columns as above, loaded as four 8-byte groups (each warp load instruction
+// covers 64 contiguous bytes of four rows), widened exactly to fp32; stores
+// round to nearest even.
+template <int NG>
+__device__ __forceinline__ void load_rows(const __nv_bfloat16 *rows, float4 (&r)[NG][4])
+{
+    const int lane = threadIdx.x & 31;
+    const int rg = lane >> 3;
+    const int sub = lane & 7;
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(
+                rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4));
+            const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+            const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+            r[gi][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+}
+
+template <int NG>
+__device__ __forceinline__ void store_rows(const float4 (&r)[NG][4], __nv_bfloat16 *rows)
+{
+    const int lane = threadIdx.x & 31;
+    const int rg = lane >> 3;
+    const int sub = lane & 7;
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(r[gi][m].x, r[gi][m].y);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(r[gi][m].z, r[gi][m].w);
+            uint2 u;
+            u.x = *reinterpret_cast<const uint32_t *>(&lo);
+            u.y = *reinterpret_cast<const uint32_t *>(&hi);
+            __stcs(reinterpret_cast<uint2 *>(rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4),
+                   u);
+        }
+}
+
+// One output value in the storage type (bf16: round to nearest even).
+__device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
 }  // namespace gdn

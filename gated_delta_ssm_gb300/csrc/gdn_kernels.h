@@ -8,13 +8,13 @@
 namespace gdn {
 
 struct FusedArgs {
-    float *state;          // [B][Hv][d][d]
+    void *state;           // [B][Hv][d][d], float (bf16 for the bf16-state step)
     float *conv_state;     // [B][conv_dim][W-1]
-    float *state_snap;     // verify only
+    void *state_snap;      // verify only, float
     float *conv_snap;      // verify only
     const void *x, *z, *alpha, *beta_logit;
     const float *conv_w, *dt, *A_log, *norm_w;
-    float *out;            // [B][NTOK][Hv][d]
+    void *out;             // [B][NTOK][Hv][d], the state's type
     int64_t x_stride, z_stride, gate_stride;
     int B, Hq, Hv, W, conv_dim;
     float l2_eps, rms_eps, scale;
@@ -76,6 +76,7 @@ struct PrefillArgs {
 };
 
 cudaError_t launch_decode_fused(const FusedArgs &a, bool bf16, int ntok, cudaStream_t s);
+cudaError_t launch_decode_fused_bf16_state(const FusedArgs &a, bool bf16, cudaStream_t s);
 cudaError_t launch_decay_gate(const void *alpha, bool bf16, int64_t alpha_stride, const float *dt,
                               const float *A_log, float *g, int rows, int H, cudaStream_t s);
 cudaError_t launch_conv_update(const ConvArgs &a, bool bf16, cudaStream_t s);

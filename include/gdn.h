@@ -182,6 +182,25 @@ gdn_status gdn_decode_step(float *state, float *conv_state, const void *x, const
                            gdn_stream_t stream);
 
 /*
+ * gdn_decode_step with the recurrent state and the output stored as bf16: a
+ * serving option that halves the state traffic of a decode step. The pages
+ * define no such variant (their state is float32); it is offered outside the
+ * float32 tolerances. Each state row is widened exactly to float32, stepped
+ * with the same float32 arithmetic as gdn_decode_step (the readout uses the
+ * updated row before it is rounded), and rounded to nearest even when stored;
+ * each output value is rounded to nearest even.
+ *   state  bf16 [B][Hv][d][d] (same layout as the float32 state), in place
+ *   out    bf16 [B][Hv][d]
+ *   conv_state, x, z, alpha, beta_logit, params, dims as for gdn_decode_step
+ *          (the conv history stays float32).
+ * Errors: INVALID_ARG, UNSUPPORTED as for gdn_decode_step.
+ */
+gdn_status gdn_decode_step_bf16_state(void *state, float *conv_state, const void *x,
+                                      const void *z, const void *alpha, const void *beta_logit,
+                                      gdn_dtype act_dtype, const gdn_params *params, void *out,
+                                      const gdn_dims *dims, gdn_stream_t stream);
+
+/*
  * K=2 draft verification ("ssm_mamba.rs", gdn_verify_fused_conv_k2 and
  * gdn_verify_fused_norm_k2): both positions of every sequence in ONE launch.
  * Position 0 then position 1 are applied exactly as two gdn_decode_step calls

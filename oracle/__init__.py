@@ -71,7 +71,9 @@ def lib():
                 _F, _ct.c_long, _F, _ct.c_long, _F, _F,
                 _F, _F, _F, _F, _ct.c_double, _ct.c_double,
                 _D, _D, _D, _D, _D, _D, _D,
-                _ct.c_int, _D, _D]
+                _ct.c_int, _D, _D, _ct.c_int]
+            L.gdnref_round_bf16.restype = _ct.c_double
+            L.gdnref_round_bf16.argtypes = [_ct.c_double]
             L.gdnref_recurrence_scan.restype = None
             L.gdnref_recurrence_scan.argtypes = [_ct.c_int, _ct.c_int, _D, _D, _D, _D, _D,
                                                  _D, _D, _ct.c_double]
@@ -152,6 +154,11 @@ def gated_norm(y, w, z, eps):
     return out
 
 
+def round_bf16(v: float) -> float:
+    """Nearest bfloat16 value of a double, ties to even (gdnref_round_bf16)."""
+    return lib().gdnref_round_bf16(float(v))
+
+
 def recurrence_scan(q, k, v, g, beta, S, scale):
     """Sequential scan for one head: q,k,v [T][d], g, beta [T], S [d][d] plain (copied)."""
     q, k, v, g, beta = map(_f64, (q, k, v, g, beta))
@@ -166,7 +173,7 @@ def recurrence_scan(q, k, v, g, beta, S, scale):
 # ---------------------------------------------------------------- whole layer
 def layer(x, z, alpha, beta_logit, conv_w, dt, A_log, norm_w, state_d1, hist,
           Hq, W, l2_eps=1e-6, rms_eps=1e-6, seqs=None, snap_after=-1,
-          intermediates=False, threads=None):
+          intermediates=False, threads=None, bf16_state=False):
     """Run the layer over every token of each selected sequence.
 
     Activations are float32 arrays holding the exact input values
@@ -177,6 +184,8 @@ def layer(x, z, alpha, beta_logit, conv_w, dt, A_log, norm_w, state_d1, hist,
       out [b][T][Hv][d], state (library layout), hist, and with
       ``intermediates`` also conv [b][T][conv_dim], g, beta [b][T][Hv], y [b][T][Hv][d];
       with snap_after >= 0 also state_snap, hist_snap.
+    bf16_state runs the bf16-state variant: each head's state is rounded to
+    bfloat16 after its step and each output value is rounded to bfloat16.
     Sequences run in parallel threads (the C call releases the GIL).
     """
     L = lib()
@@ -216,7 +225,7 @@ def layer(x, z, alpha, beta_logit, conv_w, dt, A_log, norm_w, state_d1, hist,
                             float(l2_eps), float(rms_eps),
                             _pd(S), _pd(hb), _pd(out),
                             _pd(inter[0]), _pd(inter[1]), _pd(inter[2]), _pd(inter[3]),
-                            int(snap_after), _pd(Ss), _pd(hs))
+                            int(snap_after), _pd(Ss), _pd(hs), int(bool(bf16_state)))
         if rc != 0:
             raise ValueError("oracle rejected the shape")
         res["out"][n] = out

@@ -159,6 +159,30 @@ void gdnref_gated_norm(const double *y, const float *w, const double *z,
 }
 
 /*
+ * Round a double to the nearest bfloat16 value, ties to even: the storage
+ * rounding of the bf16-state decode variant (a serving option that has no
+ * counterpart on the pages). bfloat16 keeps float32's exponent range and 8
+ * significant bits, so a value in the binade [2^(e-1), 2^e) is rounded to a
+ * multiple of 2^(e-8); below 2^-126 the spacing stays 2^-133 (subnormals);
+ * a result of magnitude 2^128 or more is an overflow to infinity.
+ */
+double gdnref_round_bf16(double v)
+{
+    if (v != v || v == 0.0 || isinf(v))
+        return v;
+    int e;
+    frexp(v, &e);
+    int q = e - 8;
+    if (q < -133)
+        q = -133;
+    /* scaling by a power of two is exact; rint rounds half to even */
+    const double r = ldexp(rint(ldexp(v, -q)), q);
+    if (fabs(r) >= ldexp(1.0, 128))
+        return v > 0 ? INFINITY : -INFINITY;
+    return r;
+}
+
+/*
  * The whole layer step for ONE sequence over T tokens, one token at a time.
  *
  * Per token: conv + SiLU over all channels; split [Q | K | V]; L2-normalise
@@ -179,6 +203,9 @@ void gdnref_gated_norm(const double *y, const float *w, const double *z,
  *   g_out, beta_out [T][Hv]
  *   y_out  [T][Hv][d]       recurrence readout before the norm
  *   snap_after >= 0: after that token, S and hist are copied to S_snap/hist_snap.
+ * bf16_state != 0: the bf16-state variant. After each head's step (whose
+ * readout uses the updated state before rounding) its state is rounded to
+ * bfloat16, and each output value is rounded to bfloat16.
  * Returns 0, or -1 on a bad shape.
  */
 int gdnref_layer(int T, int Hq, int Hv, int d, int W,
@@ -189,7 +216,7 @@ int gdnref_layer(int T, int Hq, int Hv, int d, int W,
                  const float *norm_w, double l2_eps, double rms_eps,
                  double *S, double *hist, double *out,
                  double *conv_out, double *g_out, double *beta_out, double *y_out,
-                 int snap_after, double *S_snap, double *hist_snap)
+                 int snap_after, double *S_snap, double *hist_snap, int bf16_state)
 {
     if (T < 0 || Hq <= 0 || Hv <= 0 || d <= 0 || W < 1 || Hv % Hq != 0)
         return -1;
@@ -231,7 +258,15 @@ int gdnref_layer(int T, int Hq, int Hv, int d, int W,
             const float *zt = z + (size_t)t * z_stride + (size_t)h * d;
             for (int j = 0; j < d; ++j)
                 zz[j] = (double)zt[j];
-            gdnref_gated_norm(y, norm_w, zz, out + ((size_t)t * Hv + h) * d, d, rms_eps);
+            double *oh = out + ((size_t)t * Hv + h) * d;
+            gdnref_gated_norm(y, norm_w, zz, oh, d, rms_eps);
+            if (bf16_state) {
+                double *Sh = S + (size_t)h * d * d;
+                for (size_t e = 0; e < (size_t)d * d; ++e)
+                    Sh[e] = gdnref_round_bf16(Sh[e]);
+                for (int j = 0; j < d; ++j)
+                    oh[j] = gdnref_round_bf16(oh[j]);
+            }
         }
         if (t == snap_after) {
             if (S_snap)

@@ -292,6 +292,66 @@ def test_token_parallel_conv_full_prefill_size_equals_serial():
     assert same and torch.equal(h1, h2)
 
 
+# ------------------------------------------------------------------ bf16-state decode
+def _bf16_state(inp):
+    """The workload's state rounded to bf16: (bf16 bits, exact float32 values)."""
+    bits = synth.bf16_round(inp["state"])
+    return bits, synth.bf16_to_f32(bits)
+
+
+def test_bf16_state_step_is_the_float_step_rounded():
+    # same inputs, state values exactly bf16: the bf16-state kernel stores exactly
+    # the round-to-nearest-even of what the float32 kernel computes
+    shape = synth.WORKLOADS["decode_b64"]
+    inp = synth.make_inputs(shape, seed=29)
+    dev = device_inputs(shape, inp)
+    bits, f32 = _bf16_state(inp)
+    st16 = to_dev(bits, "bf16")
+    st32 = to_dev(f32)
+    h16, h32 = dev["hist"].clone(), dev["hist"].clone()
+    out16 = torch.empty(shape.B, shape.Hv, shape.d, device="cuda", dtype=torch.bfloat16)
+    out32 = torch.empty(shape.B, shape.Hv, shape.d, device="cuda")
+    gdn.decode_step_bf16_state(st16, h16, dev["x"], dev["z"], dev["alpha"], dev["beta_logit"],
+                               params_of(dev), out16, dims_of(shape))
+    gdn.decode_step(st32, h32, dev["x"], dev["z"], dev["alpha"], dev["beta_logit"],
+                    params_of(dev), out32, dims_of(shape))
+    torch.cuda.synchronize()
+    assert torch.equal(st16, st32.to(torch.bfloat16))
+    assert torch.equal(out16, out32.to(torch.bfloat16))
+    assert torch.equal(h16, h32)
+
+
+@pytest.mark.parametrize("name,steps,seed", [("decode_b1", 8, 30), ("tiny_seq", 16, 31),
+                                             ("verify_k2", 2, 32)])
+def test_bf16_state_decode_matches_rounded_oracle(name, steps, seed):
+    # against the oracle's bf16-state variant (state and outputs rounded to bf16
+    # after every step). A stored value is the RNE of a float32 result within
+    # ~1e-6 of the oracle's fp64 one, so the two roundings differ by at most one
+    # bf16 ulp (2^-8 relative), and a flipped state entry perturbs later steps
+    # by about as much again: 2^-7 normwise for state and outputs.
+    base = synth.WORKLOADS[name]
+    shape = synth.Shape(B=base.B, T=steps, Hq=base.Hq, Hv=base.Hv, act_dtype=base.act_dtype,
+                        warm=True)
+    inp = synth.make_inputs(shape, seed=seed)
+    bits, f32 = _bf16_state(inp)
+    ref = run_oracle(shape, dict(inp, state=f32), bf16_state=True)
+    dev = device_inputs(shape, inp)
+    st = to_dev(bits, "bf16")
+    dims = dims_of(shape, rows_per_seq=steps)
+    outs = torch.empty(shape.B, steps, shape.Hv, shape.d, device="cuda", dtype=torch.bfloat16)
+    one = torch.empty(shape.B, shape.Hv, shape.d, device="cuda", dtype=torch.bfloat16)
+    for t in range(steps):
+        gdn.decode_step_bf16_state(st, dev["hist"], dev["x"][:, t], dev["z"][:, t],
+                                   dev["alpha"][:, t], dev["beta_logit"][:, t], params_of(dev),
+                                   one, dims)
+        outs[:, t] = one
+    torch.cuda.synchronize()
+    tol = 2.0 ** -7
+    assert out_rel(outs.float().cpu().numpy(), ref["out"]) <= tol
+    assert max_rel(st.float().cpu().numpy(), ref["state"], 2) <= tol
+    assert np.array_equal(dev["hist"].cpu().numpy(), ref["hist"].astype(np.float32))
+
+
 def test_result_independent_of_batch_split():
     # the same sequence decoded alone (few CTAs: row-split clusters) and inside a
     # large batch (one CTA per head) gives identical bits

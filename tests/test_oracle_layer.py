@@ -118,3 +118,26 @@ def test_strided_rows_and_z_inside_row():
     ra = _run(base, a)
     rb = _run(strided, b)
     np.testing.assert_array_equal(ra["out"], rb["out"])
+
+
+def test_bf16_state_variant_is_the_rounded_float_step():
+    # three tokens of the bf16-state variant == three plain steps with the state
+    # and the outputs rounded to bf16 after each step (by the pinned rounding)
+    shape, inp = _small(B=2, T=3, Hq=1, Hv=2)
+    rnd = np.vectorize(oracle.round_bf16)
+    st0 = rnd(inp["state"]).astype(np.float32)                # a bf16 starting state
+    lp = oracle.layer(inp["x"], inp["z"], inp["alpha"], inp["beta_logit"], inp["conv_w"],
+                      inp["dt"], inp["A_log"], inp["norm_w"], st0, inp["hist"], Hq=shape.Hq,
+                      W=shape.W, bf16_state=True)
+    st, hi = st0, inp["hist"]
+    for t in range(shape.T):
+        one = oracle.layer(inp["x"][:, t:t + 1], inp["z"][:, t:t + 1], inp["alpha"][:, t:t + 1],
+                           inp["beta_logit"][:, t:t + 1], inp["conv_w"], inp["dt"], inp["A_log"],
+                           inp["norm_w"], st, hi, Hq=shape.Hq, W=shape.W)
+        np.testing.assert_array_equal(lp["out"][:, t], rnd(one["out"][:, 0]))
+        st = rnd(one["state"])          # exact in float32: bf16 values
+        assert np.array_equal(st.astype(np.float32).astype(np.float64), st)
+        st = st.astype(np.float32)
+        hi = one["hist"]
+    np.testing.assert_array_equal(lp["state"], st)
+    np.testing.assert_array_equal(lp["hist"], hi)

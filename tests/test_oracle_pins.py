@@ -259,3 +259,37 @@ def test_gated_norm_scale_invariant():
     # RMS of the normalised value (before the gate) is 1
     one = oracle.gated_norm(y, w, np.full(d, 50.0), 0.0) / (50.0 * expit(50.0))
     assert math.sqrt(np.mean(one ** 2)) == pytest.approx(1.0, rel=1e-13)
+
+
+# ------------------------------------------------------------------ bf16 storage rounding
+def test_round_bf16_closed_forms():
+    r = oracle.round_bf16
+    ulp1 = 2.0 ** -7                       # bf16 spacing in [1, 2)
+    assert r(1.0) == 1.0 and r(-3.5) == -3.5 and r(0.0) == 0.0
+    assert r(1.0 + ulp1 / 2) == 1.0                        # tie -> even (1.0)
+    assert r(1.0 + 3 * ulp1 / 2) == 1.0 + 2 * ulp1          # tie -> even mantissa
+    assert r(1.0 + ulp1 / 2 + 2.0 ** -40) == 1.0 + ulp1     # just above the tie: up
+    assert r(1.0 + ulp1 / 2 - 2.0 ** -40) == 1.0            # just below: down
+    assert r(-(1.0 + ulp1 / 2 + 2.0 ** -40)) == -(1.0 + ulp1)
+    big = 2.0 ** 128 - 2.0 ** 120                          # largest finite bf16
+    assert r(big) == big
+    assert r(2.0 ** 128 - 2.0 ** 119) == math.inf          # tie above the largest: overflow
+    assert r(2.0 ** 128 - 2.0 ** 119 - 2.0 ** 100) == big
+    assert r(2.0 ** -133) == 2.0 ** -133                   # smallest subnormal
+    assert r(2.0 ** -134) == 0.0                           # tie with zero -> zero
+    assert r(3 * 2.0 ** -134) == 2.0 ** -132               # tie -> even
+    assert math.isnan(r(math.nan)) and r(-math.inf) == -math.inf
+
+
+def test_round_bf16_matches_torch_on_float32_values():
+    torch = pytest.importorskip("torch")
+    # for float32-representable inputs a single float32 -> bf16 RNE (torch's
+    # conversion) is the same rounding; the draws include exact ties
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(4000) * np.exp(rng.uniform(-30, 30, 4000))).astype(np.float32)
+    bits = x.view(np.uint32)
+    ties = ((bits & ~np.uint32(0xFFFF)) | np.uint32(0x8000)).view(np.float32)[:500]
+    vals = np.concatenate([x, ties])
+    want = torch.from_numpy(vals).to(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.round_bf16(float(v)) for v in vals])
+    np.testing.assert_array_equal(got, want)
