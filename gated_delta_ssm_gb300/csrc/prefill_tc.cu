@@ -420,31 +420,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 *reinterpret_cast<uint4 *>(smem + QK_3 + off) = p3;
             }
         }
-        // ---- V rows: conv + SiLU -> fp32 V^T staged in each value row's X^T footprint
-        if (warp < 4) {
-            const int t0 = 16 * warp + 8 * (lane >> 4);
-            const int grp = lane & 15;
-            const int cb = 2 * a.Hq * kD + h * kD + 8 * grp;
-            float v[8][8];
-            if (a.W == 4 && c0 + t0 >= 3)
-                conv8x8_w4_inner<TIn>(a, b, cb, c0 + t0, v);
-            else if (a.W == 4)
-                conv8x8<TIn, 4>(a, b, cb, c0 + t0, v);
-            else
-                conv8x8<TIn, 0>(a, b, cb, c0 + t0, v);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int j = 8 * grp + e;
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int chunk4 = t0 / 4 + q;     // float4 chunk of the row (0..15)
-                    const uint32_t off = (chunk4 < 8 ? XU_HI : XU_LO) + (j >> 3) * 1024 +
-                                         (chunk4 & 7) * 128 + (j & 7) * 16;
-                    *reinterpret_cast<float4 *>(smem + off) =
-                        make_float4(v[4 * q][e], v[4 * q + 1][e], v[4 * q + 2][e], v[4 * q + 3][e]);
-                }
-            }
-        }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
         __syncthreads();
@@ -488,6 +463,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
             tc::mma_commit(mbar + 8);
         }
 
+        // ---- V rows: conv + SiLU -> fp32 V^T staged in each value row's X^T footprint.
+        // Warps 4-7 do this while the tensor core forms G and KS and warps 0-3 wait
+        // for them and build P and A; the X^T/U^T tile is no operand of those products.
+        if (warp >= 4) {
+            const int t0 = 16 * (warp & 3) + 8 * (lane >> 4);
+            const int grp = lane & 15;
+            const int cb = 2 * a.Hq * kD + h * kD + 8 * grp;
+            float v[8][8];
+            if (a.W == 4 && c0 + t0 >= 3)
+                conv8x8_w4_inner<TIn>(a, b, cb, c0 + t0, v);
+            else if (a.W == 4)
+                conv8x8<TIn, 4>(a, b, cb, c0 + t0, v);
+            else
+                conv8x8<TIn, 0>(a, b, cb, c0 + t0, v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j = 8 * grp + e;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int chunk4 = t0 / 4 + q;     // float4 chunk of the row (0..15)
+                    const uint32_t off = (chunk4 < 8 ? XU_HI : XU_LO) + (j >> 3) * 1024 +
+                                         (chunk4 & 7) * 128 + (j & 7) * 16;
+                    *reinterpret_cast<float4 *>(smem + off) =
+                        make_float4(v[4 * q][e], v[4 * q + 1][e], v[4 * q + 2][e], v[4 * q + 3][e]);
+                }
+            }
+        }
         // ---- P and A from G (both products must be done: their third parts share
         // the space P, T and (e^{Gam_C-Gam} K)^T are written to)
         if (!tc::mbar_wait(mbar + 0, par, kWaitLimit))
@@ -598,27 +600,67 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                     xv[c + e] = bt * xv[c + e] - bt * seg[c + e] * kv[e];
                 }
             }
-            // U = (I + A)^{-1} X column by column: (I + A) is unit lower triangular,
-            // so u_t = x_t - sum_{s<t} A[t][s] u_s, with the rows of A (fp32, XOR-swizzled
-            // float4 chunks) read as broadcasts
+            // U = (I + A)^{-1} X by blocks of 8 tokens: (I + A) is unit lower triangular,
+            // so u_t = x_t - sum_{s<t} A[t][s] u_s. Block b first takes the contributions
+            // of the earlier blocks (their u read back from this thread's own footprint of
+            // the X^T/U^T tile), then solves its 8 x 8 diagonal block in registers. Rows of
+            // A (fp32, XOR-swizzled float4 chunks) are read as broadcasts. The loops stay
+            // rolled: the fully unrolled substitution did not fit the instruction cache.
             const float *Af = reinterpret_cast<const float *>(smem + TT_HI);
+            const uint32_t foot = (jrow >> 3) * 1024 + (jrow & 7) * 16;
+            auto ufoot = [&](int q) {
+                return reinterpret_cast<float4 *>(smem + (q < 8 ? XU_HI : XU_LO) + foot + (q & 7) * 128);
+            };
 #pragma unroll
-            for (int t = 1; t < kC; ++t) {
-                const float *arow = Af + t * kC;
-                float acc0 = 0.0f, acc1 = 0.0f;
+            for (int q = 0; q < 16; ++q)
+                *ufoot(q) = make_float4(xv[4 * q], xv[4 * q + 1], xv[4 * q + 2], xv[4 * q + 3]);
+#pragma unroll 1
+            for (int b = 0; b < kC / 8; ++b) {
+                float acc0[8], acc1[8];
 #pragma unroll
-                for (int q = 0; q < (t + 3) / 4; ++q) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(arow + ((q ^ (t & 15)) << 2));
-                    if (4 * q + 0 < t)
-                        acc0 = __fmaf_rn(a4.x, xv[4 * q + 0], acc0);
-                    if (4 * q + 1 < t)
-                        acc1 = __fmaf_rn(a4.y, xv[4 * q + 1], acc1);
-                    if (4 * q + 2 < t)
-                        acc0 = __fmaf_rn(a4.z, xv[4 * q + 2], acc0);
-                    if (4 * q + 3 < t)
-                        acc1 = __fmaf_rn(a4.w, xv[4 * q + 3], acc1);
+                for (int t = 0; t < 8; ++t)
+                    acc0[t] = acc1[t] = 0.0f;
+#pragma unroll 1
+                for (int sb = 0; sb < b; ++sb) {
+                    const float4 u0 = *ufoot(2 * sb), u1 = *ufoot(2 * sb + 1);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const int row = 8 * b + t;
+                        const float *arow = Af + row * kC;
+                        const float4 a0 = *reinterpret_cast<const float4 *>(arow + (((2 * sb) ^ (row & 15)) << 2));
+                        const float4 a1 = *reinterpret_cast<const float4 *>(arow + (((2 * sb + 1) ^ (row & 15)) << 2));
+                        acc0[t] = __fmaf_rn(a0.x, u0.x, acc0[t]);
+                        acc1[t] = __fmaf_rn(a0.y, u0.y, acc1[t]);
+                        acc0[t] = __fmaf_rn(a0.z, u0.z, acc0[t]);
+                        acc1[t] = __fmaf_rn(a0.w, u0.w, acc1[t]);
+                        acc0[t] = __fmaf_rn(a1.x, u1.x, acc0[t]);
+                        acc1[t] = __fmaf_rn(a1.y, u1.y, acc1[t]);
+                        acc0[t] = __fmaf_rn(a1.z, u1.z, acc0[t]);
+                        acc1[t] = __fmaf_rn(a1.w, u1.w, acc1[t]);
+                    }
                 }
-                xv[t] = __fsub_rn(xv[t], __fadd_rn(acc0, acc1));
+                const float4 x0 = *ufoot(2 * b), x1 = *ufoot(2 * b + 1);
+                float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int row = 8 * b + t;
+                    const float *arow = Af + row * kC;
+                    const float4 a0 = *reinterpret_cast<const float4 *>(arow + (((2 * b) ^ (row & 15)) << 2));
+                    const float4 a1 = *reinterpret_cast<const float4 *>(arow + (((2 * b + 1) ^ (row & 15)) << 2));
+                    const float ad[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    float acc = __fadd_rn(acc0[t], acc1[t]);
+#pragma unroll
+                    for (int s2 = 0; s2 < t; ++s2)
+                        acc = __fmaf_rn(ad[s2], x[s2], acc);
+                    x[t] = __fsub_rn(x[t], acc);
+                }
+                *ufoot(2 * b) = make_float4(x[0], x[1], x[2], x[3]);
+                *ufoot(2 * b + 1) = make_float4(x[4], x[5], x[6], x[7]);
+            }
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float4 f = *ufoot(q);
+                xv[4 * q] = f.x; xv[4 * q + 1] = f.y; xv[4 * q + 2] = f.z; xv[4 * q + 3] = f.w;
             }
             // U^T row j as the three-part operand of the O and state products
 #pragma unroll
