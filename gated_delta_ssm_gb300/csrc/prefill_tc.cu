@@ -60,6 +60,18 @@ constexpr uint32_t PP_HI = 212992, PP_LO = 221184;  // [64 t][64 s]     P
 constexpr uint32_t QK_3 = 196608;                   // third part of [Q; K] (in TT and PP's space)
 // third parts of U^T and P, in the Q rows of [Q; K] (dead once G and KS are formed)
 constexpr uint32_t XU_3 = QK_HI, PP_3 = QK_LO + 8192;
+
+// bf16 parts per fp32 operand on the readout products (G, KS, O): 2 parts and
+// three product terms (~16 bits), or 3 parts and six terms (~24 bits). Two
+// parts keep the outputs within ~3e-5 of the fp64 scan (normwise per head) on
+// the 4 x 8192 workload and leave the state error (set by the two-part state
+// update) unchanged; three parts (built with -DGDN_PREFILL_PARTS=3) give
+// ~5e-6 at 14% more time.
+#ifndef GDN_PREFILL_PARTS
+#define GDN_PREFILL_PARTS 2
+#endif
+constexpr int kParts = GDN_PREFILL_PARTS;
+static_assert(kParts == 2 || kParts == 3, "2 or 3 bf16 parts");
 constexpr uint32_t SC_G = 229376, SC_BETA = SC_G + 256, SC_GAM = SC_BETA + 256,
                    SC_GAML = SC_GAM + 256, SC_EG = SC_GAML + 256, SC_EGC = SC_EG + 256,
                    SC_EGCC = SC_EGC + 256, SC_MBAR = SC_EGCC + 8, SC_TMEM = SC_MBAR + 32,
@@ -323,7 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 const uint32_t off = tc::km_offset(jrow, c + 8 * half, kD);
                 *reinterpret_cast<uint4 *>(smem + ST_HI + off) = p1;
                 *reinterpret_cast<uint4 *>(smem + ST_LO + off) = p2;
-                *reinterpret_cast<uint4 *>(smem + ST_3 + off) = p3;
+                if (kParts == 3)
+                    *reinterpret_cast<uint4 *>(smem + ST_3 + off) = p3;
             }
         }
     }
@@ -417,7 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 const uint32_t off = tc::km_offset(part * kC + t0 + t, 8 * grp, kD);
                 *reinterpret_cast<uint4 *>(smem + QK_HI + off) = p1;
                 *reinterpret_cast<uint4 *>(smem + QK_LO + off) = p2;
-                *reinterpret_cast<uint4 *>(smem + QK_3 + off) = p3;
+                if (kParts == 3)
+                    *reinterpret_cast<uint4 *>(smem + QK_3 + off) = p3;
             }
         }
         tc::fence_smem_to_async();
@@ -439,9 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 tc::mma_bf16(tmem + TM_G, a1, b1, id_g, kk > 0);
                 tc::mma_bf16(tmem + TM_G, a1, b2, id_g, 1);
                 tc::mma_bf16(tmem + TM_G, a2, b1, id_g, 1);
-                tc::mma_bf16(tmem + TM_G, a1, b3, id_g, 1);
-                tc::mma_bf16(tmem + TM_G, a2, b2, id_g, 1);
-                tc::mma_bf16(tmem + TM_G, a3, b1, id_g, 1);
+                if (kParts == 3) {
+                    tc::mma_bf16(tmem + TM_G, a1, b3, id_g, 1);
+                    tc::mma_bf16(tmem + TM_G, a2, b2, id_g, 1);
+                    tc::mma_bf16(tmem + TM_G, a3, b1, id_g, 1);
+                }
             }
             tc::mma_commit(mbar + 0);
 #pragma unroll 1
@@ -456,9 +472,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 tc::mma_bf16(tmem + TM_KS, a1, b1, id_128, kk > 0);
                 tc::mma_bf16(tmem + TM_KS, a1, b2, id_128, 1);
                 tc::mma_bf16(tmem + TM_KS, a2, b1, id_128, 1);
-                tc::mma_bf16(tmem + TM_KS, a1, b3, id_128, 1);
-                tc::mma_bf16(tmem + TM_KS, a2, b2, id_128, 1);
-                tc::mma_bf16(tmem + TM_KS, a3, b1, id_128, 1);
+                if (kParts == 3) {
+                    tc::mma_bf16(tmem + TM_KS, a1, b3, id_128, 1);
+                    tc::mma_bf16(tmem + TM_KS, a2, b2, id_128, 1);
+                    tc::mma_bf16(tmem + TM_KS, a3, b1, id_128, 1);
+                }
             }
             tc::mma_commit(mbar + 8);
         }
@@ -490,11 +508,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 }
             }
         }
-        // ---- P and A from G (both products must be done: their third parts share
-        // the space P, T and (e^{Gam_C-Gam} K)^T are written to)
+        // ---- P and A from G. With three parts both products must be done first
+        // (their third parts share the space P, T and (e^{Gam_C-Gam} K)^T are written
+        // to); with two parts only G is awaited here, and KS before X is formed.
         if (!tc::mbar_wait(mbar + 0, par, kWaitLimit))
             atomicOr(serr, 1);
-        if (!tc::mbar_wait(mbar + 8, par, kWaitLimit))
+        if (kParts == 3 && !tc::mbar_wait(mbar + 8, par, kWaitLimit))
             atomicOr(serr, 2);
         tc::fence_after_sync();
         if (warp < 4) {
@@ -533,7 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                         const uint32_t off = tc::km_offset(t, c + 8 * half, kC);
                         *reinterpret_cast<uint4 *>(smem + PP_HI + off) = p1;
                         *reinterpret_cast<uint4 *>(smem + PP_LO + off) = p2;
-                        *reinterpret_cast<uint4 *>(smem + PP_3 + off) = p3;
+                        if (kParts == 3)
+                            *reinterpret_cast<uint4 *>(smem + PP_3 + off) = p3;
                     }
                 }
             }
@@ -570,6 +590,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 tc::tmem_st16(tmem + lane_q + TM_S + c2, sv);
             }
         } else {
+            if (kParts == 2) {
+                if (!tc::mbar_wait(mbar + 8, par, kWaitLimit))
+                    atomicOr(serr, 2);
+                tc::fence_after_sync();
+            }
             // ---- (Q S_0)^T scaled by e^{Gam}; X^T = beta V^T - beta e^{Gam} (K S_0)^T
 #pragma unroll 1
             for (int c = 0; c < kC; c += 16) {
@@ -674,7 +699,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 const uint32_t off = tc::km_offset(jrow, c, kC);
                 *reinterpret_cast<uint4 *>(smem + XU_HI + off) = p1;
                 *reinterpret_cast<uint4 *>(smem + XU_LO + off) = p2;
-                *reinterpret_cast<uint4 *>(smem + XU_3 + off) = p3;
+                if (kParts == 3)
+                    *reinterpret_cast<uint4 *>(smem + XU_3 + off) = p3;
             }
         }
         tc::fence_smem_to_async();
@@ -698,9 +724,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 tc::mma_bf16(tmem + TM_KS, ah, ph, id_g, 1);
                 tc::mma_bf16(tmem + TM_KS, ah, pl, id_g, 1);
                 tc::mma_bf16(tmem + TM_KS, al, ph, id_g, 1);
-                tc::mma_bf16(tmem + TM_KS, ah, p3, id_g, 1);
-                tc::mma_bf16(tmem + TM_KS, al, pl, id_g, 1);
-                tc::mma_bf16(tmem + TM_KS, a3, ph, id_g, 1);
+                if (kParts == 3) {
+                    tc::mma_bf16(tmem + TM_KS, ah, p3, id_g, 1);
+                    tc::mma_bf16(tmem + TM_KS, al, pl, id_g, 1);
+                    tc::mma_bf16(tmem + TM_KS, a3, ph, id_g, 1);
+                }
                 tc::mma_bf16(tmem + TM_S, ah, kh, id_128, 1);
                 tc::mma_bf16(tmem + TM_S, ah, kl, id_128, 1);
                 tc::mma_bf16(tmem + TM_S, al, kh, id_128, 1);
@@ -738,7 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                     const uint32_t off = tc::km_offset(jrow, c + 8 * half, kD);
                     *reinterpret_cast<uint4 *>(smem + ST_HI + off) = p1;
                     *reinterpret_cast<uint4 *>(smem + ST_LO + off) = p2;
-                    *reinterpret_cast<uint4 *>(smem + ST_3 + off) = p3;
+                    if (kParts == 3)
+                        *reinterpret_cast<uint4 *>(smem + ST_3 + off) = p3;
                 }
             }
         }
