@@ -61,6 +61,26 @@ def test_prefill_fp32_activations():
     assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= PREFILL_STATE_TOL
 
 
+def test_prefill_with_unaligned_z_rows():
+    # z rows an odd number of bf16 elements apart cannot be staged by 16-byte copies;
+    # the kernel reads them directly instead
+    shape = synth.Shape(B=2, T=130, Hq=2, Hv=4, warm=True)
+    inp = synth.make_inputs(shape, seed=35)
+    ref = run_oracle(shape, inp)
+    dev = device_inputs(shape, inp)
+    zs = shape.Hv * shape.d + 1
+    zpad = torch.zeros(shape.B, shape.T, zs, dtype=dev["z"].dtype, device="cuda")
+    zpad[..., :shape.Hv * shape.d] = dev["z"]
+    dims = dims_of(shape)
+    dims.z_stride = zs
+    out = torch.empty(shape.B, shape.T, shape.Hv, shape.d, device="cuda")
+    gdn.prefill_chunked(dev["state"], dev["hist"], dev["x"], zpad, dev["alpha"], dev["beta_logit"],
+                        params_of(dev), out, dims, shape.T, 64)
+    torch.cuda.synchronize()
+    assert out_rel(out.cpu().numpy(), ref["out"]) <= OUT_TOL
+    assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= PREFILL_STATE_TOL
+
+
 def test_prefill_then_decode_continues_the_sequence():
     # prefill T tokens then decode one more == oracle over T + 1 tokens
     shape = synth.Shape(B=2, T=97, Hq=2, Hv=4, warm=True)
