@@ -351,53 +351,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
         const int n = min(kC, T - c0);
         const uint32_t par = chunk & 1;
 
-        // ---- gates and in-chunk cumulative decay (warp 7)
+        // ---- gate inputs of this chunk (warp 7): requested now, used after warp 7's
+        // share of the conv below, so their latency hides under it
+        float graw[2] = {0.0f, 0.0f}, braw[2] = {0.0f, 0.0f};
         if (warp == 7) {
-            float gv[2], bv[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int t = 2 * lane + u;
-                gv[u] = bv[u] = 0.0f;
                 if (t < n) {
-                    const int64_t row = c0 + t;
-                    gv[u] = decay_gate_f(load_act<TIn>(alb + row * a.gate_stride), dtv, alog);
-                    bv[u] = sigmoid_f(load_act<TIn>(blb + row * a.gate_stride));
+                    graw[u] = load_act<TIn>(alb + (int64_t)(c0 + t) * a.gate_stride);
+                    braw[u] = load_act<TIn>(blb + (int64_t)(c0 + t) * a.gate_stride);
                 }
-                sg[t] = gv[u];
-                sbeta[t] = bv[u];
             }
-            // inclusive scan of the token pairs in two-float arithmetic
-            float ph, pl;
-            two_sum(gv[0], gv[1], ph, pl);
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float yh = __shfl_up_sync(0xffffffffu, ph, off);
-                const float yl = __shfl_up_sync(0xffffffffu, pl, off);
-                if (lane >= off)
-                    two_add(ph, pl, yh, yl);
-            }
-            float exh = __shfl_up_sync(0xffffffffu, ph, 1);
-            float exl = __shfl_up_sync(0xffffffffu, pl, 1);
-            if (lane == 0)
-                exh = exl = 0.0f;
-            float g0h = exh, g0l = exl;
-            two_add(g0h, g0l, gv[0], 0.0f);
-            float g1h = g0h, g1l = g0l;
-            two_add(g1h, g1l, gv[1], 0.0f);
-            const float gch = __shfl_sync(0xffffffffu, g1h, 31);
-            const float gcl = __shfl_sync(0xffffffffu, g1l, 31);
-            sgam[2 * lane] = g0h;
-            sgaml[2 * lane] = g0l;
-            sgam[2 * lane + 1] = g1h;
-            sgaml[2 * lane + 1] = g1l;
-            seg[2 * lane] = exp_diff(g0h, g0l, 0.0f, 0.0f);
-            seg[2 * lane + 1] = exp_diff(g1h, g1l, 0.0f, 0.0f);
-            segc[2 * lane] = 2 * lane < n ? exp_diff(gch, gcl, g0h, g0l) : 0.0f;
-            segc[2 * lane + 1] = 2 * lane + 1 < n ? exp_diff(gch, gcl, g1h, g1l) : 0.0f;
-            if (lane == 0)
-                *segC = exp_diff(gch, gcl, 0.0f, 0.0f);
         }
-        __syncthreads();
 
         // ---- Q and K rows: conv + SiLU + L2 -> [Q; K] tile, and (e^{Gam_C-Gam} K)^T tile
         {
@@ -433,6 +399,49 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 if (kParts == 3)
                     *reinterpret_cast<uint4 *>(smem + QK_3 + off) = p3;
             }
+        }
+        // ---- gates and in-chunk cumulative decay (warp 7); every reader comes after
+        // the barrier that ends the conv
+        if (warp == 7) {
+            float gv[2], bv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = 2 * lane + u;
+                gv[u] = t < n ? decay_gate_f(graw[u], dtv, alog) : 0.0f;
+                bv[u] = t < n ? sigmoid_f(braw[u]) : 0.0f;
+                sg[t] = gv[u];
+                sbeta[t] = bv[u];
+            }
+            // inclusive scan of the token pairs in two-float arithmetic
+            float ph, pl;
+            two_sum(gv[0], gv[1], ph, pl);
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float yh = __shfl_up_sync(0xffffffffu, ph, off);
+                const float yl = __shfl_up_sync(0xffffffffu, pl, off);
+                if (lane >= off)
+                    two_add(ph, pl, yh, yl);
+            }
+            float exh = __shfl_up_sync(0xffffffffu, ph, 1);
+            float exl = __shfl_up_sync(0xffffffffu, pl, 1);
+            if (lane == 0)
+                exh = exl = 0.0f;
+            float g0h = exh, g0l = exl;
+            two_add(g0h, g0l, gv[0], 0.0f);
+            float g1h = g0h, g1l = g0l;
+            two_add(g1h, g1l, gv[1], 0.0f);
+            const float gch = __shfl_sync(0xffffffffu, g1h, 31);
+            const float gcl = __shfl_sync(0xffffffffu, g1l, 31);
+            sgam[2 * lane] = g0h;
+            sgaml[2 * lane] = g0l;
+            sgam[2 * lane + 1] = g1h;
+            sgaml[2 * lane + 1] = g1l;
+            seg[2 * lane] = exp_diff(g0h, g0l, 0.0f, 0.0f);
+            seg[2 * lane + 1] = exp_diff(g1h, g1l, 0.0f, 0.0f);
+            segc[2 * lane] = 2 * lane < n ? exp_diff(gch, gcl, g0h, g0l) : 0.0f;
+            segc[2 * lane + 1] = 2 * lane + 1 < n ? exp_diff(gch, gcl, g1h, g1l) : 0.0f;
+            if (lane == 0)
+                *segC = exp_diff(gch, gcl, 0.0f, 0.0f);
         }
         tc::fence_smem_to_async();
         tc::fence_before_sync();
