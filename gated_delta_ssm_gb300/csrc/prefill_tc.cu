@@ -50,7 +50,7 @@ constexpr int kThreads = 256;
 // Tiles whose live ranges do not overlap share space: the third parts of
 // [Q; K] and S^T are only read by the G and KS products, before T, P and
 // (e^{Gam_C-Gam} K)^T are written.
-constexpr uint32_t QK_HI = 0, QK_LO = 32768;        // [128 t'][128 i]  (Q rows, then K rows)
+constexpr uint32_t QK_HI = 0, QK_LO = 32768;        // [128 t'][128 i]  (Q rows, then K rows), 128-byte swizzled
 constexpr uint32_t ST_HI = 65536, ST_LO = 98304;    // [128 j][128 i]   S^T
 constexpr uint32_t KT_HI = 131072, KT_LO = 147456;  // [128 i][64 t]    (e^{Gam_C-Gam} K)^T
 constexpr uint32_t ST_3 = 131072;                   // third part of S^T (in KT's space)
@@ -77,6 +77,8 @@ constexpr uint32_t SC_G = 229376, SC_BETA = SC_G + 256, SC_GAM = SC_BETA + 256,
                    SC_EGCC = SC_EGC + 256, SC_MBAR = SC_EGCC + 8, SC_TMEM = SC_MBAR + 32,
                    SC_ERR = SC_TMEM + 4, SMEM_BYTES = SC_ERR + 4;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(QK_HI % 1024 == 0 && QK_LO % 1024 == 0 && QK_3 % 1024 == 0,
+              "swizzled [Q; K] tiles start on 1024-byte boundaries");
 
 // TMEM columns
 constexpr uint32_t TM_G = 0, TM_KS = 64, TM_S = 256, TM_COLS = 512;
@@ -287,6 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
     const int hk = h / (a.Hv / a.Hq);
     const int T = a.T;
     const uint32_t sbase = tc::smem_addr(smem);
+    // the [Q; K] tile's swizzle follows address bits 7-9: its atoms must be 1024-byte aligned
+    if (sbase & 1023u) {
+        if (threadIdx.x == 0)
+            atomicOr(&g_device_error, 32);
+        return;
+    }
     float *sg = reinterpret_cast<float *>(smem + SC_G);
     float *sbeta = reinterpret_cast<float *>(smem + SC_BETA);
     float *sgam = reinterpret_cast<float *>(smem + SC_GAM);     // Gam, high part
@@ -393,7 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                     v[t][e] *= inv;
                 uint4 p1, p2, p3;
                 split8x3(v[t], p1, p2, p3);
-                const uint32_t off = tc::km_offset(part * kC + t0 + t, 8 * grp, kD);
+                // 128-byte swizzled rows: a quarter-warp's 16-byte stores (8 channel groups
+                // of one token row) land on distinct bank groups
+                const uint32_t off = tc::sw128_offset(part * kC + t0 + t, 8 * grp, 2 * kC);
                 *reinterpret_cast<uint4 *>(smem + QK_HI + off) = p1;
                 *reinterpret_cast<uint4 *>(smem + QK_LO + off) = p2;
                 if (kParts == 3)
@@ -453,12 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
 #pragma unroll 1
             for (int kk = 0; kk < kD / 16; ++kk) {
                 const uint32_t ko = kk * 256;
-                const uint64_t a1 = tc::sdesc(sbase + QK_HI + ko, 128, 2048);
-                const uint64_t a2 = tc::sdesc(sbase + QK_LO + ko, 128, 2048);
-                const uint64_t a3 = tc::sdesc(sbase + QK_3 + ko, 128, 2048);
-                const uint64_t b1 = tc::sdesc(sbase + QK_HI + 16384 + ko, 128, 2048);
-                const uint64_t b2 = tc::sdesc(sbase + QK_LO + 16384 + ko, 128, 2048);
-                const uint64_t b3 = tc::sdesc(sbase + QK_3 + 16384 + ko, 128, 2048);
+                // [Q; K] tile: K slice kk at atom column kk / 4, 32 bytes per slice inside it
+                const uint32_t kq = (kk >> 2) * (2 * kC * 128) + (kk & 3) * 32;
+                const uint64_t a1 = tc::sdesc_sw128(sbase + QK_HI + kq);
+                const uint64_t a2 = tc::sdesc_sw128(sbase + QK_LO + kq);
+                const uint64_t a3 = tc::sdesc_sw128(sbase + QK_3 + kq);
+                const uint64_t b1 = tc::sdesc_sw128(sbase + QK_HI + 8192 + kq);
+                const uint64_t b2 = tc::sdesc_sw128(sbase + QK_LO + 8192 + kq);
+                const uint64_t b3 = tc::sdesc_sw128(sbase + QK_3 + 8192 + kq);
                 tc::mma_bf16(tmem + TM_G, a1, b1, id_g, kk > 0);
                 tc::mma_bf16(tmem + TM_G, a1, b2, id_g, 1);
                 tc::mma_bf16(tmem + TM_G, a2, b1, id_g, 1);
@@ -475,9 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 const uint64_t a1 = tc::sdesc(sbase + ST_HI + ko, 128, 2048);
                 const uint64_t a2 = tc::sdesc(sbase + ST_LO + ko, 128, 2048);
                 const uint64_t a3 = tc::sdesc(sbase + ST_3 + ko, 128, 2048);
-                const uint64_t b1 = tc::sdesc(sbase + QK_HI + ko, 128, 2048);
-                const uint64_t b2 = tc::sdesc(sbase + QK_LO + ko, 128, 2048);
-                const uint64_t b3 = tc::sdesc(sbase + QK_3 + ko, 128, 2048);
+                const uint32_t kq = (kk >> 2) * (2 * kC * 128) + (kk & 3) * 32;
+                const uint64_t b1 = tc::sdesc_sw128(sbase + QK_HI + kq);
+                const uint64_t b2 = tc::sdesc_sw128(sbase + QK_LO + kq);
+                const uint64_t b3 = tc::sdesc_sw128(sbase + QK_3 + kq);
                 tc::mma_bf16(tmem + TM_KS, a1, b1, id_128, kk > 0);
                 tc::mma_bf16(tmem + TM_KS, a1, b2, id_128, 1);
                 tc::mma_bf16(tmem + TM_KS, a2, b1, id_128, 1);
@@ -576,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 float col[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
-                    const uint32_t off = tc::km_offset(kC + t0 + t, tq, kD);
+                    const uint32_t off = tc::sw128_offset(kC + t0 + t, tq, 2 * kC);
                     const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + QK_HI + off)) +
                                      __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + QK_LO + off));
                     col[t] = kv * segc[t0 + t];

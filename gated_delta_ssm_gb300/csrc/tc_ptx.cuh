@@ -39,6 +39,31 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     return d;
 }
 
+// 128-byte-swizzled K-major tile of 16-bit elements, `rows` x 128: atoms of 8
+// rows x 64 elements (8 x 128 bytes, 1024-byte aligned) in which the 16-byte
+// chunk index of a row is XOR-ed with address bits 7-9 (the row within the
+// atom); atoms run down the rows 1024 bytes apart, and the two 64-element
+// halves of K are rows * 128 bytes apart. Byte offset of element (r, k).
+__host__ __device__ constexpr uint32_t sw128_offset(int r, int k, int rows)
+{
+    return (uint32_t)((k >> 6) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 +
+                      ((((k >> 3) & 7) ^ (r & 7)) << 4) + (k & 7) * 2);
+}
+
+// Descriptor of such a tile starting at saddr (an atom row start plus the
+// K offset within the 128-byte row): stride byte offset 1024 between 8-row
+// groups, leading byte offset unused, version bits 46..48 = 0b001, base
+// offset 0 (atoms are 1024-byte aligned), layout type 2 = 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr)
+{
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator,
 // both operands K-major, dense: D format bits 4-5 = 1 (f32), A format bits
 // 7-9 = 1 (bf16), B format bits 10-12 = 1 (bf16), N >> 3 at bits 17-22,

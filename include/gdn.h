@@ -332,8 +332,9 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
  * Every wait inside a kernel (on a bulk copy or a tensor-core operation) is
  * bounded; a kernel whose wait gives up sets a bit in a device-side error word
  * and skips the rest of its work instead of hanging (bits 1, 2, 8: the chunked
- * prefill's tensor-core and copy waits; bit 64: the multi-token conv's tile
- * copy wait). gdn_verify_commit_kn sets bit 16 for an accepted count outside
+ * prefill's tensor-core and copy waits; bit 32: the chunked prefill found its
+ * shared memory not 1024-byte aligned and did nothing; bit 64: the multi-token
+ * conv's tile copy wait). gdn_verify_commit_kn sets bit 16 for an accepted count outside
  * 1..K. This call waits for all
  * work on the device (it synchronises), reads the word into *code (may be
  * NULL) and clears it. Returns GDN_OK when no bit was set, GDN_ERR_DEVICE when
