@@ -757,6 +757,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
             }
             tc::mma_commit(mbar + 24);
         }
+        // this chunk's z values for the gated norm (warp w: tokens w, w+8, ...), requested
+        // now so that their latency hides under the products
+        float zv[kC / 8][4];
+        {
+            const TIn *zb = static_cast<const TIn *>(a.z) + (int64_t)b * T * a.z_stride + (int64_t)h * kD;
+#pragma unroll
+            for (int i = 0; i < kC / 8; ++i) {
+                const int t = warp + 8 * i;
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    zv[i][m] = t < n ? load_act<TIn>(zb + ((int64_t)c0 + t) * a.z_stride + 32 * m + lane) : 0.0f;
+            }
+        }
         if (!tc::mbar_wait(mbar + 24, par, kWaitLimit))
             atomicOr(serr, 8);
         tc::fence_after_sync();
@@ -795,19 +808,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
         }
         __syncthreads();
 
-        // ---- gated RMSNorm of each token's output row (warp w: tokens w, w+8, ...;
-        // every z value is requested before the first is used)
+        // ---- gated RMSNorm of each token's output row (warp w: tokens w, w+8, ...)
         {
             const float *O = reinterpret_cast<const float *>(smem + XU_HI);
-            const TIn *zb = static_cast<const TIn *>(a.z) + (int64_t)b * T * a.z_stride + (int64_t)h * kD;
-            float zv[kC / 8][4];
-#pragma unroll
-            for (int i = 0; i < kC / 8; ++i) {
-                const int t = warp + 8 * i;
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    zv[i][m] = t < n ? load_act<TIn>(zb + ((int64_t)c0 + t) * a.z_stride + 32 * m + lane) : 0.0f;
-            }
             float nwv[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m)
