@@ -562,6 +562,9 @@ def main(argv=None):
     if not args.no_cpu_baseline and world == 1:
         cpu = oracle_decode_b64_sample()
         cpu.pop("seconds")
+        # the same oracle on one host thread (a smaller sample: 8 steps of 8 sequences)
+        one = oracle_decode_b64_sample(n_seqs=8, n_steps=8, threads=1, min_seconds=2.0)
+        cpu["single_thread"] = {"value": one["value"], "unit": one["unit"], "sample": one["sample"]}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
