@@ -109,9 +109,10 @@ __global__ void __launch_bounds__(256) gated_norm_kernel(const float *y, const f
 // loads or stores: (1) state-row loads, (2) conv-window, gate, z and norm-gain
 // loads, one memory round trip; (3) conv + SiLU, then cluster arrive (every
 // read of the shared Q/K history is done); (4) L2, gates; (5) recurrence in
-// registers; (6) gated norm (row slices of a head exchange partial sums
-// through distributed shared memory when NSPLIT > 1); (7) state stores; (8)
-// cluster wait, then the single owner of each Q/K channel rewrites its
+// registers, each 4-row group stored as soon as it is stepped (its stores
+// overlap the later groups' arithmetic); (6) gated norm (row slices of a head
+// exchange partial sums through distributed shared memory when NSPLIT > 1);
+// (7) cluster wait, then the single owner of each Q/K channel rewrites its
 // history.
 //
 // TS is the storage type of the state and the output: float, or bf16 for the
@@ -217,11 +218,12 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
     }
     __syncthreads();
 
-    // (5) recurrence over this CTA's rows, in registers
-    step_rows<NG, NTOK, SNAP>(st, SNAP ? static_cast<float *>(a.state_snap) + head_off + warp_off
-                                       : nullptr,
-                              sk, sq, sv,
-                              ROWS, sdecay, sbeta, sy, warp * RPW, a.scale);
+    // (5) recurrence over this CTA's rows, in registers; the rows go back to HBM group
+    // by group as they are finished
+    step_rows<NG, NTOK, SNAP, TS>(st, SNAP ? static_cast<float *>(a.state_snap) + head_off + warp_off
+                                           : nullptr,
+                                  sk, sq, sv, ROWS, sdecay, sbeta, sy, warp * RPW, a.scale,
+                                  state + head_off + warp_off);
     __syncthreads();
 
     // (6) gated RMSNorm: 32-row block partials, combined in block order
@@ -264,10 +266,8 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
     if (NSPLIT > 1)
         cluster_arrive_relaxed();   // this CTA no longer reads its peers' shared memory
 
-    // (7) state rows back to HBM
-    store_rows<NG>(st, state + head_off + warp_off);
 
-    // (8) Q/K history: each channel rewritten by exactly one CTA of the cluster,
+    // (7) Q/K history: each channel rewritten by exactly one CTA of the cluster,
     // after every CTA of the cluster has read it
     if (csize > 1 && NSPLIT == 1)
         cluster_wait_acquire();

@@ -259,11 +259,27 @@ __device__ __forceinline__ void load_rows(const float *rows, float4 (&r)[NG][4])
             r[gi][m] = ld_stream(rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4);
 }
 
-template <int NG, int NTOK, bool SNAP>
+// One float4 of a row to its storage type (streaming store; bf16: round to nearest even).
+__device__ __forceinline__ void store_one(float *p, float4 v) { st_stream(p, v); }
+__device__ __forceinline__ void store_one(__nv_bfloat16 *p, float4 v)
+{
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&lo);
+    u.y = *reinterpret_cast<const uint32_t *>(&hi);
+    __stcs(reinterpret_cast<uint2 *>(p), u);
+}
+
+// final_rows, when given, receives each 4-row group as soon as its last token
+// is applied, so the write traffic starts while later groups are still being
+// stepped (the single-token kernels otherwise keep the rows until the norm).
+template <int NG, int NTOK, bool SNAP, typename TSt = float>
 __device__ __forceinline__ void step_rows(float4 (&r)[NG][4], float *snap_rows,
                                           const float *sk, const float *sq, const float *sv,
                                           int v_stride, const float *sdecay, const float *sbeta,
-                                          float *sy, int local_row0, float scale)
+                                          float *sy, int local_row0, float scale,
+                                          TSt *final_rows = nullptr)
 {
     const int lane = threadIdx.x & 31;
     const int rg = lane >> 3;
@@ -320,6 +336,11 @@ __device__ __forceinline__ void step_rows(float4 (&r)[NG][4], float *snap_rows,
             const float y = __fmul_rn(scale, __fmaf_rn(delta, kq, __fmul_rn(decay, pq)));
             if (sub == 0)
                 sy[p * v_stride + lrow] = y;
+            if (final_rows != nullptr && p == NTOK - 1) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    store_one(final_rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4, r[gi][m]);
+            }
         }
         if (SNAP && p == 0) {
 #pragma unroll
