@@ -268,9 +268,65 @@ class Gpu:
             step(i)
             hout.copy_(out, non_blocking=True)
 
-        e2e_times = self.time_steps(e2e_step, steps, max(3, warmup // 2))
+        serial_times = self.time_steps(e2e_step, steps, max(3, warmup // 2))
         self.launches += steps
-        return shape, times, e2e_times, h2d, d2h
+
+        # The serving loop: every step's inputs still come from pinned host memory and
+        # its output still goes back to pinned host memory, but the copies run on a
+        # second stream, double-buffered, so step i+1's inputs arrive while step i runs.
+        cd = shape.conv_dim
+        copy = torch.cuda.Stream(device=self.dev)
+        comp = self.stream
+        dx = [d["x"], torch.empty_like(d["x"])]
+        da = [d["alpha"], torch.empty_like(d["alpha"])]
+        db = [d["beta_logit"], torch.empty_like(d["beta_logit"])]
+        dz = [t[..., cd:cd + shape.Hv * shape.d] for t in dx]
+        outs = [out, torch.empty_like(out)]
+        houts = [hout, torch.empty(out.shape, dtype=out.dtype).pin_memory()]
+        ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_k = [torch.cuda.Event(), torch.cuda.Event()]
+
+        def h2d_into(j):
+            dx[j].copy_(hx, non_blocking=True)
+            da[j].copy_(ha, non_blocking=True)
+            db[j].copy_(hb, non_blocking=True)
+
+        def pipelined(n_steps, first):
+            with torch.cuda.stream(copy):
+                h2d_into(0)
+                ev_in[0].record(copy)
+            for i in range(n_steps):
+                j = i % 2
+                if i + 1 < n_steps:
+                    with torch.cuda.stream(copy):
+                        if i >= 1:
+                            copy.wait_event(ev_k[1 - j])   # step i-1 has read that buffer
+                        h2d_into(1 - j)
+                        ev_in[1 - j].record(copy)
+                comp.wait_event(ev_in[j])
+                gdn.decode_step(d["states"][(first + i) % nbuf], d["hists"][(first + i) % nbuf],
+                                dx[j], dz[j], da[j], db[j], prm, outs[j], dims, stream=comp)
+                ev_k[j].record(comp)
+                with torch.cuda.stream(copy):
+                    copy.wait_event(ev_k[j])
+                    houts[j].copy_(outs[j], non_blocking=True)
+
+        pipelined(max(3, warmup), 0)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(copy)
+        comp.wait_event(t0)
+        pipelined(steps, 0)
+        comp_done = torch.cuda.Event()
+        comp_done.record(comp)
+        copy.wait_event(comp_done)
+        t1.record(copy)
+        torch.cuda.synchronize()
+        self.launches += steps
+        e2e_total = t0.elapsed_time(t1) * 1e-3
+        return shape, times, e2e_total, h2d, d2h, sum(serial_times)
 
     # -- single-sequence decode: 1000 steps in one CUDA graph, 64 rotating state buffers
     def decode_b1(self, n_steps=1000, nbuf=64, reps=3):
@@ -536,13 +592,13 @@ def main(argv=None):
     gpu = Gpu(local)
     shape = synth.WORKLOADS[HEADLINE]
     with ClockSampler(local) as clocks:
-        _, times, e2e_times, h2d, d2h = gpu.decode_b64(args.steps, args.warmup, dist)
+        _, times, e2e_total, h2d, d2h, e2e_serial = gpu.decode_b64(args.steps, args.warmup, dist)
     total_s = sum(times)
     max_s = reduce_max(dist, total_s, gpu.dev)
     nb = decode_bytes(shape)
     mean = max_s / args.steps
     value = aggregate(nb["state"] * args.steps, world, max_s) / 1e9
-    e2e_max = reduce_max(dist, sum(e2e_times), gpu.dev)
+    e2e_max = reduce_max(dist, e2e_total, gpu.dev)
     e2e_value = aggregate(nb["state"] * args.steps, world, e2e_max) / 1e9
     hbm_peak, _, peak_kind = measured_peaks()
     achieved = nb["total"] / statistics.mean(times) / 1e9
@@ -581,7 +637,10 @@ def main(argv=None):
                      "kernel": "decode_fused_kernel", "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": nb["total"]},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max / args.steps * 1e3},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max / args.steps * 1e3,
+                "copies": "each step's inputs from pinned host memory and its output back to pinned "
+                          "host memory, on a second stream overlapping the previous step's kernel",
+                "serialized_ms_per_step": e2e_serial / args.steps * 1e3},
         "gpu_launches": gpu.launches,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
