@@ -227,11 +227,14 @@ __global__ void __launch_bounds__(256, 2) layer_scan_kernel(LayerScanArgs a)
         }
         __syncthreads();
 
+        // each 4-row group goes out as soon as it is stepped: to this position's
+        // snapshot, and after the last position to the state itself
+        float *dst = p + 1 == T ? a.state + head_off + warp_off
+                     : a.state_snap ? a.state_snap + (((size_t)b * (T - 1) + p) * a.Hv + h) * kD * kD +
+                                          warp_off
+                                    : nullptr;
         step_rows<NG, 1, false>(st, nullptr, sk, sq, sv, ROWS, sdecay, sbeta, sy, warp * RPW,
-                                a.scale);
-        if (a.state_snap && p + 1 < T)
-            store_rows<NG>(st, a.state_snap + (((size_t)b * (T - 1) + p) * a.Hv + h) * kD * kD +
-                                   warp_off);
+                                a.scale, dst);
         __syncthreads();
 
         const int slot = p & 1;
@@ -269,7 +272,6 @@ __global__ void __launch_bounds__(256, 2) layer_scan_kernel(LayerScanArgs a)
             cluster_arrive_relaxed();   // this CTA's reads of its peers' partials are done
     }
 
-    store_rows<NG>(st, a.state + head_off + warp_off);
     if (has_v) {
         float nh[kMaxW - 1];
         window_history(wv, nh);
