@@ -61,6 +61,18 @@ constexpr uint32_t QK_3 = 196608;                   // third part of [Q; K] (in 
 // third parts of U^T and P, in the Q rows of [Q; K] (dead once G and KS are formed)
 constexpr uint32_t XU_3 = QK_HI, PP_3 = QK_LO + 8192;
 
+// The fp32 footprint of value row j in the X^T/U^T tile: float4 chunk q
+// (tokens 4q .. 4q+3) of the row. Its 16-byte slot is XOR-ed with the row
+// group (j / 8), so that the V conv's stores (eight rows of different 8-row
+// groups per quarter-warp) and a warp's per-row reads both hit distinct bank
+// groups. The two-part U^T operand written over it afterwards uses the plain
+// core-matrix slots, so that write waits for every row's last read.
+__host__ __device__ constexpr uint32_t foot_off(int j, int q)
+{
+    return (uint32_t)((q < 8 ? XU_HI : XU_LO) + (j >> 3) * 1024 + (q & 7) * 128 +
+                      (((j & 7) ^ ((j >> 3) & 7)) << 4));
+}
+
 // bf16 parts per fp32 operand on the readout products (G, KS, O): 2 parts and
 // three product terms (~16 bits), or 3 parts and six terms (~24 bits). Two
 // parts keep the outputs within ~3e-5 of the fp64 scan (normwise per head) on
@@ -523,8 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int chunk4 = t0 / 4 + q;     // float4 chunk of the row (0..15)
-                    const uint32_t off = (chunk4 < 8 ? XU_HI : XU_LO) + (j >> 3) * 1024 +
-                                         (chunk4 & 7) * 128 + (j & 7) * 16;
+                    const uint32_t off = foot_off(j, chunk4);
                     *reinterpret_cast<float4 *>(smem + off) =
                         make_float4(v[4 * q][e], v[4 * q + 1][e], v[4 * q + 2][e], v[4 * q + 3][e]);
                 }
@@ -543,8 +554,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
             const bool krow = jrow >= kC;
             const float gt = sgam[t], gtl = sgaml[t];
             const float bt = sbeta[t];
+            const int tmax = (warp & 1) ? kC - 1 : kC / 2 - 1;   // largest token of this warp
 #pragma unroll 1
             for (int c = 0; c < kC; c += 16) {
+                if (c > tmax) {
+                    // s > t everywhere in this block: P is zero there (an operand of the
+                    // O product), A is never read there
+                    if (!krow) {
+                        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const uint32_t off = tc::km_offset(t, c + 8 * half, kC);
+                            *reinterpret_cast<uint4 *>(smem + PP_HI + off) = zero;
+                            *reinterpret_cast<uint4 *>(smem + PP_LO + off) = zero;
+                            if (kParts == 3)
+                                *reinterpret_cast<uint4 *>(smem + PP_3 + off) = zero;
+                        }
+                    }
+                    continue;
+                }
                 float gv[16];
                 tc::tmem_ld16(tmem + lane_q + TM_G + c, gv);
                 float o[16];
@@ -632,9 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
             float xv[kC];
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
-                const uint32_t off = (q < 8 ? XU_HI : XU_LO) + (jrow >> 3) * 1024 + (q & 7) * 128 +
-                                     (jrow & 7) * 16;
-                const float4 f = *reinterpret_cast<const float4 *>(smem + off);
+                const float4 f = *reinterpret_cast<const float4 *>(smem + foot_off(jrow, q));
                 xv[4 * q] = f.x; xv[4 * q + 1] = f.y; xv[4 * q + 2] = f.z; xv[4 * q + 3] = f.w;
             }
 #pragma unroll
@@ -654,10 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
             // A (fp32, XOR-swizzled float4 chunks) are read as broadcasts. The loops stay
             // rolled: the fully unrolled substitution did not fit the instruction cache.
             const float *Af = reinterpret_cast<const float *>(smem + TT_HI);
-            const uint32_t foot = (jrow >> 3) * 1024 + (jrow & 7) * 16;
-            auto ufoot = [&](int q) {
-                return reinterpret_cast<float4 *>(smem + (q < 8 ? XU_HI : XU_LO) + foot + (q & 7) * 128);
-            };
+            auto ufoot = [&](int q) { return reinterpret_cast<float4 *>(smem + foot_off(jrow, q)); };
 #pragma unroll
             for (int q = 0; q < 16; ++q)
                 *ufoot(q) = make_float4(xv[4 * q], xv[4 * q + 1], xv[4 * q + 2], xv[4 * q + 3]);
@@ -709,7 +732,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                 const float4 f = *ufoot(q);
                 xv[4 * q] = f.x; xv[4 * q + 1] = f.y; xv[4 * q + 2] = f.z; xv[4 * q + 3] = f.w;
             }
-            // U^T row j as the three-part operand of the O and state products
+            // U^T row j as the two-part operand of the O and state products; every row
+            // of warps 0-3 has read its fp32 footprint back first (named barrier 1)
+            asm volatile("bar.sync 1, 128;" ::: "memory");
 #pragma unroll
             for (int c = 0; c < kC; c += 8) {
                 float u8[8];
