@@ -73,6 +73,13 @@ __host__ __device__ constexpr uint32_t foot_off(int j, int q)
                       (((j & 7) ^ ((j >> 3) & 7)) << 4));
 }
 
+// Tokens per block of the blocked forward substitution U = (I + A)^{-1} X.
+#ifndef GDN_SUBST_BLOCK
+#define GDN_SUBST_BLOCK 8
+#endif
+constexpr int kSB = GDN_SUBST_BLOCK;
+static_assert(kSB == 8 || kSB == 16, "8- or 16-token blocks");
+
 // bf16 parts per fp32 operand on the readout products (G, KS, O): 2 parts and
 // three product terms (~16 bits), or 3 parts and six terms (~24 bits). Two
 // parts keep the outputs within ~3e-5 of the fp64 scan (normwise per head) on
@@ -673,10 +680,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
                     xv[c + e] = bt * xv[c + e] - bt * seg[c + e] * kv[e];
                 }
             }
-            // U = (I + A)^{-1} X by blocks of 8 tokens: (I + A) is unit lower triangular,
+            // U = (I + A)^{-1} X by blocks of kSB tokens: (I + A) is unit lower triangular,
             // so u_t = x_t - sum_{s<t} A[t][s] u_s. Block b first takes the contributions
             // of the earlier blocks (their u read back from this thread's own footprint of
-            // the X^T/U^T tile), then solves its 8 x 8 diagonal block in registers. Rows of
+            // the X^T/U^T tile), then solves its diagonal block in registers. Rows of
             // A (fp32, XOR-swizzled float4 chunks) are read as broadcasts. The loops stay
             // rolled: the fully unrolled substitution did not fit the instruction cache.
             const float *Af = reinterpret_cast<const float *>(smem + TT_HI);
@@ -685,47 +692,58 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
             for (int q = 0; q < 16; ++q)
                 *ufoot(q) = make_float4(xv[4 * q], xv[4 * q + 1], xv[4 * q + 2], xv[4 * q + 3]);
 #pragma unroll 1
-            for (int b = 0; b < kC / 8; ++b) {
-                float acc0[8], acc1[8];
+            for (int b = 0; b < kC / kSB; ++b) {
+                float acc0[kSB], acc1[kSB];
 #pragma unroll
-                for (int t = 0; t < 8; ++t)
+                for (int t = 0; t < kSB; ++t)
                     acc0[t] = acc1[t] = 0.0f;
 #pragma unroll 1
                 for (int sb = 0; sb < b; ++sb) {
-                    const float4 u0 = *ufoot(2 * sb), u1 = *ufoot(2 * sb + 1);
+                    float4 u4[kSB / 4];
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        const int row = 8 * b + t;
+                    for (int q = 0; q < kSB / 4; ++q)
+                        u4[q] = *ufoot(sb * (kSB / 4) + q);
+#pragma unroll
+                    for (int t = 0; t < kSB; ++t) {
+                        const int row = kSB * b + t;
                         const float *arow = Af + row * kC;
-                        const float4 a0 = *reinterpret_cast<const float4 *>(arow + (((2 * sb) ^ (row & 15)) << 2));
-                        const float4 a1 = *reinterpret_cast<const float4 *>(arow + (((2 * sb + 1) ^ (row & 15)) << 2));
-                        acc0[t] = __fmaf_rn(a0.x, u0.x, acc0[t]);
-                        acc1[t] = __fmaf_rn(a0.y, u0.y, acc1[t]);
-                        acc0[t] = __fmaf_rn(a0.z, u0.z, acc0[t]);
-                        acc1[t] = __fmaf_rn(a0.w, u0.w, acc1[t]);
-                        acc0[t] = __fmaf_rn(a1.x, u1.x, acc0[t]);
-                        acc1[t] = __fmaf_rn(a1.y, u1.y, acc1[t]);
-                        acc0[t] = __fmaf_rn(a1.z, u1.z, acc0[t]);
-                        acc1[t] = __fmaf_rn(a1.w, u1.w, acc1[t]);
+#pragma unroll
+                        for (int q = 0; q < kSB / 4; ++q) {
+                            const float4 a4 = *reinterpret_cast<const float4 *>(
+                                arow + (((sb * (kSB / 4) + q) ^ (row & 15)) << 2));
+                            acc0[t] = __fmaf_rn(a4.x, u4[q].x, acc0[t]);
+                            acc1[t] = __fmaf_rn(a4.y, u4[q].y, acc1[t]);
+                            acc0[t] = __fmaf_rn(a4.z, u4[q].z, acc0[t]);
+                            acc1[t] = __fmaf_rn(a4.w, u4[q].w, acc1[t]);
+                        }
                     }
                 }
-                const float4 x0 = *ufoot(2 * b), x1 = *ufoot(2 * b + 1);
-                float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                float x[kSB];
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const int row = 8 * b + t;
+                for (int q = 0; q < kSB / 4; ++q) {
+                    const float4 f = *ufoot(b * (kSB / 4) + q);
+                    x[4 * q] = f.x; x[4 * q + 1] = f.y; x[4 * q + 2] = f.z; x[4 * q + 3] = f.w;
+                }
+#pragma unroll
+                for (int t = 0; t < kSB; ++t) {
+                    const int row = kSB * b + t;
                     const float *arow = Af + row * kC;
-                    const float4 a0 = *reinterpret_cast<const float4 *>(arow + (((2 * b) ^ (row & 15)) << 2));
-                    const float4 a1 = *reinterpret_cast<const float4 *>(arow + (((2 * b + 1) ^ (row & 15)) << 2));
-                    const float ad[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    float ad[kSB];
+#pragma unroll
+                    for (int q = 0; q < kSB / 4; ++q) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(
+                            arow + (((b * (kSB / 4) + q) ^ (row & 15)) << 2));
+                        ad[4 * q] = a4.x; ad[4 * q + 1] = a4.y; ad[4 * q + 2] = a4.z; ad[4 * q + 3] = a4.w;
+                    }
                     float acc = __fadd_rn(acc0[t], acc1[t]);
 #pragma unroll
                     for (int s2 = 0; s2 < t; ++s2)
                         acc = __fmaf_rn(ad[s2], x[s2], acc);
                     x[t] = __fsub_rn(x[t], acc);
                 }
-                *ufoot(2 * b) = make_float4(x[0], x[1], x[2], x[3]);
-                *ufoot(2 * b + 1) = make_float4(x[4], x[5], x[6], x[7]);
+#pragma unroll
+                for (int q = 0; q < kSB / 4; ++q)
+                    *ufoot(b * (kSB / 4) + q) = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
             }
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
