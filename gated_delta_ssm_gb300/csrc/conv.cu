@@ -12,11 +12,11 @@
 // the input rows meet the tensor-copy alignment; the token kernel (plain
 // loads) covers the rest.
 #include <algorithm>
-#include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched at run time)
 
 #include "gdn_device.cuh"
 #include "gdn_kernels.h"
 #include "tc_ptx.cuh"
+#include "tma_map.cuh"
 
 namespace gdn {
 
@@ -164,18 +164,6 @@ struct TileLayout {
     static constexpr uint32_t bytes = flag + 16 + 1024;        // + alignment slack
 };
 
-__device__ __forceinline__ void tile_copy(const CUtensorMap *map, uint32_t dst, uint32_t mbar,
-                                          uint32_t bytes, int c0, int t, int b)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                 :: "r"(mbar), "r"(bytes) : "memory");
-    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%2, %3, %4}], [%5];"
-                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(t), "r"(b),
-                    "r"(mbar)
-                 : "memory");
-}
-
 template <typename TIn>
 __device__ __forceinline__ float smem_act(const TIn *p);
 template <>
@@ -208,7 +196,7 @@ __global__ void __launch_bounds__(256) conv_tiles_kernel(const __grid_constant__
 
     auto issue = [&](int item, int buf) {
         const int head = item % n_heads, rest = item / n_heads;
-        tile_copy(&xmap, tile0 + buf * L::tile, mbar0 + 8 * buf, tx_bytes, head * kD,
+        tile_copy_3d(&xmap, tile0 + buf * L::tile, mbar0 + 8 * buf, tx_bytes, head * kD,
                   (rest % n_tiles) * kTT - (W - 1), rest / n_tiles);
     };
     if (tid == 0) {
@@ -327,42 +315,11 @@ __global__ void __launch_bounds__(256) conv_tiles_kernel(const __grid_constant__
     }
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn tensor_map_encoder()
-{
-    static EncodeTiledFn fn = [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    return fn;
-}
-
-// The [B][T][conv_dim] view of x (rows x_stride apart), boxes of 128 channels x (kTT + W - 1) rows.
+// The [B][T][conv_dim] view of x, boxes of 128 channels x (kTT + W - 1) rows.
 bool encode_x_map(CUtensorMap *map, const ConvArgs &a, bool bf16)
 {
-    const size_t es = bf16 ? 2 : 4;
-    const EncodeTiledFn enc = tensor_map_encoder();
-    if (!enc || reinterpret_cast<uintptr_t>(a.x) % 16 != 0 || (a.x_stride * es) % 16 != 0)
-        return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)a.conv_dim, (cuuint64_t)a.T, (cuuint64_t)a.B};
-    const cuuint64_t strides[2] = {(cuuint64_t)a.x_stride * es, (cuuint64_t)a.x_stride * es * a.T};
-    if (strides[1] >= (1ull << 40))
-        return false;
-    const cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)(kTT + a.W - 1), 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
-               const_cast<void *>(a.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_rows_map(map, a.x, bf16, a.conv_dim, a.x_stride, a.T, a.B, kD,
+                           (uint32_t)(kTT + a.W - 1));
 }
 
 template <typename TIn, int WC>

@@ -138,15 +138,6 @@ __device__ __forceinline__ void split8x3(const float (&v)[8], uint4 &p1, uint4 &
     p3 = make_uint4(c[0], c[1], c[2], c[3]);
 }
 
-__device__ __forceinline__ void split1x3(float v, __nv_bfloat16 &p1, __nv_bfloat16 &p2,
-                                         __nv_bfloat16 &p3)
-{
-    p1 = __float2bfloat16_rn(v);
-    const float r = v - __bfloat162float(p1);
-    p2 = __float2bfloat16_rn(r);
-    p3 = __float2bfloat16_rn(r - __bfloat162float(p2));
-}
-
 // Two-float arithmetic for the in-chunk cumulative decay Gam: its values reach
 // hundreds while the decays exp(Gam_t - Gam_s) need the differences to full
 // float precision, so Gam is carried as hi + lo (Knuth's TwoSum keeps the
@@ -481,7 +472,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a)
         if (tid == 0) {
 #pragma unroll 1
             for (int kk = 0; kk < kD / 16; ++kk) {
-                const uint32_t ko = kk * 256;
                 // [Q; K] tile: K slice kk at atom column kk / 4, 32 bytes per slice inside it
                 const uint32_t kq = (kk >> 2) * (2 * kC * 128) + (kk & 3) * 32;
                 const uint64_t a1 = tc::sdesc_sw128(sbase + QK_HI + kq);
