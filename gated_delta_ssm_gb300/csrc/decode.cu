@@ -12,6 +12,7 @@
 // owner rewrites it, and carries the gated-norm partial sums between the row
 // slices of a head through distributed shared memory.
 #include <cooperative_groups.h>
+#include <type_traits>
 
 #include "cluster.cuh"
 #include "gdn_device.cuh"
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(256) gated_norm_kernel(const float *y, const f
 // bf16-state decode (NTOK = 1 only), whose rows are widened to fp32 on load,
 // stepped in fp32 and rounded to nearest even on store.
 template <typename TIn, int NTOK, int NSPLIT, typename TS = float>
-__global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
+__global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_kernel(FusedArgs a)
 {
     static_assert(sizeof(TS) == 4 || NTOK == 1, "snapshots are float32");
     TS *const state = static_cast<TS *>(a.state);
@@ -152,7 +153,9 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
     // (1) this warp's state rows: loads in flight during the prologue
     const size_t head_off = ((size_t)b * a.Hv + h) * kD * kD;
     const size_t warp_off = (size_t)(row0 + warp * RPW) * kD;
-    float4 st[NG][4];
+    // float32 rows as float4; bf16 rows stay packed (half the registers: 3 CTAs per SM)
+    using Reg = typename std::conditional<sizeof(TS) == 4, float4, uint2>::type;
+    Reg st[NG][4];
     load_rows<NG>(state + head_off + warp_off, st);
 
     // (2) conv windows: Q/K channel (every thread), V channel (threads < ROWS); gate inputs
@@ -220,7 +223,7 @@ __global__ void __launch_bounds__(256, 2) decode_fused_kernel(FusedArgs a)
 
     // (5) recurrence over this CTA's rows, in registers; the rows go back to HBM group
     // by group as they are finished
-    step_rows<NG, NTOK, SNAP, TS>(st, SNAP ? static_cast<float *>(a.state_snap) + head_off + warp_off
+    step_rows<NG, NTOK, SNAP, TS, Reg>(st, SNAP ? static_cast<float *>(a.state_snap) + head_off + warp_off
                                            : nullptr,
                                   sk, sq, sv, ROWS, sdecay, sbeta, sy, warp * RPW, a.scale,
                                   state + head_off + warp_off);

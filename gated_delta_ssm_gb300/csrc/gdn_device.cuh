@@ -259,6 +259,24 @@ __device__ __forceinline__ void load_rows(const float *rows, float4 (&r)[NG][4])
             r[gi][m] = ld_stream(rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4);
 }
 
+// Row registers to and from fp32 float4 (identity for float32 rows; packed bf16
+// pairs are widened exactly and rounded to nearest even).
+__device__ __forceinline__ float4 to_f4(float4 v) { return v; }
+__device__ __forceinline__ float4 to_f4(uint2 u)
+{
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+__device__ __forceinline__ void from_f4(float4 v, float4 &r) { r = v; }
+__device__ __forceinline__ void from_f4(float4 v, uint2 &r)
+{
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    r.x = *reinterpret_cast<const uint32_t *>(&lo);
+    r.y = *reinterpret_cast<const uint32_t *>(&hi);
+}
+
 // One float4 of a row to its storage type (streaming store; bf16: round to nearest even).
 __device__ __forceinline__ void store_one(float *p, float4 v) { st_stream(p, v); }
 __device__ __forceinline__ void store_one(__nv_bfloat16 *p, float4 v)
@@ -274,8 +292,8 @@ __device__ __forceinline__ void store_one(__nv_bfloat16 *p, float4 v)
 // final_rows, when given, receives each 4-row group as soon as its last token
 // is applied, so the write traffic starts while later groups are still being
 // stepped (the single-token kernels otherwise keep the rows until the norm).
-template <int NG, int NTOK, bool SNAP, typename TSt = float>
-__device__ __forceinline__ void step_rows(float4 (&r)[NG][4], float *snap_rows,
+template <int NG, int NTOK, bool SNAP, typename TSt = float, typename Reg = float4>
+__device__ __forceinline__ void step_rows(Reg (&r)[NG][4], float *snap_rows,
                                           const float *sk, const float *sq, const float *sv,
                                           int v_stride, const float *sdecay, const float *sbeta,
                                           float *sy, int local_row0, float scale,
@@ -306,20 +324,24 @@ __device__ __forceinline__ void step_rows(float4 (&r)[NG][4], float *snap_rows,
         const float beta = sbeta[p];
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi) {
-            float pk = __fmul_rn(r[gi][0].x, k4[0].x);
-            float pq = __fmul_rn(r[gi][0].x, q4[0].x);
+            float4 f[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                f[m] = to_f4(r[gi][m]);
+            float pk = __fmul_rn(f[0].x, k4[0].x);
+            float pq = __fmul_rn(f[0].x, q4[0].x);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 if (m > 0) {
-                    pk = __fmaf_rn(r[gi][m].x, k4[m].x, pk);
-                    pq = __fmaf_rn(r[gi][m].x, q4[m].x, pq);
+                    pk = __fmaf_rn(f[m].x, k4[m].x, pk);
+                    pq = __fmaf_rn(f[m].x, q4[m].x, pq);
                 }
-                pk = __fmaf_rn(r[gi][m].y, k4[m].y, pk);
-                pq = __fmaf_rn(r[gi][m].y, q4[m].y, pq);
-                pk = __fmaf_rn(r[gi][m].z, k4[m].z, pk);
-                pq = __fmaf_rn(r[gi][m].z, q4[m].z, pq);
-                pk = __fmaf_rn(r[gi][m].w, k4[m].w, pk);
-                pq = __fmaf_rn(r[gi][m].w, q4[m].w, pq);
+                pk = __fmaf_rn(f[m].y, k4[m].y, pk);
+                pq = __fmaf_rn(f[m].y, q4[m].y, pq);
+                pk = __fmaf_rn(f[m].z, k4[m].z, pk);
+                pq = __fmaf_rn(f[m].z, q4[m].z, pq);
+                pk = __fmaf_rn(f[m].w, k4[m].w, pk);
+                pq = __fmaf_rn(f[m].w, q4[m].w, pq);
             }
             pk = row8_sum(pk);
             pq = row8_sum(pq);
@@ -328,10 +350,11 @@ __device__ __forceinline__ void step_rows(float4 (&r)[NG][4], float *snap_rows,
             const float delta = __fmul_rn(beta, __fsub_rn(vj, __fmul_rn(decay, pk)));
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                r[gi][m].x = __fmaf_rn(delta, k4[m].x, __fmul_rn(decay, r[gi][m].x));
-                r[gi][m].y = __fmaf_rn(delta, k4[m].y, __fmul_rn(decay, r[gi][m].y));
-                r[gi][m].z = __fmaf_rn(delta, k4[m].z, __fmul_rn(decay, r[gi][m].z));
-                r[gi][m].w = __fmaf_rn(delta, k4[m].w, __fmul_rn(decay, r[gi][m].w));
+                f[m].x = __fmaf_rn(delta, k4[m].x, __fmul_rn(decay, f[m].x));
+                f[m].y = __fmaf_rn(delta, k4[m].y, __fmul_rn(decay, f[m].y));
+                f[m].z = __fmaf_rn(delta, k4[m].z, __fmul_rn(decay, f[m].z));
+                f[m].w = __fmaf_rn(delta, k4[m].w, __fmul_rn(decay, f[m].w));
+                from_f4(f[m], r[gi][m]);
             }
             const float y = __fmul_rn(scale, __fmaf_rn(delta, kq, __fmul_rn(decay, pq)));
             if (sub == 0)
@@ -339,15 +362,18 @@ __device__ __forceinline__ void step_rows(float4 (&r)[NG][4], float *snap_rows,
             if (final_rows != nullptr && p == NTOK - 1) {
 #pragma unroll
                 for (int m = 0; m < 4; ++m)
-                    store_one(final_rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4, r[gi][m]);
+                    store_one(final_rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4, f[m]);
             }
         }
-        if (SNAP && p == 0) {
+        if constexpr (SNAP) {
+            if (p == 0) {
 #pragma unroll
-            for (int gi = 0; gi < NG; ++gi)
+                for (int gi = 0; gi < NG; ++gi)
 #pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    st_stream(snap_rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4, r[gi][m]);
+                    for (int m = 0; m < 4; ++m)
+                        st_stream(snap_rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4,
+                                  to_f4(r[gi][m]));
+            }
         }
     }
 }
@@ -368,11 +394,12 @@ __device__ __forceinline__ void store_rows(const float4 (&r)[NG][4], float *rows
 }
 
 // bf16 storage of the same rows (the bf16-state decode): lane l holds the same
-// 16 columns as above, loaded as four 8-byte groups (each warp load instruction
-// covers 64 contiguous bytes of four rows), widened exactly to fp32; stores
-// round to nearest even.
+// 16 columns as above as four 8-byte groups of packed bf16 pairs (each warp
+// load instruction covers 64 contiguous bytes of four rows). The rows stay
+// packed in registers, half the registers of the float32 rows, and are widened
+// exactly to fp32 group by group as they are stepped.
 template <int NG>
-__device__ __forceinline__ void load_rows(const __nv_bfloat16 *rows, float4 (&r)[NG][4])
+__device__ __forceinline__ void load_rows(const __nv_bfloat16 *rows, uint2 (&r)[NG][4])
 {
     const int lane = threadIdx.x & 31;
     const int rg = lane >> 3;
@@ -380,33 +407,9 @@ __device__ __forceinline__ void load_rows(const __nv_bfloat16 *rows, float4 (&r)
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi)
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(
+        for (int m = 0; m < 4; ++m)
+            r[gi][m] = __ldcs(reinterpret_cast<const uint2 *>(
                 rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4));
-            const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-            const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-            r[gi][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
-        }
-}
-
-template <int NG>
-__device__ __forceinline__ void store_rows(const float4 (&r)[NG][4], __nv_bfloat16 *rows)
-{
-    const int lane = threadIdx.x & 31;
-    const int rg = lane >> 3;
-    const int sub = lane & 7;
-#pragma unroll
-    for (int gi = 0; gi < NG; ++gi)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(r[gi][m].x, r[gi][m].y);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(r[gi][m].z, r[gi][m].w);
-            uint2 u;
-            u.x = *reinterpret_cast<const uint32_t *>(&lo);
-            u.y = *reinterpret_cast<const uint32_t *>(&hi);
-            __stcs(reinterpret_cast<uint2 *>(rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4),
-                   u);
-        }
 }
 
 // One output value in the storage type (bf16: round to nearest even).
