@@ -12,7 +12,7 @@
 
 namespace gdn {
 
-constexpr int kD = 128;        // head_dim this build supports
+constexpr int kD = 128;        // head_dim this library supports
 constexpr int kMaxW = 8;       // largest conv tap count
 constexpr float kSoftplusGuard = 20.0f;
 

@@ -15,12 +15,12 @@
  *               except GDN_ERR_CUDA, where the launch itself failed;
  *               gdn_last_cuda_error() then names the CUDA error.
  *   Reentrancy  The library holds no mutable global state besides the
- *               last-error text (per host thread) and one device-side error
- *               word (see gdn_check_device): calls from several host threads
+ *               last-error text (per host thread) and the device-side error
+ *               bits (see gdn_check_device): calls from several host threads
  *               and streams are safe as long as their buffers do not overlap.
  *   Precision   Parameters, recurrent state, conv history and all outputs are
- *               float32; activations are float32 or bf16 (gdn_dtype). All
- *               arithmetic is float32.
+ *               float32 (gdn_decode_step_bf16_state excepted); activations are
+ *               float32 or bf16 (gdn_dtype). All arithmetic is float32.
  *
  * SHAPES (gdn_dims)
  *   B   = n_seq, Hq = n_qk_heads, Hv = n_v_heads (a multiple of Hq; r = Hv/Hq),
@@ -61,7 +61,7 @@ typedef struct CUstream_st *gdn_stream_t;
 typedef enum gdn_status {
     GDN_OK = 0,
     GDN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, stride too small, misalignment */
-    GDN_ERR_UNSUPPORTED = 2,  /* a valid shape this build has no kernel for (d != 128, W > 8, r > 8) */
+    GDN_ERR_UNSUPPORTED = 2,  /* a valid shape this library has no kernel for (d != 128, W > 8, r > 8) */
     GDN_ERR_CUDA = 3,         /* the launch failed; see gdn_last_cuda_error() */
     GDN_ERR_DEVICE = 4        /* a kernel's bounded wait gave up (see gdn_check_device) */
 } gdn_status;
@@ -183,9 +183,9 @@ gdn_status gdn_decode_step(float *state, float *conv_state, const void *x, const
 
 /*
  * gdn_decode_step with the recurrent state and the output stored as bf16: a
- * serving option that halves the state traffic of a decode step. The pages
- * define no such variant (their state is float32); it is offered outside the
- * float32 tolerances. Each state row is widened exactly to float32, stepped
+ * serving option that halves the state traffic of a decode step. None of the
+ * source pages defines such a variant (their state is float32); it is offered
+ * outside the float32 tolerances. Each state row is widened exactly to float32, stepped
  * with the same float32 arithmetic as gdn_decode_step (the readout uses the
  * updated row before it is rounded), and rounded to nearest even when stored;
  * each output value is rounded to nearest even.
