@@ -75,6 +75,7 @@ def test_decode_step_rejects_null_pointers(lib, field):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(n_seq=0), gdn.GDN_ERR_INVALID_ARG),
+    (dict(n_seq=65536), gdn.GDN_ERR_INVALID_ARG),                    # one past the grid limit
     (dict(n_qk_heads=3, n_v_heads=4), gdn.GDN_ERR_INVALID_ARG),      # Hv not a multiple of Hq
     (dict(head_dim=64), gdn.GDN_ERR_UNSUPPORTED),
     (dict(d_conv=1), gdn.GDN_ERR_UNSUPPORTED),

@@ -374,6 +374,23 @@ def test_result_independent_of_batch_split():
     assert torch.equal(st1[0], st_big[b])
 
 
+def test_decode_at_the_largest_batch():
+    # n_seq = 65535, the largest the entry points accept (one CTA row per sequence);
+    # the first, a middle and the last sequence are held to the oracle
+    shape = synth.Shape(B=65535, T=1, Hq=1, Hv=1, warm=False)
+    inp = synth.make_inputs(shape, seed=36)
+    dev = device_inputs(shape, inp)
+    out = torch.empty(shape.B, shape.Hv, shape.d, device="cuda")
+    gdn.decode_step(dev["state"], dev["hist"], dev["x"], dev["z"], dev["alpha"],
+                    dev["beta_logit"], params_of(dev), out, dims_of(shape))
+    torch.cuda.synchronize()
+    seqs = [0, 32767, 65534]
+    ref = run_oracle(shape, inp, seqs=seqs)
+    assert out_rel(out.cpu().numpy()[seqs], ref["out"][:, 0]) <= OUT_TOL
+    assert max_rel(dev["state"][seqs].cpu().numpy(), ref["state"], 2) <= STATE_TOL
+    assert np.array_equal(dev["hist"][seqs].cpu().numpy(), ref["hist"].astype(np.float32))
+
+
 def test_repeat_runs_are_deterministic():
     shape = synth.WORKLOADS["decode_b64"]
     inp = synth.make_inputs(shape, seed=26)
