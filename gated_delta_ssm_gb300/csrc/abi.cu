@@ -416,7 +416,7 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
     a.l2_eps = params->l2_eps;
     a.rms_eps = params->rms_eps;
     a.scale = 1.0f / sqrtf((float)dims->head_dim);
-    return from_cuda(gdn::launch_prefill(a, act_dtype == GDN_BF16, as_cuda(stream)));
+    return from_cuda(gdn::launch_prefill_tc(a, act_dtype == GDN_BF16, as_cuda(stream)));
 }
 
 gdn_status gdn_check_device(int32_t *code)

@@ -87,7 +87,6 @@ cudaError_t launch_gated_norm(const float *y, const float *w, const void *z, boo
 cudaError_t launch_verify_commit(float *state, float *conv_state, const float *state_snap,
                                  const float *conv_snap, const int32_t *n_accept, int B,
                                  int64_t state_elems, int64_t hist_elems, cudaStream_t s);
-cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s);
 cudaError_t take_decode_device_error(int *code);
 cudaError_t launch_recurrence_scan(const RecScanArgs &a, cudaStream_t s);
 cudaError_t launch_layer_scan(const LayerScanArgs &a, bool bf16, cudaStream_t s);
@@ -98,6 +97,5 @@ cudaError_t take_sequential_device_error(int *code);
 cudaError_t take_conv_device_error(int *code);
 cudaError_t take_prefill_device_error(int *code);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, bool bf16, cudaStream_t s);
-cudaError_t launch_prefill_simt(const PrefillArgs &a, bool bf16, cudaStream_t s);
 
 }  // namespace gdn
