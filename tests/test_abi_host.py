@@ -155,3 +155,30 @@ def test_verify_kn_requires_distinct_snapshots(lib):
 def test_binding_raises_loudly_on_bad_status(lib):
     with pytest.raises(gdn.GdnError):
         gdn._check(gdn.GDN_ERR_INVALID_ARG, "gdn_decode_step")
+
+
+def test_header_is_plain_c99(tmp_path):
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "uses_header.c"
+    src.write_text('#include "gdn.h"\nint main(void) { return (int)GDN_OK + (int)sizeof(gdn_dims); }\n')
+    r = subprocess.run([cc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_c_client_compiles_as_c():
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = "/usr/local/cuda/include"
+    if cc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime.h")):
+        pytest.skip("no C compiler or CUDA headers")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+                        os.path.join(ROOT, "tests", "c_client", "gdn_c_client.c")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
