@@ -19,7 +19,8 @@ import threading as _th
 __all__ = [
     "Dims", "Params", "GdnError", "load", "library_path",
     "decay_gate", "conv_update", "recurrence_decode", "gated_norm",
-    "decode_step", "verify_k2", "verify_commit", "prefill_chunked", "recurrence_scan",
+    "decode_step", "verify_k2", "verify_commit", "prefill_chunked", "prefill_workspace_bytes",
+    "recurrence_scan",
     "layer_scan", "verify_kn", "verify_commit_kn", "decode_step_bf16_state", "check_device",
     "version",
 ]
@@ -114,7 +115,8 @@ def load():
             "gdn_decode_step_bf16_state": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, vp],
             "gdn_verify_k2": [vp, vp, vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, vp],
             "gdn_verify_commit": [vp, vp, vp, vp, vp, pd, vp],
-            "gdn_prefill_chunked": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, i32, i32, vp],
+            "gdn_prefill_chunked": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, i32, i32, vp,
+                                    _ct.c_size_t, vp],
             "gdn_recurrence_scan": [vp, vp, vp, vp, i64, vp, vp, vp, pd, i32, f32, vp],
             "gdn_layer_scan": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, i32, vp],
             "gdn_verify_kn": [vp, vp, vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, i32, vp],
@@ -127,6 +129,10 @@ def load():
         for name in ("gdn_last_cuda_error", "gdn_version"):
             getattr(L, name).restype = _ct.c_char_p
             getattr(L, name).argtypes = []
+        L.gdn_prefill_workspace_bytes.restype = _ct.c_size_t
+        L.gdn_prefill_workspace_bytes.argtypes = [pd, i32, i32]
+        L.gdn_testing_set_first_wait_ns.restype = None
+        L.gdn_testing_set_first_wait_ns.argtypes = [_ct.c_uint64]
         L.gdn_check_device.restype = _ct.c_int
         L.gdn_check_device.argtypes = [_ct.POINTER(_ct.c_int32)]
         L.gdn_status_string.restype = _ct.c_char_p
@@ -253,13 +259,33 @@ def verify_commit(state, conv_state, state_snap, conv_snap, n_accept, dims: Dims
            "gdn_verify_commit")
 
 
+def prefill_workspace_bytes(dims: Dims, n_tokens: int, chunk: int = 64) -> int:
+    """Bytes of device workspace gdn_prefill_chunked needs (0 for invalid arguments)."""
+    cd = dims.c()
+    return int(load().gdn_prefill_workspace_bytes(_ct.byref(cd), n_tokens, chunk))
+
+
 def prefill_chunked(state, conv_state, x, z, alpha, beta_logit, params: Params, out, dims: Dims,
-                    n_tokens: int, chunk: int = 64, stream=None):
+                    n_tokens: int, chunk: int = 64, workspace=None, stream=None):
+    """workspace: a device tensor of at least prefill_workspace_bytes(dims, n_tokens, chunk)
+    bytes; when None, one is allocated with torch for this call."""
     cd, cp = dims.c(), params.c()
+    if workspace is None:
+        import torch
+        nbytes = prefill_workspace_bytes(dims, n_tokens, chunk)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
     _check(load().gdn_prefill_chunked(_ptr(state), _ptr(conv_state), _ptr(x), _ptr(z), _ptr(alpha),
                                       _ptr(beta_logit), _dtype(x), _ct.byref(cp), _ptr(out),
-                                      _ct.byref(cd), n_tokens, chunk, _stream(stream)),
+                                      _ct.byref(cd), n_tokens, chunk, _ptr(workspace), ws_bytes,
+                                      _stream(stream)),
            "gdn_prefill_chunked")
+
+
+def testing_set_first_wait_ns(ns: int):
+    """Test hook (include/gdn_testing.h): limit of the prefill's and the tiled conv's first
+    bounded wait, in GPU global-timer nanoseconds, for later calls (0 = default)."""
+    load().gdn_testing_set_first_wait_ns(int(ns))
 
 
 def recurrence_scan(state, q, k, v, qkv_stride: int, g, beta, y, dims: Dims, n_tokens: int,

@@ -5,9 +5,23 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "../../include/gdn.h"
+#include "../../include/gdn_testing.h"
 #include "gdn_device.cuh"
 #include "gdn_kernels.h"
+
+namespace gdn {
+namespace {
+std::atomic<uint64_t> g_first_wait_ns{0};
+}
+uint64_t first_wait_override_ns()
+{
+    const uint64_t v = g_first_wait_ns.load(std::memory_order_relaxed);
+    return v != 0 ? v : kDefaultWaitNs;
+}
+}  // namespace gdn
 
 namespace {
 
@@ -211,6 +225,7 @@ gdn_status gdn_conv_update(float *conv_state, const void *x, gdn_dtype x_dtype,
     a.conv_dim = conv_dim_of(dims);
     a.T = n_tokens;
     a.l2_eps = l2_eps;
+    a.first_wait_ns = gdn::first_wait_override_ns();
     return from_cuda(gdn::launch_conv_update(a, x_dtype == GDN_BF16, as_cuda(stream)));
 }
 
@@ -370,10 +385,19 @@ gdn_status gdn_verify_commit_kn(float *state, float *conv_state, const float *st
         as_cuda(stream)));
 }
 
+size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t n_tokens, int32_t chunk)
+{
+    if (check_dims(dims, 0) != GDN_OK || n_tokens < 1 || chunk != 64)
+        return 0;
+    const int64_t n_chunks = ((int64_t)n_tokens + 63) / 64;
+    return (size_t)dims->n_seq * (size_t)dims->n_v_heads * (size_t)n_chunks * gdn::kPrefillChunkImage;
+}
+
 gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, const void *z,
                                const void *alpha, const void *beta_logit, gdn_dtype act_dtype,
                                const gdn_params *params, float *out, const gdn_dims *dims,
-                               int32_t n_tokens, int32_t chunk, gdn_stream_t stream)
+                               int32_t n_tokens, int32_t chunk, void *workspace,
+                               size_t workspace_bytes, gdn_stream_t stream)
 {
     gdn_status st = check_dims(dims, 7);
     if (st != GDN_OK)
@@ -382,16 +406,22 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
         return st;
     if (!valid_dtype(act_dtype) || n_tokens < 1)
         return GDN_ERR_INVALID_ARG;
-    if (!state || !conv_state || !x || !z || !alpha || !beta_logit || !out)
+    if (!state || !conv_state || !x || !z || !alpha || !beta_logit || !out || !workspace)
         return GDN_ERR_INVALID_ARG;
     const size_t es = act_size(act_dtype);
-    // the chunk kernel reads 8 channels of a token row per 16-byte load
+    // the chunk kernels read 4 channels of a token row per 8- or 16-byte load
     if (!aligned(state, 16) || !aligned(x, 16) || (dims->x_stride * (int64_t)es) % 16 != 0 ||
-        !aligned(params->conv_w, 16) ||
+        !aligned(params->conv_w, 16) || !aligned(workspace, 16) ||
         !aligned(z, es) || !aligned(alpha, es) || !aligned(beta_logit, es) || !aligned(out, 16))
         return GDN_ERR_INVALID_ARG;
     if (chunk != 64)
         return GDN_ERR_UNSUPPORTED;
+    const size_t need = gdn_prefill_workspace_bytes(dims, n_tokens, chunk);
+    if (need == 0 || workspace_bytes < need)
+        return GDN_ERR_INVALID_ARG;
+    const int64_t n_chunks = ((int64_t)n_tokens + 63) / 64;
+    if (n_chunks > INT32_MAX)
+        return GDN_ERR_INVALID_ARG;
     gdn::PrefillArgs a;
     a.state = state;
     a.conv_state = conv_state;
@@ -404,6 +434,7 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
     a.A_log = params->A_log;
     a.norm_w = params->norm_w;
     a.out = out;
+    a.ws = static_cast<uint8_t *>(workspace);
     a.x_stride = dims->x_stride;
     a.z_stride = dims->z_stride;
     a.gate_stride = dims->gate_stride;
@@ -413,10 +444,18 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
     a.W = dims->d_conv;
     a.conv_dim = conv_dim_of(dims);
     a.T = n_tokens;
+    a.n_chunks = (int)n_chunks;
     a.l2_eps = params->l2_eps;
     a.rms_eps = params->rms_eps;
     a.scale = 1.0f / sqrtf((float)dims->head_dim);
-    return from_cuda(gdn::launch_prefill_tc(a, act_dtype == GDN_BF16, as_cuda(stream)));
+    a.wait_ns = gdn::kDefaultWaitNs;
+    a.first_wait_ns = gdn::first_wait_override_ns();
+    return from_cuda(gdn::launch_prefill(a, act_dtype == GDN_BF16, as_cuda(stream)));
+}
+
+void gdn_testing_set_first_wait_ns(uint64_t ns)
+{
+    gdn::g_first_wait_ns.store(ns, std::memory_order_relaxed);
 }
 
 gdn_status gdn_check_device(int32_t *code)

@@ -149,7 +149,6 @@ constexpr int kTokensPerThread = 16;
 // then the four group sums in order, as in head_l2_inv.
 constexpr int kTT = 64;
 constexpr int kTileRows = kTT + kMaxW - 1;
-constexpr int kConvWaitLimit = 1 << 26;
 // Row stride of the per-warp squares buffer: 16-byte rows for vector reads,
 // and 36 mod 32 = 4 keeps each quarter-warp's 16-byte reads on distinct banks.
 constexpr int kSqStride = 36;
@@ -214,7 +213,7 @@ __global__ void __launch_bounds__(256) conv_tiles_kernel(const __grid_constant__
         const int buf = k & 1;
         if (tid == 0 && item + (int)gridDim.x < n_items)
             issue(item + gridDim.x, buf ^ 1);
-        if (!tc::mbar_wait(mbar0 + 8 * buf, (k >> 1) & 1, kConvWaitLimit))
+        if (!tc::mbar_wait_ns(mbar0 + 8 * buf, (k >> 1) & 1, k == 0 ? a.first_wait_ns : kDefaultWaitNs))
             *sflag = 1;
         __syncthreads();
         if (*sflag)
@@ -309,9 +308,9 @@ __global__ void __launch_bounds__(256) conv_tiles_kernel(const __grid_constant__
     if (*sflag && tid == 0) {
         atomicOr(&g_conv_error, kErrConvWait);
         // let the copies this CTA issued finish before it exits
-        tc::mbar_wait(mbar0 + 8 * (k & 1), (k >> 1) & 1, kConvWaitLimit);
+        tc::mbar_wait_ns(mbar0 + 8 * (k & 1), (k >> 1) & 1, kDefaultWaitNs);
         if (blockIdx.x + (k + 1) * gridDim.x < (unsigned)n_items)
-            tc::mbar_wait(mbar0 + 8 * ((k + 1) & 1), ((k + 1) >> 1) & 1, kConvWaitLimit);
+            tc::mbar_wait_ns(mbar0 + 8 * ((k + 1) & 1), ((k + 1) >> 1) & 1, kDefaultWaitNs);
     }
 }
 

@@ -28,6 +28,7 @@ struct ConvArgs {
     int64_t x_stride;
     int B, Hq, Hv, W, conv_dim, T;
     float l2_eps;
+    uint64_t first_wait_ns;  // limit of each CTA's first tile wait (global-timer ns)
 };
 
 struct RecArgs {
@@ -70,10 +71,21 @@ struct PrefillArgs {
     const void *x, *z, *alpha, *beta_logit;
     const float *conv_w, *dt, *A_log, *norm_w;
     float *out;            // [B][T][Hv][d]
+    uint8_t *ws;           // [B][Hv][n_chunks] chunk images of (I + A)^-1, 16 KB each
     int64_t x_stride, z_stride, gate_stride;
-    int B, Hq, Hv, W, conv_dim, T;
+    int B, Hq, Hv, W, conv_dim, T, n_chunks;
     float l2_eps, rms_eps, scale;
+    uint64_t wait_ns;        // limit of every bounded wait (global-timer nanoseconds)
+    uint64_t first_wait_ns;  // limit of the chain kernel's first wait
 };
+
+// Bytes of one chunk's (I + A)^-1 image in the prefill workspace.
+constexpr size_t kPrefillChunkImage = 16384;
+
+// Default limit of a bounded wait, and the test-only override of one prefill
+// wait and of the tiled conv's first tile wait (0 = the default).
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+uint64_t first_wait_override_ns();
 
 cudaError_t launch_decode_fused(const FusedArgs &a, bool bf16, int ntok, cudaStream_t s);
 cudaError_t launch_decode_fused_bf16_state(const FusedArgs &a, bool bf16, cudaStream_t s);
@@ -96,6 +108,6 @@ cudaError_t launch_verify_commit_kn(float *state, float *conv_state, const float
 cudaError_t take_sequential_device_error(int *code);
 cudaError_t take_conv_device_error(int *code);
 cudaError_t take_prefill_device_error(int *code);
-cudaError_t launch_prefill_tc(const PrefillArgs &a, bool bf16, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s);
 
 }  // namespace gdn

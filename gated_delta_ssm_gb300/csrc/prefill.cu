@@ -1,0 +1,1242 @@
+// prefill.cu -- chunked prefill in two passes, on the tcgen05 tensor cores.
+//
+// The chunk algebra is derived from the recurrence of "fm_kernel_ssm.h",
+// section "Delta-rule recurrence", over 64-token chunks joined by ceil(T/64)
+// sequential state links (the "Mamba-2 SSD chunked prefill scan" note of
+// "ssm_mamba.rs"). Per (sequence, V head, chunk), with Gam_t the in-chunk
+// cumulative decay, S_0 the entering state (plain orientation S[i][j], i the
+// key index, j the value index), K, Q the L2-normalised key / query rows and
+// V the value rows of the chunk:
+//   A   = strictly lower part of diag(beta) (e^{Gam_t - Gam_s}) (K K^T)
+//   T   = (I + A)^-1                                   (the chunk's UT transform)
+//   X   = diag(beta) (V - diag(e^Gam) K S_0)
+//   U   = T X                                          (the delta-rule updates)
+//   O   = diag(e^Gam) Q S_0 + P U,  P = lower part (s <= t) of e^{Gam_t - Gam_s} (Q K^T)
+//   S_C = e^{Gam_C} S_0 + K^T diag(e^{Gam_C - Gam}) U
+//
+// Pass 1 (prefill_ut_kernel) is parallel over every (sequence, QK head,
+// chunk): it stages the chunk's raw K rows in shared memory by tensor copy,
+// runs the conv + SiLU + L2 on them, forms K K^T on the tensor core, and for
+// each V head of the group builds A and solves T = (I + A)^-1 by blocked
+// forward substitution, writing T as a 16 KB two-part fp16 operand image to the
+// caller's workspace. Nothing in it depends on the state.
+//
+// Pass 2 (prefill_chain_kernel) walks the chunks of one (sequence, V head)
+// with the fp32 state master in tensor memory. Its warps are specialised:
+//   * an issue warp: the bulk/tensor copies of the next chunks' raw rows and
+//     T images, and every tensor-core product;
+//   * 8 conv warps: conv + SiLU + L2 of chunk c+1's Q, K, V rows (from the
+//     staged rows) and the gates, while chunk c's products run; P of chunk c;
+//   * 8 epilogue warps (two per TMEM lane quarter, value row j = lane):
+//     X, U, the state re-split, the state write-back, and the gated RMSNorm.
+// The products (transposed orientation, M = 128 value rows j, A operands in
+// tensor memory, B operands in shared memory):
+//   D1 = S_0^T [Q; K]^T        ((Q S_0)^T | (K S_0)^T)
+//   G  = [Q; K] K^T            (Q K^T for P)
+//   D2 = X^T T^T = U^T         (the UT transform on the tensor core)
+//   S^T += U'^T K              (U' = diag(e^{Gam_C - Gam}) U; K read MN-major)
+//   (P U)^T = U^T P^T          (into D2 once U^T is read; O = e^Gam Q S_0 + P U is
+//                               summed in the epilogue)
+// so that the sequential part per chunk is three products and three short
+// epilogues; everything that does not depend on the state runs ahead.
+//
+// Precision: every operand is an fp32 value split into two fp16 parts
+// (x = x1 + x2, ~22 bits; products x1 y1 + x1 y2 + x2 y1), accumulation fp32.
+//
+// Every wait is bounded by the global timer (PrefillArgs::wait_ns); a wait that
+// gives up sets a bit of the device error word, the other roles stop at their
+// next wait, in-flight copies and products are drained, tensor memory is freed
+// and the kernel returns.
+#include <algorithm>
+
+#include <cuda_fp16.h>
+
+#include "gdn_device.cuh"
+#include "gdn_kernels.h"
+#include "tc_ptx.cuh"
+#include "tma_map.cuh"
+
+namespace gdn {
+
+// Set when a bounded wait of a kernel in this file gives up; read and cleared
+// by take_prefill_device_error.
+static __device__ int g_device_error;
+
+namespace {
+
+constexpr int kC = 64;
+constexpr uint32_t kErrChain = 1, kErrUT = 2, kErrDrain = 8;
+// The normalised Q / K rows (entries at most 1) enter the tensor core scaled by
+// 16, so that the low fp16 part of most entries is a normal number; every
+// product that contains them is scaled back by the same power of two.
+constexpr float kQK = 16.0f, kInvQK = 1.0f / 16.0f, kInvQK2 = 1.0f / 256.0f;
+
+// ------------------------------------------------------------------ small helpers
+// Tensor-core operands are fp32 values split into two fp16 parts, x = hi + lo
+// (hi = fp16(x), lo = fp16(x - hi)): 22 significant bits for |x| >= 0.25 and an
+// absolute representation error below 2^-25 for smaller x, at the price of
+// fp16's range (every operand, i.e. the normalised Q/K rows, the state, X, U, P
+// and T, must stay below 65504 in magnitude). Both pairs packed, element a in
+// the low half.
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t &hi, uint32_t &lo)
+{
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(__fsub_rn(a, hf.x), __fsub_rn(b, hf.y));
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+// Two-float arithmetic for the in-chunk cumulative decay Gam: its values reach
+// hundreds while the decays exp(Gam_t - Gam_s) need the differences to full
+// float precision, so Gam is carried as hi + lo (Knuth's TwoSum keeps the
+// rounding error of every addition).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ void two_add(float &h, float &l, float bh, float bl)
+{
+    float s, e;
+    two_sum(h, bh, s, e);
+    const float t = __fadd_rn(__fadd_rn(l, bl), e);
+    h = __fadd_rn(s, t);
+    l = __fsub_rn(t, __fsub_rn(h, s));
+}
+
+// exp((ah + al) - (bh + bl)) with the difference formed exactly before rounding
+__device__ __forceinline__ float exp_diff(float ah, float al, float bh, float bl)
+{
+    float dh, de;
+    two_sum(ah, -bh, dh, de);
+    const float dl = __fadd_rn(de, __fsub_rn(al, bl));
+    return __fmul_rn(expf(dh), __fadd_rn(1.0f, dl));
+}
+
+// 2^e for an integer e in [-126, 127], exactly
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// One chunk's gate values ("fm_kernel_ssm.h" "Decay gate"; beta = sigmoid).
+//
+// The chain keeps the fp32 state master scaled by a power of two, 2^rho S, with
+// rho chosen per chunk from the gates so that the scaled state stays of order
+// one however strongly it has decayed: the fp16 operand parts split from it
+// (and the update U' that adds to it) then stay in fp16's normal range. The
+// factors below fold those exact powers of two in; chunk c enters with rho_c
+// and leaves with rho_{c+1}.
+struct Gates {
+    float beta[kC];        // beta_t, 0 at or past the end of the call
+    float gh[kC], gl[kC];  // Gam_t = g_0 + ... + g_t (two floats); g = 0 past the end
+    float eg[kC];          // exp(Gam_t) 2^-rho_c / 16          (scales 16 2^rho_c (Q S_0)^T)
+    float egc[kC];         // exp(Gam_C - Gam_t) 2^rho_{c+1} / 16, 0 past the end  (U' against 16 K)
+    float bg[kC];          // beta_t exp(Gam_t) 2^-rho_c / 16   (scales 16 2^rho_c (K S_0)^T)
+    float ec;              // exp(Gam_C) 2^(rho_{c+1} - rho_c)  (the scaled master's decay)
+    int rho;               // rho_c
+    int rho_next;          // rho_{c+1}
+    float pad[13];
+};
+
+// Gates of tokens c0 .. c0+n-1 of sequence b, V head h, entering with state
+// scale rho; executed by one warp.
+template <typename TIn>
+__device__ __forceinline__ void chunk_gates(const PrefillArgs &a, int b, int h, int c0, int n,
+                                            int rho, Gates *G)
+{
+    const int lane = threadIdx.x & 31;
+    const float dtv = __ldg(a.dt + h), alog = __ldg(a.A_log + h);
+    const int64_t row0 = (int64_t)b * a.T + c0;
+    const TIn *al = static_cast<const TIn *>(a.alpha) + row0 * a.gate_stride + h;
+    const TIn *bl = static_cast<const TIn *>(a.beta_logit) + row0 * a.gate_stride + h;
+    float gv[2], bv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int t = 2 * lane + u;
+        gv[u] = t < n ? decay_gate_f(load_act<TIn>(al + (int64_t)t * a.gate_stride), dtv, alog) : 0.0f;
+        bv[u] = t < n ? sigmoid_f(load_act<TIn>(bl + (int64_t)t * a.gate_stride)) : 0.0f;
+        G->beta[t] = bv[u];
+    }
+    // inclusive scan of the token pairs in two-float arithmetic
+    float ph, pl;
+    two_sum(gv[0], gv[1], ph, pl);
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float yh = __shfl_up_sync(0xffffffffu, ph, off);
+        const float yl = __shfl_up_sync(0xffffffffu, pl, off);
+        if (lane >= off)
+            two_add(ph, pl, yh, yl);
+    }
+    float exh = __shfl_up_sync(0xffffffffu, ph, 1);
+    float exl = __shfl_up_sync(0xffffffffu, pl, 1);
+    if (lane == 0)
+        exh = exl = 0.0f;
+    float g0h = exh, g0l = exl;
+    two_add(g0h, g0l, gv[0], 0.0f);
+    float g1h = g0h, g1l = g0l;
+    two_add(g1h, g1l, gv[1], 0.0f);
+    const float gch = __shfl_sync(0xffffffffu, g1h, 31);
+    const float gcl = __shfl_sync(0xffffffffu, g1l, 31);
+    G->gh[2 * lane] = g0h;
+    G->gl[2 * lane] = g0l;
+    G->gh[2 * lane + 1] = g1h;
+    G->gl[2 * lane + 1] = g1l;
+    // rho_{c+1}: with the entering scaled state of order one, the state after the
+    // chunk has magnitude about max(e^{Gam_C} 2^-rho_c, max_t beta_t e^{Gam_C - Gam_t})
+    // (times the values' scale); lmax is its log2 and rho_{c+1} = -lmax brings it
+    // back to order one. Since 2^rho_{c+1} <= 1 / (beta_t e^{Gam_C - Gam_t}), the
+    // update factors egc below stay bounded by 1 / (16 beta_t).
+    const float l2e = 1.4426950408889634f;
+    const float dc0 = 2 * lane < n ? exp_diff(gch, gcl, g0h, g0l) : 0.0f;
+    const float dc1 = 2 * lane + 1 < n ? exp_diff(gch, gcl, g1h, g1l) : 0.0f;
+    float lu = -1e30f;   // log2 of the largest update factor of the warp's two tokens
+    if (bv[0] > 0.0f && dc0 > 0.0f)
+        lu = __log2f(bv[0]) + __fmul_rn(__fadd_rn(__fsub_rn(gch, g0h), __fsub_rn(gcl, g0l)), l2e);
+    if (bv[1] > 0.0f && dc1 > 0.0f)
+        lu = fmaxf(lu, __log2f(bv[1]) + __fmul_rn(__fadd_rn(__fsub_rn(gch, g1h), __fsub_rn(gcl, g1l)), l2e));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1)
+        lu = fmaxf(lu, __shfl_xor_sync(0xffffffffu, lu, m));
+    const float lold = __fmul_rn(__fadd_rn(gch, gcl), l2e) - (float)rho;   // old state, in 2^rho units
+    const float lmax = fmaxf(lold, lu);
+    const int rho_next = (int)fminf(fmaxf(floorf(-lmax), 0.0f), 60.0f);
+    const float inv_in = __fmul_rn(exp2i(-rho), kInvQK), up_out = __fmul_rn(exp2i(rho_next), kInvQK);
+    const float e0 = __fmul_rn(exp_diff(g0h, g0l, 0.0f, 0.0f), inv_in);
+    const float e1 = __fmul_rn(exp_diff(g1h, g1l, 0.0f, 0.0f), inv_in);
+    G->eg[2 * lane] = e0;
+    G->eg[2 * lane + 1] = e1;
+    G->bg[2 * lane] = __fmul_rn(bv[0], e0);
+    G->bg[2 * lane + 1] = __fmul_rn(bv[1], e1);
+    G->egc[2 * lane] = __fmul_rn(dc0, up_out);
+    G->egc[2 * lane + 1] = __fmul_rn(dc1, up_out);
+    if (lane == 0) {
+        G->ec = __fmul_rn(exp_diff(gch, gcl, 0.0f, 0.0f), exp2i(rho_next - rho));
+        G->rho = rho;
+        G->rho_next = rho_next;
+    }
+}
+
+// conv + SiLU ("fm_kernel_ssm.h", "Causal depthwise conv1d + SiLU") of the
+// NCH (4 or 8) channels ch0 .. ch0+NCH-1 for tokens t0 .. t0+7 of the chunk that
+// starts at token c0 of the call; tokens at or past n give 0. Stream index
+// s < 0 of the call reads the fp32 history, s >= T reads 0. raw: the chunk's
+// rows of this channel's 128-channel head staged in shared memory
+// ([63 + W][128] bf16, row r = token c0 - (W-1) + r), or nullptr to read x
+// directly. Taps are summed oldest first.
+template <int NCH, typename TIn>
+__device__ __forceinline__ void load_row(const TIn *p, float (&v)[NCH]);
+template <>
+__device__ __forceinline__ void load_row<4, __nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[4])
+{
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+}
+template <>
+__device__ __forceinline__ void load_row<8, __nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[8])
+{
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        v[2 * e] = __uint_as_float(w[e] << 16);
+        v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+}
+template <>
+__device__ __forceinline__ void load_row<4, float>(const float *p, float (&v)[4])
+{
+    const float4 f = *reinterpret_cast<const float4 *>(p);
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+}
+template <>
+__device__ __forceinline__ void load_row<8, float>(const float *p, float (&v)[8])
+{
+    const float4 f = *reinterpret_cast<const float4 *>(p);
+    const float4 g = *reinterpret_cast<const float4 *>(p + 4);
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    v[4] = g.x; v[5] = g.y; v[6] = g.z; v[7] = g.w;
+}
+
+template <typename TIn, int WC, int NCH>
+__device__ __forceinline__ void conv_block(const PrefillArgs &a, int b, int c0, int n, int ch0,
+                                           int t0, const __nv_bfloat16 *raw, float (&out)[8][NCH])
+{
+    const int W = WC > 0 ? WC : a.W;
+    constexpr int WM = WC > 0 ? WC : kMaxW;
+    float w[NCH][WM];
+#pragma unroll
+    for (int e = 0; e < NCH; ++e) {
+        if (WC == 4) {
+            const float4 f = __ldg(reinterpret_cast<const float4 *>(a.conv_w + (size_t)(ch0 + e) * 4));
+            w[e][0] = f.x; w[e][1] = f.y; w[e][2] = f.z; w[e][3 % WM] = f.w;
+        } else {
+#pragma unroll
+            for (int tau = 0; tau < WM; ++tau)
+                w[e][tau] = tau < W ? __ldg(a.conv_w + (size_t)(ch0 + e) * W + tau) : 0.0f;
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int e = 0; e < NCH; ++e)
+            out[t][e] = 0.0f;
+    const int s0 = c0 + t0 - (W - 1);              // stream index of row 0 of the window
+    const bool inside = s0 >= 0 && s0 + 7 + W - 1 < a.T;   // no history, no tail rows
+    const TIn *xb = static_cast<const TIn *>(a.x) + ((int64_t)b * a.T + s0) * a.x_stride + ch0;
+    const __nv_bfloat16 *rb = raw != nullptr ? raw + t0 * kD + (ch0 & (kD - 1)) : nullptr;
+    const float *hist = a.conv_state + ((size_t)b * a.conv_dim + ch0) * (W - 1);
+#pragma unroll
+    for (int rr = 0; rr < 7 + WM; ++rr) {
+        if (WC == 0 && rr >= 7 + W)
+            break;
+        float v[NCH];
+        const int s = s0 + rr;
+        if (inside || (s >= 0 && s < a.T)) {
+            if (rb != nullptr)
+                load_row<NCH, __nv_bfloat16>(rb + rr * kD, v);
+            else
+                load_row<NCH, TIn>(xb + (int64_t)rr * a.x_stride, v);
+        } else if (s < 0) {
+#pragma unroll
+            for (int e = 0; e < NCH; ++e)
+                v[e] = hist[(size_t)e * (W - 1) + (W - 1 + s)];
+        } else {
+#pragma unroll
+            for (int e = 0; e < NCH; ++e)
+                v[e] = 0.0f;
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int tau = rr - t;               // tap that row rr feeds for token t
+            if (tau >= 0 && tau < WM && (WC > 0 || tau < W)) {
+#pragma unroll
+                for (int e = 0; e < NCH; ++e)
+                    out[t][e] = __fmaf_rn(v[e], w[e][tau], out[t][e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const bool live = t0 + t < n;
+#pragma unroll
+        for (int e = 0; e < NCH; ++e)
+            out[t][e] = live ? silu_f(out[t][e]) : 0.0f;
+    }
+}
+
+// L2 normalisation of 8 token rows whose 128 channels are spread NCH per lane
+// over 128 / NCH consecutive lanes ("ssm_mamba.rs" conv1d_update_l2norm;
+// x / sqrt(sum x^2 + eps) as in "scr_state.hpp").
+template <int NCH>
+__device__ __forceinline__ void l2_rows(float (&v)[8][NCH], float eps, float post)
+{
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        float ss = __fmul_rn(v[t][0], v[t][0]);
+#pragma unroll
+        for (int e = 1; e < NCH; ++e)
+            ss = __fmaf_rn(v[t][e], v[t][e], ss);
+#pragma unroll
+        for (int m = (kD / NCH) / 2; m >= 1; m >>= 1)
+            ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, m));
+        const float inv = __fmul_rn(rsqrtf(__fadd_rn(ss, eps)), post);
+#pragma unroll
+        for (int e = 0; e < NCH; ++e)
+            v[t][e] = __fmul_rn(v[t][e], inv);
+    }
+}
+
+// Store 8 token rows x NCH channels (channels NCH*g .. of the head) as the two
+// fp16 parts of a 128-byte-swizzled K-major tile with `rows` rows.
+template <int NCH>
+__device__ __forceinline__ void store_rows_split(uint8_t *hi, uint8_t *lo, int row0, int rows, int g,
+                                                 const float (&v)[8][NCH])
+{
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        uint32_t h[NCH / 2], l[NCH / 2];
+#pragma unroll
+        for (int e = 0; e < NCH / 2; ++e)
+            split_pair(v[t][2 * e], v[t][2 * e + 1], h[e], l[e]);
+        const uint32_t off = tc::sw128_offset(row0 + t, NCH * g, rows);
+        if constexpr (NCH == 8) {
+            *reinterpret_cast<uint4 *>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4 *>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+        } else {
+            *reinterpret_cast<uint2 *>(hi + off) = make_uint2(h[0], h[1]);
+            *reinterpret_cast<uint2 *>(lo + off) = make_uint2(l[0], l[1]);
+        }
+    }
+}
+
+// One tensor copy of a chunk's rows of a 128-channel head (no arrive: the caller
+// sets the barrier's expected bytes once for all copies of a chunk).
+__device__ __forceinline__ void rows_copy(const CUtensorMap *map, uint32_t dst, uint32_t mbar,
+                                          int ch, int row, int b)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4}], [%5];"
+                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(ch), "r"(row), "r"(b),
+                    "r"(mbar)
+                 : "memory");
+}
+
+// staged rows of one 128-channel head: (63 + W) rows of 128 bf16, padded to 1 KB
+constexpr uint32_t kRawBox = ((kC + kMaxW - 1) * kD * 2 + 1023) / 1024 * 1024;
+
+// ================================================================== pass 1
+namespace p1 {
+constexpr int kThreads = 256;
+constexpr uint32_t RAW = 0;                       // staged K rows
+constexpr uint32_t KT = RAW + kRawBox;            // K tile, two parts [64][128] sw128 (+ slack)
+constexpr uint32_t KT_LO = KT + 16384;
+constexpr uint32_t KT_BYTES = 40960;              // the M = 128 A descriptor reads 8 KB past KT_LO's end
+constexpr uint32_t AM = KT;                       // after G: A of two heads, fp32 [64][64] each
+constexpr int kTS = 68;                           // T row stride (floats)
+constexpr uint32_t TB = KT + KT_BYTES;            // T of two heads, fp32 [64][68]
+constexpr uint32_t GATES = TB + 2 * kC * kTS * 4;
+constexpr uint32_t MBAR = GATES + 8 * sizeof(Gates);
+constexpr uint32_t SLOT = MBAR + 16;
+constexpr uint32_t BYTES = SLOT + 16 + 1024;      // + alignment slack
+static_assert(KT % 1024 == 0 && KT_LO % 1024 == 0, "swizzled tiles on 1 KB boundaries");
+static_assert(2 * kC * kC * 4 <= KT_BYTES, "A of two heads fits in the K tile's space");
+}  // namespace p1
+
+// A[t][s] (fp32, 64 floats per row), float4 chunks XOR-swizzled by the row
+__device__ __forceinline__ int a_idx(int t, int s) { return t * kC + ((((s >> 2) ^ (t & 15))) << 2) + (s & 3); }
+
+template <typename TIn, int WC>
+__global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                PrefillArgs a, int staged)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int r = a.Hv / a.Hq;
+    const int W = WC > 0 ? WC : a.W;
+    const int c0 = c * kC, n = min(kC, a.T - c0);
+    const uint32_t sbase = tc::smem_addr(smem);
+    const uint32_t mb_raw = sbase + p1::MBAR, mb_mma = sbase + p1::MBAR + 8;
+    Gates *gates = reinterpret_cast<Gates *>(smem + p1::GATES);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + p1::SLOT + 4);
+    const uint64_t lim = a.wait_ns;
+
+    if (tid == 0) {
+        tc::mbar_init(mb_raw, 1);
+        tc::mbar_init(mb_mma, 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (staged) {
+            tc::mbar_expect_tx(mb_raw, (uint32_t)(kC + W - 1) * kD * 2);
+            rows_copy(&xmap, sbase + p1::RAW, mb_raw, a.Hq * kD + hk * kD, c0 - (W - 1), b);
+        } else {
+            tc::mbar_arrive(mb_raw);
+        }
+    }
+    if (warp == 0)
+        tc::tmem_alloc(sbase + p1::SLOT, 64);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + p1::SLOT);
+
+    // gates of the group's V heads (warp w: head hk*r + w)
+    if (warp < r)
+        chunk_gates<TIn>(a, b, hk * r + warp, c0, n, 0, gates + warp);
+
+    // K rows: conv + SiLU + L2 (warp = 8-token block, lane = 4 channels) -> K tile
+    bool ok = tc::mbar_wait_ns(mb_raw, 0, lim, abort);
+    if (ok) {
+        float v[8][4];
+        conv_block<TIn, WC, 4>(a, b, c0, n, a.Hq * kD + hk * kD + 4 * lane, 8 * warp,
+                               staged ? reinterpret_cast<const __nv_bfloat16 *>(smem + p1::RAW) : nullptr, v);
+        l2_rows<4>(v, a.l2_eps, kQK);
+        store_rows_split<4>(smem + p1::KT, smem + p1::KT_LO, 8 * warp, kC, lane, v);
+    } else {
+        atomicOr(const_cast<int *>(abort), (int)kErrUT);
+    }
+    tc::fence_smem_to_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    ok = *abort == 0;
+
+    // G = K K^T (rows 64..127 of the A operand read unused data: their results are ignored)
+    const bool mma_issued = ok;
+    if (ok && tid == 0) {
+        const uint32_t id = tc::idesc_f16(128, 64);
+#pragma unroll 1
+        for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t kq = (kk >> 2) * (kC * 128) + (kk & 3) * 32;
+            const uint64_t d1 = tc::sdesc_sw128(sbase + p1::KT + kq);
+            const uint64_t d2 = tc::sdesc_sw128(sbase + p1::KT_LO + kq);
+            tc::mma_f16(tmem, d1, d1, id, kk > 0);
+            tc::mma_f16(tmem, d1, d2, id, 1);
+            tc::mma_f16(tmem, d2, d1, id, 1);
+        }
+        tc::mma_commit(mb_mma);
+    }
+    if (ok && !tc::mbar_wait_ns(mb_mma, 0, lim, abort)) {
+        atomicOr(const_cast<int *>(abort), (int)kErrUT);
+        ok = false;
+    }
+    tc::fence_after_sync();
+    __syncthreads();
+    ok = *abort == 0;
+
+    float *Am = reinterpret_cast<float *>(smem + p1::AM);
+    float *Tb = reinterpret_cast<float *>(smem + p1::TB);
+    const int hsel = warp >> 2;                 // head of the pair this warp serves
+    const bool solver = (warp & 3) < 2;         // warps 0, 1, 4, 5: TMEM lanes 0..63
+    const int trow = 32 * (warp & 1) + lane;    // token row t (A) / column j (T)
+    const uint32_t lane_q = (uint32_t)(32 * (warp & 3)) << 16;
+
+#pragma unroll 1
+    for (int hp = 0; ok && hp < r; hp += 2) {
+        const int hh = hp + hsel;
+        // ---- A[t][s] = beta_t e^{Gam_t - Gam_s} (k_t . k_s), s < t
+        if (solver && hh < r) {
+            const Gates *G = gates + hh;
+            float *A = Am + hsel * kC * kC;
+            const int t = trow;
+            const float gt = G->gh[t], gtl = G->gl[t], bt = G->beta[t];
+#pragma unroll 1
+            for (int s0 = 0; s0 < kC; s0 += 16) {
+                float gv[16];
+                if (s0 <= 32 * (warp & 1) + 31)   // warp-uniform: some row of this warp needs the block
+                    tc::tmem_ld16(tmem + lane_q + s0, gv);
+                else
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        gv[e] = 0.0f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = s0 + 4 * q + e;
+                        o[e] = (s < t && t < n) ? __fmul_rn(__fmul_rn(__fmul_rn(bt, kInvQK2),
+                                                                        exp_diff(gt, gtl, G->gh[s], G->gl[s])),
+                                                            gv[4 * q + e])
+                                                : 0.0f;
+                    }
+                    *reinterpret_cast<float4 *>(A + a_idx(t, s0 + 4 * q)) = make_float4(o[0], o[1], o[2], o[3]);
+                }
+            }
+        }
+        __syncthreads();
+        // ---- T = (I + A)^-1, column j per thread, blocks of 8 rows:
+        //      T[i][j] = [i == j] - sum_{s < i} A[i][s] T[s][j]
+        if (solver && hh < r) {
+            const float *A = Am + hsel * kC * kC;
+            float *Tc = Tb + hsel * kC * p1::kTS;
+            const int j = trow;
+            const int S0 = (32 * (warp & 1)) >> 3;   // T[s][j] = 0 for s < j: earlier blocks are zero
+#pragma unroll 1
+            for (int I = 0; I < 8; ++I) {
+                float acc[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    acc[q] = 0.0f;
+#pragma unroll 1
+                for (int S = S0; S < I; ++S) {
+                    float ts[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        ts[e] = Tc[(8 * S + e) * p1::kTS + j];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int i = 8 * I + q;
+                        const float4 a0 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * S));
+                        const float4 a1 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * S + 4));
+                        acc[q] = __fmaf_rn(a0.x, ts[0], acc[q]);
+                        acc[q] = __fmaf_rn(a0.y, ts[1], acc[q]);
+                        acc[q] = __fmaf_rn(a0.z, ts[2], acc[q]);
+                        acc[q] = __fmaf_rn(a0.w, ts[3], acc[q]);
+                        acc[q] = __fmaf_rn(a1.x, ts[4], acc[q]);
+                        acc[q] = __fmaf_rn(a1.y, ts[5], acc[q]);
+                        acc[q] = __fmaf_rn(a1.z, ts[6], acc[q]);
+                        acc[q] = __fmaf_rn(a1.w, ts[7], acc[q]);
+                    }
+                }
+                float x[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int i = 8 * I + q;
+                    const float4 a0 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * I));
+                    const float4 a1 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * I + 4));
+                    const float ad[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    float s = acc[q];
+#pragma unroll
+                    for (int e = 0; e < q; ++e)
+                        s = __fmaf_rn(ad[e], x[e], s);
+                    x[q] = __fsub_rn(i == j ? 1.0f : 0.0f, s);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    Tc[(8 * I + q) * p1::kTS + j] = x[q];
+            }
+        }
+        __syncthreads();
+        // ---- T -> two-part fp16 K-major image ([t][s], 8x8 core matrices) in the workspace
+#pragma unroll 1
+        for (int u = 0; u < 2; ++u) {
+            const int hh2 = hp + u;
+            if (hh2 >= r)
+                break;
+            const float *Tc = Tb + u * kC * p1::kTS;
+            uint8_t *img = a.ws + (((size_t)b * a.Hv + hk * r + hh2) * a.n_chunks + c) * kPrefillChunkImage;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int p = tid + 256 * k;                       // 16-byte chunk of a part
+                const int t = ((p >> 6) << 3) | (p & 7), s8 = (p >> 3) & 7;
+                const float4 f0 = *reinterpret_cast<const float4 *>(Tc + t * p1::kTS + 8 * s8);
+                const float4 f1 = *reinterpret_cast<const float4 *>(Tc + t * p1::kTS + 8 * s8 + 4);
+                uint4 hi, lo;
+                split_pair(f0.x, f0.y, hi.x, lo.x);
+                split_pair(f0.z, f0.w, hi.y, lo.y);
+                split_pair(f1.x, f1.y, hi.z, lo.z);
+                split_pair(f1.z, f1.w, hi.w, lo.w);
+                *reinterpret_cast<uint4 *>(img + 16 * p) = hi;
+                *reinterpret_cast<uint4 *>(img + 8192 + 16 * p) = lo;
+            }
+        }
+        __syncthreads();
+    }
+
+    if (tid == 0 && *abort) {
+        atomicOr(&g_device_error, *abort);
+        // the staged-row copy and the product may still be in flight
+        if (!tc::mbar_wait_ns(mb_raw, 0, lim) || (mma_issued && !tc::mbar_wait_ns(mb_mma, 0, lim)))
+            atomicOr(&g_device_error, (int)kErrDrain);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0)
+        tc::tmem_dealloc(tmem, 64);
+}
+
+// ================================================================== pass 2
+namespace p2 {
+constexpr int kThreads = 512;                     // 8 epilogue warps (warp 0 also issues), 8 conv warps
+constexpr uint32_t QK_HI = 0, QK_LO = 32768;      // [Q; K] two parts, [128 t'][128 i] sw128
+constexpr uint32_t VF = 65536;                    // V^T fp32 footprint [128 j][64 t]
+constexpr uint32_t TT = 98304;                    // T image of the current chunk (16 KB)
+constexpr uint32_t PP = 114688;                   // P two parts, [64 t][64 s] K-major
+constexpr uint32_t OS = 131072;                   // O staging, fp32 [64 t][128 j]
+constexpr uint32_t RAW = 163840;                  // staged rows: Q, K, V heads
+constexpr uint32_t GATES = RAW + 3 * kRawBox;     // two Gates buffers
+constexpr uint32_t MBAR = GATES + 2 * sizeof(Gates);
+constexpr uint32_t SLOT = MBAR + 16 * 8;          // TMEM base, abort word
+constexpr uint32_t BYTES = SLOT + 16 + 1024;
+static_assert(BYTES <= 232448, "shared memory budget");
+static_assert(RAW % 1024 == 0 && kRawBox % 1024 == 0, "staged rows on 1 KB boundaries");
+// barriers
+enum { B_RAW, B_T, B_M1, B_M2, B_M3, B_QK, B_P, B_ST, B_X, B_U, B_V, B_RAWFREE, B_OS, B_N };
+// TMEM columns
+constexpr uint32_t TS = 0, D1 = 128, R1 = 256, GG = 384, D2 = 448;
+}  // namespace p2
+
+// fp32 V^T footprint: float4 q (tokens 4q .. 4q+3) of value row j; the 16-byte
+// slot is XOR-ed with the row group so that both the conv's stores (rows 4
+// apart) and a warp's row reads land on distinct bank groups.
+__device__ __forceinline__ uint32_t foot_off(int j, int q)
+{
+    return (uint32_t)(p2::VF + (q >= 8 ? 16384 : 0) + (j >> 3) * 1024 + (q & 7) * 128 +
+                      (((j & 7) ^ ((j >> 3) & 7)) << 4));
+}
+
+__device__ __forceinline__ void pack_split16(const float (&v)[16], uint32_t (&hi)[8], uint32_t (&lo)[8])
+{
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        split_pair(v[2 * e], v[2 * e + 1], hi[e], lo[e]);
+}
+
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                    "r"(v[6]), "r"(v[7]));
+}
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
+template <typename TIn, int WC>
+__global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                      PrefillArgs a, int staged, int zvec)
+{
+    using namespace p2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int r = a.Hv / a.Hq, hk = h / r;
+    const int W = WC > 0 ? WC : a.W;
+    const int nch = a.n_chunks;
+    const uint32_t sbase = tc::smem_addr(smem);
+    const uint32_t mb = sbase + MBAR;
+    auto bar = [&](int i) { return mb + 8u * (uint32_t)i; };
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + SLOT + 4);
+    Gates *gbuf = reinterpret_cast<Gates *>(smem + GATES);
+    const uint64_t lim = a.wait_ns;
+
+    if (tid == 0) {
+        const uint32_t counts[B_N] = {1, 1, 1, 1, 1, 256, 128, 256, 256, 256, 256, 256, 256};
+        for (int i = 0; i < B_N; ++i)
+            tc::mbar_init(bar(i), counts[i]);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0)
+        tc::tmem_alloc(sbase + SLOT, 512);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SLOT);
+
+    // a bounded wait that, on giving up, tells the other roles to stop
+    auto waitb = [&](int i, uint32_t parity, uint64_t limit) -> bool {
+        if (tc::mbar_wait_ns(bar(i), parity, limit, abort))
+            return true;
+        atomicOr(const_cast<int *>(abort), (int)kErrChain);
+        return false;
+    };
+
+    if (warp >= 8) {
+        // ============================================ conv warps: chunk c+1's rows, chunk c's P
+        const int cw = warp - 8;
+        const __nv_bfloat16 *raw = staged ? reinterpret_cast<const __nv_bfloat16 *>(smem + RAW) : nullptr;
+        // Q / K rows: 8 tokens x 8 channels per thread (warps 0-3 of the group: Q, 4-7: K)
+        const int qk_part = cw >> 2, qk_tb = 2 * (cw & 3) + (lane >> 4), qk_g = lane & 15;
+        const int qk_ch = (qk_part ? a.Hq * kD : 0) + hk * kD + 8 * qk_g;
+        const __nv_bfloat16 *qk_raw = raw != nullptr ? raw + qk_part * (kRawBox / 2) : nullptr;
+        // V rows: 8 tokens x 4 channels per thread
+        const int v_ch = 2 * a.Hq * kD + h * kD + 4 * lane;
+        const __nv_bfloat16 *v_raw = raw != nullptr ? raw + 2 * (kRawBox / 2) : nullptr;
+        const bool pwarp = (warp & 3) < 2;      // warps 8, 9, 12, 13: TMEM lanes 0..63 (rows t of G)
+        const int pt = 32 * (warp & 1) + lane;  // P row t
+        const int psh = (warp >> 2) & 1;        // P columns s in [32 psh, 32 psh + 32)
+
+        auto v_conv = [&](int c0, int n) {
+            float v[8][4];
+            conv_block<TIn, WC, 4>(a, b, c0, n, v_ch, 8 * cw, v_raw, v);
+            return [=](uint8_t *sm) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 4 * lane + e;
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        *reinterpret_cast<float4 *>(sm + foot_off(j, 2 * cw + q)) =
+                            make_float4(v[4 * q][e], v[4 * q + 1][e], v[4 * q + 2][e], v[4 * q + 3][e]);
+                }
+            };
+        };
+
+        // prologue: chunk 0
+        bool ok = waitb(B_RAW, 0, lim);
+        if (ok) {
+            const int n0 = min(kC, a.T);
+            if (warp == 15)
+                chunk_gates<TIn>(a, b, h, 0, n0, 0, gbuf);
+            v_conv(0, n0)(smem);
+            float v[8][8];
+            conv_block<TIn, WC, 8>(a, b, 0, n0, qk_ch, 8 * qk_tb, qk_raw, v);
+            l2_rows<8>(v, a.l2_eps, kQK);
+            store_rows_split<8>(smem + QK_HI, smem + QK_LO, qk_part * kC + 8 * qk_tb, 2 * kC, qk_g, v);
+        }
+        tc::mbar_arrive(bar(B_RAWFREE));
+        tc::fence_smem_to_async();
+        tc::mbar_arrive(bar(B_QK));
+        tc::mbar_arrive(bar(B_V));
+#pragma unroll 1
+        for (int c = 0; ok && c < nch; ++c) {
+            const uint32_t par = c & 1;
+            const int c0 = c * kC, n = min(kC, a.T - c0);
+            ok = waitb(B_M1, par, lim) && waitb(B_QK, par, lim);
+            if (!ok)
+                break;
+            tc::fence_after_sync();
+            // ---- P[t][s] = e^{Gam_t - Gam_s} (q_t . k_s) for s <= t (t < n), two parts
+            if (pwarp) {
+                const Gates *G = gbuf + (c & 1);
+                const int t = pt;
+                float o[32];
+                if (psh <= (warp & 1)) {          // warp-uniform: the block holds some s <= t
+                    float gv[32];
+                    tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + GG + 32 * psh, gv);
+                    const float gt = G->gh[t], gtl = G->gl[t];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int s = 32 * psh + e;
+                        o[e] = (s <= t && t < n) ? __fmul_rn(__fmul_rn(exp_diff(gt, gtl, G->gh[s], G->gl[s]), kInvQK2),
+                                                             gv[e])
+                                                 : 0.0f;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = 0.0f;
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 hi, lo;
+                    split_pair(o[8 * q], o[8 * q + 1], hi.x, lo.x);
+                    split_pair(o[8 * q + 2], o[8 * q + 3], hi.y, lo.y);
+                    split_pair(o[8 * q + 4], o[8 * q + 5], hi.z, lo.z);
+                    split_pair(o[8 * q + 6], o[8 * q + 7], hi.w, lo.w);
+                    const uint32_t off = tc::km_offset(t, 32 * psh + 8 * q, kC);
+                    *reinterpret_cast<uint4 *>(smem + PP + off) = hi;
+                    *reinterpret_cast<uint4 *>(smem + PP + 8192 + off) = lo;
+                }
+                tc::fence_smem_to_async();
+                tc::fence_before_sync();
+                tc::mbar_arrive(bar(B_P));
+            }
+            if (c + 1 >= nch)
+                break;
+            // ---- chunk c+1: gates, V rows (once chunk c's X has read V), Q rows, K rows
+            const int c1 = c0 + kC, n1 = min(kC, a.T - c1);
+            ok = waitb(B_RAW, (c + 1) & 1, lim);
+            if (!ok)
+                break;
+            if (warp == 15) {
+                __syncwarp();   // lane 0 wrote the previous chunk's rho_next
+                chunk_gates<TIn>(a, b, h, c1, n1, gbuf[c & 1].rho_next, gbuf + ((c + 1) & 1));
+            }
+            auto write_v = v_conv(c1, n1);
+            ok = waitb(B_X, par, lim);
+            if (!ok)
+                break;
+            write_v(smem);
+            tc::mbar_arrive(bar(B_V));
+            float v[8][8];
+            conv_block<TIn, WC, 8>(a, b, c1, n1, qk_ch, 8 * qk_tb, qk_raw, v);
+            l2_rows<8>(v, a.l2_eps, kQK);
+            tc::mbar_arrive(bar(B_RAWFREE));
+            if (qk_part == 1) {
+                ok = waitb(B_M3, par, lim);                 // K rows free: this chunk's S update done
+                if (!ok)
+                    break;
+            }
+            store_rows_split<8>(smem + QK_HI, smem + QK_LO, qk_part * kC + 8 * qk_tb, 2 * kC, qk_g, v);
+            tc::fence_smem_to_async();
+            tc::mbar_arrive(bar(B_QK));
+        }
+    } else {
+        // ============================================ epilogue warps: value row j
+        // Lane 0 of warp 0 also issues every copy and tensor-core product, at the
+        // points of its own program where their inputs are ready.
+        const bool issuer = tid == 0;
+        int raw_last = -1, t_last = -1, last_commit = -1;
+        uint32_t last_phase = 0;
+        const uint32_t raw_bytes = 3u * (uint32_t)(kC + W - 1) * kD * 2;
+        auto issue_raw = [&](int cc) {
+            if (staged) {
+                tc::mbar_expect_tx(bar(B_RAW), raw_bytes);
+                const int row = cc * kC - (W - 1);
+                rows_copy(&xmap, sbase + RAW, bar(B_RAW), hk * kD, row, b);
+                rows_copy(&xmap, sbase + RAW + kRawBox, bar(B_RAW), a.Hq * kD + hk * kD, row, b);
+                rows_copy(&xmap, sbase + RAW + 2 * kRawBox, bar(B_RAW), 2 * a.Hq * kD + h * kD, row, b);
+            } else {
+                tc::mbar_arrive(bar(B_RAW));
+            }
+            raw_last = cc;
+        };
+        auto issue_t = [&](int cc) {
+            const uint8_t *src = a.ws + (((size_t)b * a.Hv + h) * nch + cc) * kPrefillChunkImage;
+            tc::mbar_expect_tx(bar(B_T), (uint32_t)kPrefillChunkImage);
+            tc::bulk_copy_g2s(sbase + TT, src, (uint32_t)kPrefillChunkImage, bar(B_T));
+            t_last = cc;
+        };
+        const uint32_t idG = tc::idesc_f16(128, 64), id128 = tc::idesc_f16(128, 128);
+        // G = [Q; K] K^T and D1 = S_0^T [Q; K]^T, once the [Q; K] tile and S_0^T are ready
+        auto issue_m1 = [&](int c) -> bool {
+            const uint32_t par = c & 1;
+            // the first wait of the kernel takes its limit from first_wait_ns (a test hook)
+            if (!waitb(B_RAWFREE, par, c == 0 ? a.first_wait_ns : lim))
+                return false;
+            if (c + 1 < nch)     // the staged rows are free since chunk c's conv: fetch chunk c+1's
+                issue_raw(c + 1);
+            if (!waitb(B_QK, par, lim) || !waitb(B_ST, par, lim))
+                return false;
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint32_t kq = (kk >> 2) * (2 * kC * 128) + (kk & 3) * 32;
+                const uint64_t a1 = tc::sdesc_sw128(sbase + QK_HI + kq);
+                const uint64_t a2 = tc::sdesc_sw128(sbase + QK_LO + kq);
+                const uint64_t b1 = tc::sdesc_sw128(sbase + QK_HI + kC * 128 + kq);
+                const uint64_t b2 = tc::sdesc_sw128(sbase + QK_LO + kC * 128 + kq);
+                tc::mma_f16(tmem + GG, a1, b1, idG, kk > 0);
+                tc::mma_f16(tmem + GG, a1, b2, idG, 1);
+                tc::mma_f16(tmem + GG, a2, b1, idG, 1);
+                const uint32_t shi = tmem + R1 + 8 * kk, slo = tmem + R1 + 64 + 8 * kk;
+                tc::mma_f16_ta(tmem + D1, shi, a1, id128, kk > 0);
+                tc::mma_f16_ta(tmem + D1, shi, a2, id128, 1);
+                tc::mma_f16_ta(tmem + D1, slo, a1, id128, 1);
+            }
+            tc::mma_commit(bar(B_M1));
+            last_commit = B_M1;
+            last_phase = par;
+            return true;
+        };
+        // D2 = X^T T^T, once every value row's X^T is in TMEM and T has arrived
+        auto issue_m2 = [&](int c) -> bool {
+            const uint32_t par = c & 1;
+            if (!waitb(B_X, par, lim) || !waitb(B_T, par, lim))
+                return false;
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int kk = 0; kk < kC / 16; ++kk) {
+                const uint64_t b1 = tc::sdesc(sbase + TT + kk * 256, 128, 1024);
+                const uint64_t b2 = tc::sdesc(sbase + TT + 8192 + kk * 256, 128, 1024);
+                const uint32_t xhi = tmem + R1 + 8 * kk, xlo = tmem + R1 + 32 + 8 * kk;
+                tc::mma_f16_ta(tmem + D2, xhi, b1, idG, kk > 0);
+                tc::mma_f16_ta(tmem + D2, xhi, b2, idG, 1);
+                tc::mma_f16_ta(tmem + D2, xlo, b1, idG, 1);
+            }
+            tc::mma_commit(bar(B_M2));
+            last_commit = B_M2;
+            last_phase = par;
+            return true;
+        };
+        // S^T += U'^T K (K rows read MN-major), (P U)^T = U^T P^T into D2 (U^T has been
+        // read from it); T of the next chunk
+        auto issue_m3 = [&](int c) -> bool {
+            const uint32_t par = c & 1;
+            if (c + 1 < nch)     // D2 has been read (this warp waited for it): T's buffer is free
+                issue_t(c + 1);
+            if (!waitb(B_U, par, lim) || !waitb(B_P, par, lim))
+                return false;
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int kk = 0; kk < kC / 16; ++kk) {
+                const uint32_t koff = kC * 128 + kk * 2048;    // K rows 16kk.. : 8-row groups 1 KB apart
+                const uint64_t k1 = tc::sdesc_sw128_mn(sbase + QK_HI + koff, 2 * kC * 128, 1024);
+                const uint64_t k2 = tc::sdesc_sw128_mn(sbase + QK_LO + koff, 2 * kC * 128, 1024);
+                const uint32_t uphi = tmem + R1 + 64 + 8 * kk, uplo = tmem + R1 + 96 + 8 * kk;
+                tc::mma_f16_ta(tmem + TS, uphi, k1, id128 | tc::kIdescTransB, 1);
+                tc::mma_f16_ta(tmem + TS, uphi, k2, id128 | tc::kIdescTransB, 1);
+                tc::mma_f16_ta(tmem + TS, uplo, k1, id128 | tc::kIdescTransB, 1);
+                const uint64_t p1d = tc::sdesc(sbase + PP + kk * 256, 128, 1024);
+                const uint64_t p2d = tc::sdesc(sbase + PP + 8192 + kk * 256, 128, 1024);
+                const uint32_t uhi = tmem + R1 + 8 * kk, ulo = tmem + R1 + 32 + 8 * kk;
+                tc::mma_f16_ta(tmem + D2, uhi, p1d, idG, kk > 0);
+                tc::mma_f16_ta(tmem + D2, uhi, p2d, idG, 1);
+                tc::mma_f16_ta(tmem + D2, ulo, p1d, idG, 1);
+            }
+            tc::mma_commit(bar(B_M3));
+            last_commit = B_M3;
+            last_phase = par;
+            return true;
+        };
+        if (issuer) {
+            issue_raw(0);
+            issue_t(0);
+        }
+        const int q4 = warp & 3, hf = warp >> 2;
+        const int j = 32 * q4 + lane;
+        const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+        float *state_row = a.state + (((size_t)b * a.Hv + h) * kD + j) * kD + 64 * hf;
+        float *Os = reinterpret_cast<float *>(smem + OS);
+        // prologue: entering state -> fp32 master (TS) and the S_0^T operand (R1)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float v16[16];
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const float4 f = __ldg(reinterpret_cast<const float4 *>(state_row + 16 * k + e));
+                v16[e] = f.x; v16[e + 1] = f.y; v16[e + 2] = f.z; v16[e + 3] = f.w;
+            }
+            tc::tmem_st16(tl + TS + 64 * hf + 16 * k, v16);
+            uint32_t hi[8], lo[8];
+            pack_split16(v16, hi, lo);
+            tmem_st8u(tl + R1 + 32 * hf + 8 * k, hi);
+            tmem_st8u(tl + R1 + 64 + 32 * hf + 8 * k, lo);
+        }
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar(B_ST));
+        // gated-norm mapping: warp w handles tokens w, w + 8, ...; lane holds channels 4 lane .. +3
+        const float4 nw4 = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane);
+        bool ok = true;
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+            const uint32_t par = c & 1;
+            const int c0 = c * kC, n = min(kC, a.T - c0);
+            if (warp == 0) {
+                if (issuer)
+                    ok = issue_m1(c);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok)
+                    break;
+            }
+            ok = waitb(B_M1, par, lim) && waitb(B_V, par, lim);
+            if (!ok)
+                break;
+            tc::fence_after_sync();
+            const Gates *G = gbuf + (c & 1);
+            // ---- X^T[j][t] = beta_t V[t][j] - beta_t e^{Gam_t} (K S_0)[t][j]; the state master
+            //      scaled by e^{Gam_C} ahead of this chunk's update
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const int tb0 = 32 * hf + 16 * p;
+                float ks[16];
+                tc::tmem_ld16(tl + D1 + kC + tb0, ks);
+                float x[16];
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const float4 f = *reinterpret_cast<const float4 *>(smem + foot_off(j, tb0 / 4 + qq));
+                    const float4 bt = ld4(G->beta + tb0 + 4 * qq), bg = ld4(G->bg + tb0 + 4 * qq);
+                    x[4 * qq + 0] = __fsub_rn(__fmul_rn(bt.x, f.x), __fmul_rn(bg.x, ks[4 * qq + 0]));
+                    x[4 * qq + 1] = __fsub_rn(__fmul_rn(bt.y, f.y), __fmul_rn(bg.y, ks[4 * qq + 1]));
+                    x[4 * qq + 2] = __fsub_rn(__fmul_rn(bt.z, f.z), __fmul_rn(bg.z, ks[4 * qq + 2]));
+                    x[4 * qq + 3] = __fsub_rn(__fmul_rn(bt.w, f.w), __fmul_rn(bg.w, ks[4 * qq + 3]));
+                }
+                uint32_t hi[8], lo[8];
+                pack_split16(x, hi, lo);
+                tmem_st8u(tl + R1 + tb0 / 2, hi);
+                tmem_st8u(tl + R1 + 32 + tb0 / 2, lo);
+            }
+            {
+                const float ec = G->ec;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float sv[16];
+                    tc::tmem_ld16(tl + TS + 64 * hf + 16 * k, sv);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        sv[e] = __fmul_rn(sv[e], ec);
+                    tc::tmem_st16(tl + TS + 64 * hf + 16 * k, sv);
+                }
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            tc::mbar_arrive(bar(B_X));
+            if (warp == 0) {
+                if (issuer)
+                    ok = issue_m2(c);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok)
+                    break;
+            }
+            // ---- U = T X (from D2): U^T for the output product, U'^T = U^T diag(e^{Gam_C - Gam})
+            ok = waitb(B_M2, par, lim);
+            if (!ok)
+                break;
+            tc::fence_after_sync();
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const int tb0 = 32 * hf + 16 * p;
+                float u[16];
+                tc::tmem_ld16(tl + D2 + tb0, u);
+                uint32_t hi[8], lo[8];
+                pack_split16(u, hi, lo);
+                tmem_st8u(tl + R1 + tb0 / 2, hi);
+                tmem_st8u(tl + R1 + 32 + tb0 / 2, lo);
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const float4 g4 = ld4(G->egc + tb0 + 4 * qq);
+                    u[4 * qq + 0] = __fmul_rn(u[4 * qq + 0], g4.x);
+                    u[4 * qq + 1] = __fmul_rn(u[4 * qq + 1], g4.y);
+                    u[4 * qq + 2] = __fmul_rn(u[4 * qq + 2], g4.z);
+                    u[4 * qq + 3] = __fmul_rn(u[4 * qq + 3], g4.w);
+                }
+                pack_split16(u, hi, lo);
+                tmem_st8u(tl + R1 + 64 + tb0 / 2, hi);
+                tmem_st8u(tl + R1 + 96 + tb0 / 2, lo);
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            tc::mbar_arrive(bar(B_U));
+            if (warp == 0) {
+                if (issuer)
+                    ok = issue_m3(c);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok)
+                    break;
+            }
+            ok = waitb(B_M3, par, lim);
+            if (!ok)
+                break;
+            tc::fence_after_sync();
+            // ---- O^T row j = e^{Gam} (Q S_0)^T + (P U)^T -> token-major staging, scaled by 1/sqrt(d)
+            //      (the two terms are added here, rounded, rather than in the accumulator: for a
+            //      token whose readout nearly cancels this is the sum that decides its precision)
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const int tb0 = 32 * hf + 16 * p;
+                float qs[16], pu[16];
+                tc::tmem_ld16(tl + D1 + tb0, qs);
+                tc::tmem_ld16(tl + D2 + tb0, pu);
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const float4 eg = ld4(G->eg + tb0 + 4 * qq);
+                    const float egv[4] = {eg.x, eg.y, eg.z, eg.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = 4 * qq + e;
+                        Os[(tb0 + k) * kD + j] = __fmul_rn(__fmaf_rn(qs[k], egv[e], pu[k]), a.scale);
+                    }
+                }
+            }
+            if (c + 1 < nch) {
+                // ---- next chunk's S_0^T operand from the updated state master
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float sv[16];
+                    tc::tmem_ld16(tl + TS + 64 * hf + 16 * k, sv);
+                    uint32_t hi[8], lo[8];
+                    pack_split16(sv, hi, lo);
+                    tmem_st8u(tl + R1 + 32 * hf + 8 * k, hi);
+                    tmem_st8u(tl + R1 + 64 + 32 * hf + 8 * k, lo);
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                tc::mbar_arrive(bar(B_ST));
+            } else {
+                // ---- final state back to HBM (S^T rows = the library layout), unscaled
+                const float us = exp2i(-G->rho_next);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float sv[16];
+                    tc::tmem_ld16(tl + TS + 64 * hf + 16 * k, sv);
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4 *>(state_row + 16 * k + e) =
+                            make_float4(__fmul_rn(sv[e], us), __fmul_rn(sv[e + 1], us),
+                                        __fmul_rn(sv[e + 2], us), __fmul_rn(sv[e + 3], us));
+                }
+            }
+            tc::mbar_arrive(bar(B_OS));
+            ok = waitb(B_OS, par, lim);
+            if (!ok)
+                break;
+            // ---- gated RMSNorm ("fm_kernel_ssm.h", "Gated RMSNorm"): warp per token row
+#pragma unroll 1
+            for (int t = warp; t < n; t += 8) {
+                const float4 y = *reinterpret_cast<const float4 *>(Os + t * kD + 4 * lane);
+                float ss = __fmul_rn(y.x, y.x);
+                ss = __fmaf_rn(y.y, y.y, ss);
+                ss = __fmaf_rn(y.z, y.z, ss);
+                ss = __fmaf_rn(y.w, y.w, ss);
+                ss = warp_sum32(ss);
+                const float inv = rsqrtf(__fadd_rn(__fmul_rn(ss, 1.0f / kD), a.rms_eps));
+                const int64_t row = (int64_t)b * a.T + c0 + t;
+                const TIn *zr = static_cast<const TIn *>(a.z) + row * a.z_stride + (int64_t)h * kD + 4 * lane;
+                float zv[4];
+                if (zvec) {
+                    load_row<4, TIn>(zr, zv);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        zv[e] = load_act<TIn>(zr + e);
+                }
+                float4 o;
+                o.x = gated_out(y.x, inv, nw4.x, zv[0]);
+                o.y = gated_out(y.y, inv, nw4.y, zv[1]);
+                o.z = gated_out(y.z, inv, nw4.z, zv[2]);
+                o.w = gated_out(y.w, inv, nw4.w, zv[3]);
+                *reinterpret_cast<float4 *>(a.out + (row * a.Hv + h) * kD + 4 * lane) = o;
+            }
+        }
+        if (issuer) {
+            // drain: copies and products in flight finish before the CTA releases TMEM
+            bool drained = true;
+            if (last_commit >= 0)   // a commit tracks every product issued before it
+                drained &= tc::mbar_wait_ns(bar(last_commit), last_phase, lim);
+            if (raw_last >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_RAW), raw_last & 1, lim);
+            if (t_last >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_T), t_last & 1, lim);
+            if (!drained)
+                atomicOr(&g_device_error, (int)kErrDrain);
+        }
+        __syncwarp();
+    }
+
+    // ---- teardown
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0 && *abort)
+        atomicOr(&g_device_error, *abort);
+    if (warp == 0)
+        tc::tmem_dealloc(tmem, 512);
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(256) prefill_history_kernel(float *conv_state, const TIn *x,
+                                                              int64_t x_stride, int conv_dim, int W,
+                                                              int T)
+{
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    const int b = blockIdx.y;
+    if (c >= conv_dim)
+        return;
+    float *hist_c = conv_state + ((size_t)b * conv_dim + c) * (W - 1);
+    float nh[kMaxW - 1];
+    conv_history_after<TIn>(hist_c, x + (int64_t)b * T * x_stride + c, x_stride, W, T, nh);
+    store_history(hist_c, W, nh);
+}
+
+template <typename TIn, int WC>
+cudaError_t prefill_typed(const PrefillArgs &a, const CUtensorMap &map, int staged, cudaStream_t s)
+{
+    auto k1 = prefill_ut_kernel<TIn, WC>;
+    auto k2 = prefill_chain_kernel<TIn, WC>;
+    static const cudaError_t attr = [&] {
+        cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p1::BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p2::BYTES);
+        return e;
+    }();
+    if (attr != cudaSuccess)
+        return attr;
+    k1<<<dim3(a.n_chunks, a.Hq, a.B), p1::kThreads, p1::BYTES, s>>>(map, a, staged);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    // the gated norm reads 4 z values per lane with one vector load when rows allow it
+    const size_t es = sizeof(TIn);
+    const int zvec = (reinterpret_cast<uintptr_t>(a.z) % (4 * es) == 0 && (a.z_stride * es) % (4 * es) == 0) ? 1 : 0;
+    k2<<<dim3(a.Hv, a.B, 1), p2::kThreads, p2::BYTES, s>>>(map, a, staged, zvec);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    prefill_history_kernel<TIn><<<dim3((a.conv_dim + 255) / 256, a.B, 1), 256, 0, s>>>(
+        a.conv_state, static_cast<const TIn *>(a.x), a.x_stride, a.conv_dim, a.W, a.T);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t take_prefill_device_error(int *code)
+{
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int));
+    if (e == cudaSuccess && v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    }
+    *code = v;
+    return e;
+}
+
+cudaError_t launch_prefill(const PrefillArgs &a, bool bf16, cudaStream_t s)
+{
+    CUtensorMap map;
+    memset(&map, 0, sizeof map);
+    // chunk rows of one 128-channel head, (63 + W) rows from token c0 - (W - 1); bf16 rows only
+    const int staged = bf16 && encode_rows_map(&map, a.x, true, a.conv_dim, a.x_stride, a.T, a.B, kD,
+                                               (uint32_t)(kC + a.W - 1))
+                           ? 1 : 0;
+    if (bf16)
+        return a.W == 4 ? prefill_typed<__nv_bfloat16, 4>(a, map, staged, s)
+                        : prefill_typed<__nv_bfloat16, 0>(a, map, staged, s);
+    return a.W == 4 ? prefill_typed<float, 4>(a, map, staged, s) : prefill_typed<float, 0>(a, map, staged, s);
+}
+
+}  // namespace gdn

@@ -64,18 +64,49 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr)
     return d;
 }
 
-// Instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator,
-// both operands K-major, dense: D format bits 4-5 = 1 (f32), A format bits
-// 7-9 = 1 (bf16), B format bits 10-12 = 1 (bf16), N >> 3 at bits 17-22,
+// Instruction descriptor, kind::f16 with fp16 A and B, fp32 accumulator, both
+// operands K-major unless kIdescTransB is or-ed in, dense: D format bits 4-5 =
+// 1 (f32), A and B formats bits 7-9 and 10-12 = 0 (f16), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+// Instruction-descriptor bit that reads B as MN-major (N contiguous) instead of
+// K-major. With 128-byte swizzle, an MN-major B of 16-bit elements is made of
+// atoms of 8 K-rows x 64 N-elements (128 bytes each); the descriptor's leading
+// byte offset is then the distance between atoms along N and its stride byte
+// offset the distance between 8-row groups along K.
+constexpr uint32_t kIdescTransB = 1u << 16;
+
+// Descriptor of a 128-byte-swizzled tile at saddr (1024-byte aligned atoms) with
+// explicit leading / stride byte offsets (the MN-major form above).
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread. A lives in tensor
+// memory: row m of A in TMEM lane m, 16-bit elements packed two per 32-bit
+// column (element 2c in the low half of column c), so a K = 16 slice of A is
+// 8 consecutive columns.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T (kind::f16: both operands fp16 or both bf16,
+// as the instruction descriptor says), issued by one thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate)
 {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -95,19 +126,69 @@ __device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(mbar), "r"(count));
 }
 
-// Wait for the phase with the given parity to complete, giving up after
-// `limit` polls. Returns true when the phase completed.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, int limit)
+// Nanoseconds of the global timer.
+__device__ __forceinline__ uint64_t global_ns()
 {
-    uint32_t done = 0;
-    for (int it = 0; it < limit; ++it) {
-        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                     "selp.u32 %0, 1, 0, p;\n\t}"
-                     : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
-        if (done)
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// One test of the phase; while it is incomplete the thread may sleep in the
+// instruction for up to suspend_ns (it wakes as soon as the phase completes),
+// so a waiting warp issues a handful of instructions per wait, not a spin.
+__device__ __forceinline__ bool mbar_try(uint32_t mbar, uint32_t parity, uint32_t suspend_ns)
+{
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(mbar), "r"(parity), "r"(suspend_ns) : "memory");
+    return done != 0;
+}
+
+// Wait for the phase with the given parity, giving up once `limit_ns` of the
+// global timer have passed, or as soon as *abort is non-zero (when abort is
+// given). A limit under 1 us (below the timer's resolution) gives up at once,
+// without testing the phase: a test hook uses it to force the give-up path.
+// Returns true when the phase completed.
+__device__ __forceinline__ bool mbar_wait_ns(uint32_t mbar, uint32_t parity, uint64_t limit_ns,
+                                             const volatile int *abort = nullptr)
+{
+    if (limit_ns < 1000)
+        return false;
+    if (mbar_try(mbar, parity, 0))
+        return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (abort != nullptr && *abort != 0)
+            return false;
+        const uint64_t el = global_ns() - t0;
+        if (el > limit_ns)
+            return false;
+        const uint64_t rem = limit_ns - el;
+        if (mbar_try(mbar, parity, rem < 20000 ? (uint32_t)rem : 20000u))
             return true;
     }
-    return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(mbar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(mbar), "r"(bytes) : "memory");
+}
+
+// One contiguous global -> shared copy of `bytes` (16-byte aligned, a multiple
+// of 16), completing on mbar (whose expected transaction count the caller set).
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t mbar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
 }
 
 // TMEM allocation: executed by one whole warp; the base address lands in *slot.
@@ -152,6 +233,41 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 #pragma unroll
     for (int i = 0; i < 16; ++i)
         v[i] = __uint_as_float(r[i]);
+}
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+                   "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+                   "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive 32-bit TMEM columns of raw bits (packed 16-bit operand pairs).
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]),
+                    "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]),
+                    "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]));
+}
+
+__device__ __forceinline__ void tmem_wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])

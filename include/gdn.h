@@ -308,6 +308,14 @@ gdn_status gdn_verify_commit_kn(float *state, float *conv_state, const float *st
                                 const gdn_dims *dims, int32_t n_draft, gdn_stream_t stream);
 
 /*
+ * Workspace bytes gdn_prefill_chunked needs for these dims and n_tokens:
+ * one 16 KB image per (sequence, V head, 64-token chunk), i.e.
+ * n_seq * n_v_heads * ceil(n_tokens / 64) * 16384. Returns 0 for invalid
+ * dims, n_tokens < 1 or chunk != 64.
+ */
+size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t n_tokens, int32_t chunk);
+
+/*
  * Chunked prefill over n_tokens tokens of every sequence: the same function
  * as n_tokens gdn_decode_step calls, evaluated chunk by chunk
  * ("fm_kernel_ssm.h", "Delta-rule recurrence": the sequential scan is the
@@ -317,26 +325,41 @@ gdn_status gdn_verify_commit_kn(float *state, float *conv_state, const float *st
  *   state, conv_state updated in place (state after the last token);
  *   x, z, alpha, beta_logit as in LAYOUTS with T = n_tokens;
  *   out float [B][n_tokens][Hv][d].
- * chunk must be 64. x and params->conv_w must be 16-byte aligned, with x rows
- * a multiple of 16 bytes apart (x_stride * element size). Agrees with the sequential scan within
- * float32 rounding, not bit for bit.
- * Errors: INVALID_ARG (null, n_tokens < 1, bad dims, x alignment), UNSUPPORTED
- * (d, W, chunk != 64).
+ *   workspace  caller-owned device scratch of at least
+ *              gdn_prefill_workspace_bytes(dims, n_tokens, chunk) bytes,
+ *              16-byte aligned; its contents on entry do not matter and are
+ *              meaningless on return. Calls that overlap on the GPU need
+ *              separate workspaces.
+ * Runs as three launches on `stream`: every chunk's (I + A)^-1 transform in
+ * parallel into the workspace, the sequential pass over the chunks of each
+ * (sequence, V head), and the conv-history update.
+ * chunk must be 64. x, params->conv_w and out must be 16-byte aligned, with x
+ * rows a multiple of 16 bytes apart (x_stride * element size). Agrees with the
+ * sequential scan within float32 rounding, not bit for bit.
+ * Errors: INVALID_ARG (null, n_tokens < 1, bad dims, alignment, workspace too
+ * small), UNSUPPORTED (d, W, chunk != 64).
  */
 gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, const void *z,
                                const void *alpha, const void *beta_logit, gdn_dtype act_dtype,
                                const gdn_params *params, float *out, const gdn_dims *dims,
-                               int32_t n_tokens, int32_t chunk, gdn_stream_t stream);
+                               int32_t n_tokens, int32_t chunk, void *workspace,
+                               size_t workspace_bytes, gdn_stream_t stream);
 
 /*
- * Every wait inside a kernel (on a bulk copy or a tensor-core operation) is
- * bounded; a kernel whose wait gives up sets a bit in a device-side error word
- * and skips the rest of its work instead of hanging (bits 1, 2, 8: the chunked
- * prefill's tensor-core and copy waits; bit 32: the chunked prefill found its
- * shared memory not 1024-byte aligned and did nothing; bit 64: the multi-token
- * conv's tile copy wait). gdn_verify_commit_kn sets bit 16 for an accepted count outside
- * 1..K. This call waits for all
- * work on the device (it synchronises), reads the word into *code (may be
+ * Every wait inside a kernel on a bulk copy, a tensor-core operation or
+ * another warp group of the same CTA is bounded by the GPU's global timer
+ * (2 s); a kernel whose wait gives up sets a bit in a device-side error word,
+ * stops its remaining work, waits (bounded again) for the copies and products
+ * it already issued, frees its tensor memory and returns instead of hanging:
+ *   bit 1   the chunked prefill's sequential pass gave up a wait
+ *   bit 2   the chunked prefill's per-chunk transform pass gave up a wait
+ *   bit 8   a copy or product the prefill issued did not finish in its drain
+ *   bit 16  gdn_verify_commit_kn saw an accepted count outside 1..K
+ *   bit 64  the multi-token conv gave up its tile-copy wait
+ * The one wait not bounded by the library is the hardware's tensor-memory
+ * allocation at the start of the prefill kernels, which lasts until CTAs of
+ * other launches on the same SM release their columns. This call waits for
+ * all work on the device (it synchronises), reads the word into *code (may be
  * NULL) and clears it. Returns GDN_OK when no bit was set, GDN_ERR_DEVICE when
  * one was, GDN_ERR_CUDA if the read failed.
  */

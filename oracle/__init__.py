@@ -173,7 +173,7 @@ def recurrence_scan(q, k, v, g, beta, S, scale):
 # ---------------------------------------------------------------- whole layer
 def layer(x, z, alpha, beta_logit, conv_w, dt, A_log, norm_w, state_d1, hist,
           Hq, W, l2_eps=1e-6, rms_eps=1e-6, seqs=None, snap_after=-1,
-          intermediates=False, threads=None, bf16_state=False):
+          intermediates=False, threads=None, bf16_state=False, readout=False):
     """Run the layer over every token of each selected sequence.
 
     Activations are float32 arrays holding the exact input values
@@ -183,6 +183,7 @@ def layer(x, z, alpha, beta_logit, conv_w, dt, A_log, norm_w, state_d1, hist,
     Returns a dict of float64 arrays for the selected sequences:
       out [b][T][Hv][d], state (library layout), hist, and with
       ``intermediates`` also conv [b][T][conv_dim], g, beta [b][T][Hv], y [b][T][Hv][d];
+      with ``readout`` alone, y only (the readout before the gated norm);
       with snap_after >= 0 also state_snap, hist_snap.
     bf16_state runs the bf16-state variant: each head's state is rounded to
     bfloat16 after its step and each output value is rounded to bfloat16.
@@ -201,6 +202,8 @@ def layer(x, z, alpha, beta_logit, conv_w, dt, A_log, norm_w, state_d1, hist,
     if intermediates:
         res.update(conv=_np.empty((nb, T, cd)), g=_np.empty((nb, T, Hv)),
                    beta=_np.empty((nb, T, Hv)), y=_np.empty((nb, T, Hv, d)))
+    elif readout:
+        res.update(y=_np.empty((nb, T, Hv, d)))
     if snap_after >= 0:
         res.update(state_snap=_np.empty((nb, Hv, d, d)), hist_snap=_np.empty((nb, cd, W - 1)))
 
@@ -215,6 +218,8 @@ def layer(x, z, alpha, beta_logit, conv_w, dt, A_log, norm_w, state_d1, hist,
         if intermediates:
             inter = [_np.empty((T, cd)), _np.empty((T, Hv)), _np.empty((T, Hv)),
                      _np.empty((T, Hv, d))]
+        elif readout:
+            inter[3] = _np.empty((T, Hv, d))
         Ss = hs = None
         if snap_after >= 0:
             Ss = _np.empty((Hv, d, d))
@@ -233,6 +238,8 @@ def layer(x, z, alpha, beta_logit, conv_w, dt, A_log, norm_w, state_d1, hist,
         res["hist"][n] = hb
         if intermediates:
             res["conv"][n], res["g"][n], res["beta"][n], res["y"][n] = inter
+        elif readout:
+            res["y"][n] = inter[3]
         if snap_after >= 0:
             res["state_snap"][n] = _np.swapaxes(Ss, -1, -2)
             res["hist_snap"][n] = hs

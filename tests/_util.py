@@ -7,6 +7,7 @@ from gated_delta_ssm_gb300 import synth
 
 OUT_TOL = 1e-3      # max relative error on layer outputs
 STATE_TOL = 1e-4    # max relative error on the fp32 recurrent state
+ELEM_FLOOR = 1e-3   # per-element metric: each element's error over max(|ref|, floor * row max)
 
 
 def as_f32(a, dtype):
@@ -95,3 +96,41 @@ def max_rel(x, ref, slice_axes: int):
     den = np.abs(rf).max(axis=1)
     den = np.where(den == 0, 1.0, den)
     return float((np.abs(xf - rf).max(axis=1) / den).max())
+
+
+def elem_rel(x, ref, floor=ELEM_FLOOR, y=None, rms_eps=1e-6):
+    """Per-element relative error of layer outputs: each element's |x - ref| over
+    max(|ref|, floor * max|ref| of its (sequence, V head) slice * gamma_row), the
+    max over all elements. Outputs are [B][T][Hv][d] or [B][Hv][d] (one token).
+
+    The floor is taken over the slice, not the token's own row: a token whose
+    readout mean square m is far below rms_eps leaves the gated RMSNorm as a
+    1/sqrt(rms_eps) scaling of its tiny readout, so its whole row is tiny.
+
+    gamma_row (1 unless the reference readout y [.., Hv, d] is given) accounts
+    for that conditioning: the norm multiplies a row's readout by its gain
+    1/sqrt(m + rms_eps), so an absolute rounding error of the readout reaches the
+    output gamma = gain_row / median gain of the slice times larger than on the
+    slice's typical row (never less than 1)."""
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if x.ndim == 3:
+        x, ref = x[:, None], ref[:, None]
+    slicemax = np.abs(ref).max(axis=(1, 3), keepdims=True)
+    gamma = 1.0
+    if y is not None:
+        y = np.asarray(y, np.float64)
+        if y.ndim == 3:
+            y = y[:, None]
+        gain = 1.0 / np.sqrt((y * y).mean(axis=-1, keepdims=True) + rms_eps)   # [B][T][Hv][1]
+        gamma = np.maximum(1.0, gain / np.median(gain, axis=1, keepdims=True))
+    den = np.maximum(np.abs(ref), floor * slicemax * gamma)
+    den = np.where(den == 0, 1.0, den)
+    return float((np.abs(x - ref) / den).max())
+
+
+def check_out(x, ref, tol=OUT_TOL, what="out", y=None):
+    """Both output metrics within tol: normwise per (sequence, V head) and per element
+    (with the reference readout y, the per-element floor follows the norm's gain)."""
+    nr, er = out_rel(x, ref), elem_rel(x, ref, y=y)
+    assert nr <= tol and er <= tol, f"{what}: normwise {nr:.3g}, per-element {er:.3g} (tol {tol:g})"

@@ -104,8 +104,32 @@ def test_verify_rejects_aliased_snapshot(lib):
 def test_prefill_rejects_bad_chunk_and_tokens(lib):
     cd, cp = _dims().c(), _params().c()
     args = [FAKE] * 6 + [gdn.GDN_BF16, ct.byref(cp), FAKE, ct.byref(cd)]
-    assert lib.gdn_prefill_chunked(*args, 128, 32, None) == gdn.GDN_ERR_UNSUPPORTED
-    assert lib.gdn_prefill_chunked(*args, 0, 64, None) == gdn.GDN_ERR_INVALID_ARG
+    ws = 1 << 30
+    assert lib.gdn_prefill_chunked(*args, 128, 32, FAKE, ws, None) == gdn.GDN_ERR_UNSUPPORTED
+    assert lib.gdn_prefill_chunked(*args, 0, 64, FAKE, ws, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_prefill_workspace_size_and_checks(lib):
+    # one 16 KB image per (sequence, V head, 64-token chunk)
+    dims = _dims()
+    cd, cp = dims.c(), _params().c()
+    for T, chunks in ((1, 1), (64, 1), (65, 2), (8192, 128)):
+        assert gdn.prefill_workspace_bytes(dims, T) == 2 * 4 * chunks * 16384
+    assert gdn.prefill_workspace_bytes(dims, 0) == 0
+    assert gdn.prefill_workspace_bytes(dims, 64, 32) == 0
+    need = gdn.prefill_workspace_bytes(dims, 130)
+    args = [FAKE] * 6 + [gdn.GDN_BF16, ct.byref(cp), FAKE, ct.byref(cd), 130, 64]
+    # missing, too small, or misaligned workspace
+    assert lib.gdn_prefill_chunked(*args, None, need, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_prefill_chunked(*args, FAKE, need - 1, None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_prefill_chunked(*args, FAKE + 8, need, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_testing_header_hook_is_exported(lib):
+    text = open(os.path.join(ROOT, "include", "gdn_testing.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    for name in set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", text)):
+        assert hasattr(lib, name), name
 
 
 def test_other_entry_points_validate(lib):

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 from gated_delta_ssm_gb300 import synth
-from tests._util import (OUT_TOL, STATE_TOL, device_inputs, dims_of, max_rel, out_rel, params_of,
+from tests._util import (check_out, OUT_TOL, STATE_TOL, device_inputs, dims_of, max_rel, out_rel, params_of,
                          run_oracle, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -74,7 +74,7 @@ def test_layer_scan_matches_oracle(name, seed):
     ref = run_oracle(shape, inp)
     dev = device_inputs(shape, inp)
     out = _layer_scan(shape, dev, shape.T).cpu().numpy()
-    assert out_rel(out, ref["out"]) <= OUT_TOL
+    check_out(out, ref["out"])
     assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= STATE_TOL
     assert np.array_equal(dev["hist"].cpu().numpy(), ref["hist"].astype(np.float32))
 
@@ -132,7 +132,7 @@ def test_verify_kn_equals_decode_steps_and_oracle(K, B, Hq, Hv, act):
     seqs = None if B <= 4 else [0, B // 2, B - 1]
     ref = run_oracle(shape, inp, seqs=seqs)
     pick = slice(None) if seqs is None else seqs
-    assert out_rel(out.cpu().numpy()[pick], ref["out"]) <= OUT_TOL
+    check_out(out.cpu().numpy()[pick], ref["out"])
     assert max_rel(dev["state"].cpu().numpy()[pick], ref["state"], 2) <= STATE_TOL
     if K > 1 and seqs is None:
         mid = K // 2
