@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "../../include/gdn.h"
 #include "../../include/gdn_testing.h"
@@ -451,6 +452,66 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
     a.wait_ns = gdn::kDefaultWaitNs;
     a.first_wait_ns = gdn::first_wait_override_ns();
     return from_cuda(gdn::launch_prefill(a, act_dtype == GDN_BF16, as_cuda(stream)));
+}
+
+// ------------------------------------------------------------------ allocation-free prefill
+// Callers that cannot allocate device memory get the prefill's workspace from a
+// fixed array owned by the library. It lives in this file so that the host side
+// can resolve its device address here.
+}  // extern "C"
+
+namespace {
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;   // 16 MiB: 1024 chunk images
+__device__ __align__(256) uint8_t g_prefill_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_prefill_scratch on the current device, resolved once per
+// device (the host-side symbol is only a stand-in for it).
+gdn_status scratch_address(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return from_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices)
+        return GDN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_prefill_scratch);
+        if (e != cudaSuccess)
+            return from_cuda(e);
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return GDN_OK;
+}
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_prefill_chunked_noalloc(float *state, float *conv_state, const void *x,
+                                       const void *z, const void *alpha, const void *beta_logit,
+                                       gdn_dtype act_dtype, const gdn_params *params, float *out,
+                                       const gdn_dims *dims, int32_t n_tokens, int32_t chunk,
+                                       gdn_stream_t stream)
+{
+    const size_t need = gdn_prefill_workspace_bytes(dims, n_tokens, chunk);
+    if (need > kStaticScratchBytes) {
+        snprintf(g_last_cuda_error, sizeof g_last_cuda_error,
+                 "gdn_prefill_chunked_noalloc: %zu bytes of scratch needed, the static scratch "
+                 "holds %zu", need, kStaticScratchBytes);
+        return GDN_ERR_UNSUPPORTED;
+    }
+    void *scratch = nullptr;
+    const gdn_status st = scratch_address(&scratch);
+    if (st != GDN_OK)
+        return st;
+    return gdn_prefill_chunked(state, conv_state, x, z, alpha, beta_logit, act_dtype, params, out,
+                               dims, n_tokens, chunk, scratch, kStaticScratchBytes, stream);
 }
 
 void gdn_testing_set_first_wait_ns(uint64_t ns)

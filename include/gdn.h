@@ -346,6 +346,35 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
                                size_t workspace_bytes, gdn_stream_t stream);
 
 /*
+ * gdn_prefill_chunked for callers that cannot allocate device memory, e.g. a
+ * runtime that hands out every byte of device memory from a plan fixed at
+ * start-up and exposes no allocator to the libraries it loads, or a loop with
+ * latency bounds that an allocation (which may synchronise the device) would
+ * break. None of the source pages has a counterpart: it is a packaging of
+ * gdn_prefill_chunked, same arguments and results, without the workspace.
+ *
+ * The workspace is a fixed 16 MiB array inside the library (a static device
+ * variable): every GPU on which the library is loaded holds it until the
+ * process exits, and it serves up to 1024 chunk images, i.e.
+ * n_seq * n_v_heads * ceil(n_tokens / 64) <= 1024. Larger calls return
+ * GDN_ERR_UNSUPPORTED (the reason is in gdn_last_cuda_error()) and launch
+ * nothing. The library itself allocates nothing either.
+ *
+ * The first call on a device resolves the array's device address on the
+ * current device; make that first call before any stream capture. Every call
+ * on a device shares the one array and leaves its contents behind: nothing in
+ * it needs to start at zero (each call writes every image it reads first), but
+ * calls whose work overlaps on the GPU (other streams, other host threads)
+ * race on it and must be ordered by the caller.
+ * Errors: as gdn_prefill_chunked, plus GDN_ERR_UNSUPPORTED beyond the limit.
+ */
+gdn_status gdn_prefill_chunked_noalloc(float *state, float *conv_state, const void *x,
+                                       const void *z, const void *alpha, const void *beta_logit,
+                                       gdn_dtype act_dtype, const gdn_params *params, float *out,
+                                       const gdn_dims *dims, int32_t n_tokens, int32_t chunk,
+                                       gdn_stream_t stream);
+
+/*
  * Every wait inside a kernel on a bulk copy, a tensor-core operation or
  * another warp group of the same CTA is bounded by the GPU's global timer
  * (2 s); a kernel whose wait gives up sets a bit in a device-side error word,
