@@ -175,6 +175,21 @@ def decode_bytes(shape: synth.Shape) -> dict:
     return {"state": state, "total": state + hist + acts + out + params}
 
 
+def prefill_work(shape: synth.Shape) -> dict:
+    """Algorithmic work of one chunked prefill call: the chunk form's dense products
+    (5 x 2C^2 d + 3 x 2 C d^2 per (chunk, V head), C = 64, d = 128: ~11.6 MFLOP,
+    counted once per product) and the compulsory HBM bytes (x read, z read, outputs
+    written, state read + written, conv history read + written)."""
+    C, d = 64, shape.d
+    n_units = shape.B * shape.Hv * ((shape.T + C - 1) // C)
+    flops = n_units * (5 * 2 * C * C * d + 3 * 2 * C * d * d)
+    act = 2 if shape.act_dtype == "bf16" else 4
+    rows = shape.B * shape.T
+    nbytes = (rows * (shape.conv_dim + shape.Hv * d + 2 * shape.Hv) * act + rows * shape.Hv * d * 4
+              + 2 * shape.B * shape.Hv * d * d * 4 + 2 * shape.B * shape.conv_dim * (shape.W - 1) * 4)
+    return {"flops": float(flops), "bytes": float(nbytes)}
+
+
 # ------------------------------------------------------------------ GPU measurements
 class Gpu:
     def __init__(self, local_rank: int):
@@ -483,20 +498,32 @@ class Gpu:
         d = self.upload(shape, inp)
         dims, prm = self.dims(shape), self.params(d)
         out = torch.empty(shape.B, shape.T, shape.Hv, shape.d, device=self.dev)
+        ws_bytes = gdn.prefill_workspace_bytes(dims, shape.T)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=self.dev)
 
         def pstep(i):
             gdn.prefill_chunked(d["states"][0], d["hists"][0], d["x"], d["z"], d["alpha"],
-                                d["beta_logit"], prm, out, dims, shape.T, 64)
+                                d["beta_logit"], prm, out, dims, shape.T, 64, workspace=ws)
 
         try:
             t = self.time_steps(pstep, steps, warmup)
         except gdn.GdnError as e:
             return {"unavailable": str(e)}
-        self.launches += steps
+        self.launches += 3 * steps           # transform pass, sequential pass, history update
         m = statistics.mean(t)
         toks = shape.B * shape.T
-        flops = 11.6e6 * shape.B * shape.Hv * (shape.T / 64)
-        return {"ms": m * 1e3, "tokens_per_s": toks / m, "chunk_TFLOPs": flops / m / 1e12}
+        nb = prefill_work(shape)
+        hbm_peak, tc_peak, peak_kind = measured_peaks()
+        tflops, gbs = nb["flops"] / m / 1e12, nb["bytes"] / m / 1e9
+        return {"ms": m * 1e3, "tokens_per_s": toks / m, "chunk_TFLOPs": tflops,
+                "workspace_bytes": ws_bytes,
+                "roofline": {"bound": "tensor", "flops_per_launch": nb["flops"],
+                             "bytes_per_launch": nb["bytes"], "achieved": tflops, "peak": tc_peak,
+                             "unit": "TFLOP/s", "frac": tflops / tc_peak,
+                             "hbm_achieved": gbs, "hbm_peak": hbm_peak, "hbm_frac": gbs / hbm_peak,
+                             "peak_kind": peak_kind,
+                             "note": "whole call (3 launches); per-kernel shares in "
+                                     "profiles/prefill_*__prefill_4x8192.md"}}
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
