@@ -461,7 +461,7 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
 }  // extern "C"
 
 namespace {
-constexpr size_t kStaticScratchBytes = (size_t)16 << 20;   // 16 MiB: 1024 chunk images
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;   // 16 MiB: 512 chunk images
 __device__ __align__(256) uint8_t g_prefill_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;

@@ -15,24 +15,23 @@
 //   S_C = e^{Gam_C} S_0 + K^T diag(e^{Gam_C - Gam}) U
 //
 // Pass 1 (prefill_ut_kernel) is parallel over every (sequence, QK head,
-// chunk): it stages the chunk's raw K rows in shared memory by tensor copy,
-// runs the conv + SiLU + L2 on them, forms K K^T on the tensor core, and for
-// each V head of the group builds A and solves T = (I + A)^-1 by blocked
-// forward substitution, writing T as a 16 KB two-part fp16 operand image to the
+// chunk): it stages the chunk's raw Q and K rows in shared memory by tensor
+// copy, runs the conv + SiLU + L2 on them, forms G = [Q; K] K^T on the tensor
+// core, and for each V head of the group builds P (from Q K^T) and A (from
+// K K^T) in parallel and solves T = (I + A)^-1 by blocked forward
+// substitution, writing T and P as 16 KB two-part fp16 operand images to the
 // caller's workspace. Nothing in it depends on the state.
 //
 // Pass 2 (prefill_chain_kernel) walks the chunks of one (sequence, V head)
 // with the fp32 state master in tensor memory. Its warps are specialised:
-//   * an issue warp: the bulk/tensor copies of the next chunks' raw rows and
-//     T images, and every tensor-core product;
 //   * 8 conv warps: conv + SiLU + L2 of chunk c+1's Q, K, V rows (from the
-//     staged rows) and the gates, while chunk c's products run; P of chunk c;
+//     staged rows) and the gates, while chunk c's products run;
 //   * 8 epilogue warps (two per TMEM lane quarter, value row j = lane):
-//     X, U, the state re-split, the state write-back, and the gated RMSNorm.
+//     X, U, the state re-split, the state write-back, and the gated RMSNorm;
+//     lane 0 of warp 0 also issues every bulk / tensor copy and every product.
 // The products (transposed orientation, M = 128 value rows j, A operands in
 // tensor memory, B operands in shared memory):
 //   D1 = S_0^T [Q; K]^T        ((Q S_0)^T | (K S_0)^T)
-//   G  = [Q; K] K^T            (Q K^T for P)
 //   D2 = X^T T^T = U^T         (the UT transform on the tensor core)
 //   S^T += U'^T K              (U' = diag(e^{Gam_C - Gam}) U; K read MN-major)
 //   (P U)^T = U^T P^T          (into D2 once U^T is read; O = e^Gam Q S_0 + P U is
@@ -389,23 +388,27 @@ constexpr uint32_t kRawBox = ((kC + kMaxW - 1) * kD * 2 + 1023) / 1024 * 1024;
 // ================================================================== pass 1
 namespace p1 {
 constexpr int kThreads = 256;
-constexpr uint32_t RAW = 0;                       // staged K rows
-constexpr uint32_t KT = RAW + kRawBox;            // K tile, two parts [64][128] sw128 (+ slack)
-constexpr uint32_t KT_LO = KT + 16384;
-constexpr uint32_t KT_BYTES = 40960;              // the M = 128 A descriptor reads 8 KB past KT_LO's end
-constexpr uint32_t AM = KT;                       // after G: A of two heads, fp32 [64][64] each
-constexpr int kTS = 68;                           // T row stride (floats)
-constexpr uint32_t TB = KT + KT_BYTES;            // T of two heads, fp32 [64][68]
-constexpr uint32_t GATES = TB + 2 * kC * kTS * 4;
-constexpr uint32_t MBAR = GATES + 8 * sizeof(Gates);
+constexpr uint32_t RAWQ = 0, RAWK = kRawBox;       // staged Q and K rows of the QK head
+constexpr uint32_t QK = 2 * kRawBox;               // [Q; K] two fp16 parts, [128 t'][128 i] sw128
+constexpr uint32_t QK_LO = QK + 32768;
+constexpr uint32_t AM = QK;                        // after G: A of two heads, fp32 [64][64]
+constexpr uint32_t TB = QK + 32768;                // after G: T of two heads, fp32 [64][64]
+constexpr uint32_t GATES = QK + 65536;             // two Gates
+constexpr uint32_t MBAR = GATES + 2 * sizeof(Gates);
 constexpr uint32_t SLOT = MBAR + 16;
 constexpr uint32_t BYTES = SLOT + 16 + 1024;      // + alignment slack
-static_assert(KT % 1024 == 0 && KT_LO % 1024 == 0, "swizzled tiles on 1 KB boundaries");
-static_assert(2 * kC * kC * 4 <= KT_BYTES, "A of two heads fits in the K tile's space");
+static_assert(QK % 1024 == 0, "swizzled tiles on 1 KB boundaries");
 }  // namespace p1
 
-// A[t][s] (fp32, 64 floats per row), float4 chunks XOR-swizzled by the row
+// A[t][s] and T[i][j] (fp32, 64 floats per row), float4 chunks XOR-swizzled by the row
 __device__ __forceinline__ int a_idx(int t, int s) { return t * kC + ((((s >> 2) ^ (t & 15))) << 2) + (s & 3); }
+
+// One chunk's image in the workspace: T = (I + A)^-1 then P, each as two fp16
+// parts of a [64][64] K-major core-matrix tile (8 KB per part).
+__device__ __forceinline__ uint8_t *chunk_image(const PrefillArgs &a, int b, int h, int c)
+{
+    return a.ws + (((size_t)b * a.Hv + h) * a.n_chunks + c) * kPrefillChunkImage;
+}
 
 template <typename TIn, int WC>
 __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_constant__ CUtensorMap xmap,
@@ -430,8 +433,9 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         if (staged) {
-            tc::mbar_expect_tx(mb_raw, (uint32_t)(kC + W - 1) * kD * 2);
-            rows_copy(&xmap, sbase + p1::RAW, mb_raw, a.Hq * kD + hk * kD, c0 - (W - 1), b);
+            tc::mbar_expect_tx(mb_raw, 2u * (uint32_t)(kC + W - 1) * kD * 2);
+            rows_copy(&xmap, sbase + p1::RAWQ, mb_raw, hk * kD, c0 - (W - 1), b);
+            rows_copy(&xmap, sbase + p1::RAWK, mb_raw, a.Hq * kD + hk * kD, c0 - (W - 1), b);
         } else {
             tc::mbar_arrive(mb_raw);
         }
@@ -443,18 +447,18 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + p1::SLOT);
 
-    // gates of the group's V heads (warp w: head hk*r + w)
-    if (warp < r)
-        chunk_gates<TIn>(a, b, hk * r + warp, c0, n, 0, gates + warp);
-
-    // K rows: conv + SiLU + L2 (warp = 8-token block, lane = 4 channels) -> K tile
+    // Q and K rows: conv + SiLU + L2 (warp = 8-token block, lane = 4 channels) -> [Q; K] tile
     bool ok = tc::mbar_wait_ns(mb_raw, 0, lim, abort);
     if (ok) {
-        float v[8][4];
-        conv_block<TIn, WC, 4>(a, b, c0, n, a.Hq * kD + hk * kD + 4 * lane, 8 * warp,
-                               staged ? reinterpret_cast<const __nv_bfloat16 *>(smem + p1::RAW) : nullptr, v);
-        l2_rows<4>(v, a.l2_eps, kQK);
-        store_rows_split<4>(smem + p1::KT, smem + p1::KT_LO, 8 * warp, kC, lane, v);
+#pragma unroll 1
+        for (int part = 0; part < 2; ++part) {
+            float v[8][4];
+            const __nv_bfloat16 *raw =
+                staged ? reinterpret_cast<const __nv_bfloat16 *>(smem + (part ? p1::RAWK : p1::RAWQ)) : nullptr;
+            conv_block<TIn, WC, 4>(a, b, c0, n, (part ? a.Hq * kD : 0) + hk * kD + 4 * lane, 8 * warp, raw, v);
+            l2_rows<4>(v, a.l2_eps, kQK);
+            store_rows_split<4>(smem + p1::QK, smem + p1::QK_LO, part * kC + 8 * warp, 2 * kC, lane, v);
+        }
     } else {
         atomicOr(const_cast<int *>(abort), (int)kErrUT);
     }
@@ -464,18 +468,20 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
     tc::fence_after_sync();
     ok = *abort == 0;
 
-    // G = K K^T (rows 64..127 of the A operand read unused data: their results are ignored)
+    // G = [Q; K] K^T: rows 0..63 give Q K^T (for P), rows 64..127 K K^T (for A)
     const bool mma_issued = ok;
     if (ok && tid == 0) {
         const uint32_t id = tc::idesc_f16(128, 64);
 #pragma unroll 1
         for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t kq = (kk >> 2) * (kC * 128) + (kk & 3) * 32;
-            const uint64_t d1 = tc::sdesc_sw128(sbase + p1::KT + kq);
-            const uint64_t d2 = tc::sdesc_sw128(sbase + p1::KT_LO + kq);
-            tc::mma_f16(tmem, d1, d1, id, kk > 0);
-            tc::mma_f16(tmem, d1, d2, id, 1);
-            tc::mma_f16(tmem, d2, d1, id, 1);
+            const uint32_t kq = (kk >> 2) * (2 * kC * 128) + (kk & 3) * 32;
+            const uint64_t a1 = tc::sdesc_sw128(sbase + p1::QK + kq);
+            const uint64_t a2 = tc::sdesc_sw128(sbase + p1::QK_LO + kq);
+            const uint64_t b1 = tc::sdesc_sw128(sbase + p1::QK + kC * 128 + kq);
+            const uint64_t b2 = tc::sdesc_sw128(sbase + p1::QK_LO + kC * 128 + kq);
+            tc::mma_f16(tmem, a1, b1, id, kk > 0);
+            tc::mma_f16(tmem, a1, b2, id, 1);
+            tc::mma_f16(tmem, a2, b1, id, 1);
         }
         tc::mma_commit(mb_mma);
     }
@@ -489,112 +495,131 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
 
     float *Am = reinterpret_cast<float *>(smem + p1::AM);
     float *Tb = reinterpret_cast<float *>(smem + p1::TB);
-    const int hsel = warp >> 2;                 // head of the pair this warp serves
-    const bool solver = (warp & 3) < 2;         // warps 0, 1, 4, 5: TMEM lanes 0..63
-    const int trow = 32 * (warp & 1) + lane;    // token row t (A) / column j (T)
-    const uint32_t lane_q = (uint32_t)(32 * (warp & 3)) << 16;
+    const int q4 = warp & 3, hsel = warp >> 2;
+    const uint32_t lane_q = (uint32_t)(32 * q4) << 16;
 
 #pragma unroll 1
     for (int hp = 0; ok && hp < r; hp += 2) {
+        if (warp < 2 && hp + warp < r)
+            chunk_gates<TIn>(a, b, hk * r + hp + warp, c0, n, 0, gates + warp);
+        __syncthreads();
         const int hh = hp + hsel;
-        // ---- A[t][s] = beta_t e^{Gam_t - Gam_s} (k_t . k_s), s < t
-        if (solver && hh < r) {
-            const Gates *G = gates + hh;
+        // ---- P (TMEM lanes 0..63, the Q rows: warps 0, 1, 4, 5) and A (lanes 64..127, the
+        //      K rows: warps 2, 3, 6, 7) of the pair's two heads, one token row per thread
+        if (hh < r) {
+            const Gates *G = gates + hsel;
+            const int t = 32 * (q4 & 1) + lane;
+            const bool is_a = q4 >= 2;
+            const float gt = G->gh[t], gtl = G->gl[t];
+            const float rowf = is_a ? __fmul_rn(G->beta[t], kInvQK2) : kInvQK2;
+            uint8_t *pimg = chunk_image(a, b, hk * r + hh, c) + 16384;
             float *A = Am + hsel * kC * kC;
-            const int t = trow;
-            const float gt = G->gh[t], gtl = G->gl[t], bt = G->beta[t];
+            const int tmax = 32 * (q4 & 1) + 31;              // largest row of this warp
 #pragma unroll 1
             for (int s0 = 0; s0 < kC; s0 += 16) {
                 float gv[16];
-                if (s0 <= 32 * (warp & 1) + 31)   // warp-uniform: some row of this warp needs the block
+                if (s0 <= tmax)                               // warp-uniform
                     tc::tmem_ld16(tmem + lane_q + s0, gv);
-                else
+                float o[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        gv[e] = 0.0f;
+                for (int e = 0; e < 16; ++e) {
+                    const int s = s0 + e;
+                    const bool keep = t < n && (is_a ? s < t : s <= t);
+                    o[e] = keep ? __fmul_rn(__fmul_rn(rowf, exp_diff(gt, gtl, G->gh[s], G->gl[s])), gv[e]) : 0.0f;
+                }
+                if (is_a) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float o[4];
+                    for (int qq = 0; qq < 4; ++qq)
+                        *reinterpret_cast<float4 *>(A + a_idx(t, s0 + 4 * qq)) =
+                            make_float4(o[4 * qq], o[4 * qq + 1], o[4 * qq + 2], o[4 * qq + 3]);
+                } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s = s0 + 4 * q + e;
-                        o[e] = (s < t && t < n) ? __fmul_rn(__fmul_rn(__fmul_rn(bt, kInvQK2),
-                                                                        exp_diff(gt, gtl, G->gh[s], G->gl[s])),
-                                                            gv[4 * q + e])
-                                                : 0.0f;
+                    for (int hq = 0; hq < 2; ++hq) {
+                        uint4 hi, lo;
+                        split_pair(o[8 * hq], o[8 * hq + 1], hi.x, lo.x);
+                        split_pair(o[8 * hq + 2], o[8 * hq + 3], hi.y, lo.y);
+                        split_pair(o[8 * hq + 4], o[8 * hq + 5], hi.z, lo.z);
+                        split_pair(o[8 * hq + 6], o[8 * hq + 7], hi.w, lo.w);
+                        const uint32_t off = tc::km_offset(t, s0 + 8 * hq, kC);
+                        *reinterpret_cast<uint4 *>(pimg + off) = hi;
+                        *reinterpret_cast<uint4 *>(pimg + 8192 + off) = lo;
                     }
-                    *reinterpret_cast<float4 *>(A + a_idx(t, s0 + 4 * q)) = make_float4(o[0], o[1], o[2], o[3]);
                 }
             }
         }
         __syncthreads();
-        // ---- T = (I + A)^-1, column j per thread, blocks of 8 rows:
-        //      T[i][j] = [i == j] - sum_{s < i} A[i][s] T[s][j]
-        if (solver && hh < r) {
-            const float *A = Am + hsel * kC * kC;
-            float *Tc = Tb + hsel * kC * p1::kTS;
-            const int j = trow;
-            const int S0 = (32 * (warp & 1)) >> 3;   // T[s][j] = 0 for s < j: earlier blocks are zero
+        // ---- T = (I + A)^-1, two threads per column j (the row blocks of the sum split by
+        //      parity), blocks of 8 rows: T[i][j] = [i == j] - sum_{s < i} A[i][s] T[s][j]
+        {
+            const int hs = tid >> 7, j = (tid >> 1) & 63, half = tid & 1;
+            if (hp + hs < r) {
+                const float *A = Am + hs * kC * kC;
+                float *Tc = Tb + hs * kC * kC;
+                const int S0 = 2 * (warp & 3);                 // T[s][j] = 0 for s < j: skip those blocks
 #pragma unroll 1
-            for (int I = 0; I < 8; ++I) {
-                float acc[8];
+                for (int I = 0; I < 8; ++I) {
+                    float acc[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    acc[q] = 0.0f;
+                    for (int q = 0; q < 8; ++q)
+                        acc[q] = 0.0f;
 #pragma unroll 1
-                for (int S = S0; S < I; ++S) {
-                    float ts[8];
+                    for (int S = S0 + half; S < I; S += 2) {
+                        float ts[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        ts[e] = Tc[(8 * S + e) * p1::kTS + j];
+                        for (int e = 0; e < 8; ++e)
+                            ts[e] = Tc[a_idx(8 * S + e, j)];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int i = 8 * I + q;
+                            const float4 a0 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * S));
+                            const float4 a1 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * S + 4));
+                            acc[q] = __fmaf_rn(a0.x, ts[0], acc[q]);
+                            acc[q] = __fmaf_rn(a0.y, ts[1], acc[q]);
+                            acc[q] = __fmaf_rn(a0.z, ts[2], acc[q]);
+                            acc[q] = __fmaf_rn(a0.w, ts[3], acc[q]);
+                            acc[q] = __fmaf_rn(a1.x, ts[4], acc[q]);
+                            acc[q] = __fmaf_rn(a1.y, ts[5], acc[q]);
+                            acc[q] = __fmaf_rn(a1.z, ts[6], acc[q]);
+                            acc[q] = __fmaf_rn(a1.w, ts[7], acc[q]);
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        acc[q] = __fadd_rn(acc[q], __shfl_xor_sync(0xffffffffu, acc[q], 1));
+                    float x[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const int i = 8 * I + q;
-                        const float4 a0 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * S));
-                        const float4 a1 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * S + 4));
-                        acc[q] = __fmaf_rn(a0.x, ts[0], acc[q]);
-                        acc[q] = __fmaf_rn(a0.y, ts[1], acc[q]);
-                        acc[q] = __fmaf_rn(a0.z, ts[2], acc[q]);
-                        acc[q] = __fmaf_rn(a0.w, ts[3], acc[q]);
-                        acc[q] = __fmaf_rn(a1.x, ts[4], acc[q]);
-                        acc[q] = __fmaf_rn(a1.y, ts[5], acc[q]);
-                        acc[q] = __fmaf_rn(a1.z, ts[6], acc[q]);
-                        acc[q] = __fmaf_rn(a1.w, ts[7], acc[q]);
+                        const float4 a0 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * I));
+                        const float4 a1 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * I + 4));
+                        const float ad[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                        float sum = acc[q];
+#pragma unroll
+                        for (int e = 0; e < q; ++e)
+                            sum = __fmaf_rn(ad[e], x[e], sum);
+                        x[q] = __fsub_rn(i == j ? 1.0f : 0.0f, sum);
                     }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        Tc[a_idx(8 * I + 4 * half + q, j)] = x[4 * half + q];
+                    __syncwarp();
                 }
-                float x[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int i = 8 * I + q;
-                    const float4 a0 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * I));
-                    const float4 a1 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * I + 4));
-                    const float ad[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                    float s = acc[q];
-#pragma unroll
-                    for (int e = 0; e < q; ++e)
-                        s = __fmaf_rn(ad[e], x[e], s);
-                    x[q] = __fsub_rn(i == j ? 1.0f : 0.0f, s);
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    Tc[(8 * I + q) * p1::kTS + j] = x[q];
             }
         }
         __syncthreads();
         // ---- T -> two-part fp16 K-major image ([t][s], 8x8 core matrices) in the workspace
 #pragma unroll 1
         for (int u = 0; u < 2; ++u) {
-            const int hh2 = hp + u;
-            if (hh2 >= r)
+            if (hp + u >= r)
                 break;
-            const float *Tc = Tb + u * kC * p1::kTS;
-            uint8_t *img = a.ws + (((size_t)b * a.Hv + hk * r + hh2) * a.n_chunks + c) * kPrefillChunkImage;
+            const float *Tc = Tb + u * kC * kC;
+            uint8_t *img = chunk_image(a, b, hk * r + hp + u, c);
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const int p = tid + 256 * k;                       // 16-byte chunk of a part
                 const int t = ((p >> 6) << 3) | (p & 7), s8 = (p >> 3) & 7;
-                const float4 f0 = *reinterpret_cast<const float4 *>(Tc + t * p1::kTS + 8 * s8);
-                const float4 f1 = *reinterpret_cast<const float4 *>(Tc + t * p1::kTS + 8 * s8 + 4);
+                const float4 f0 = *reinterpret_cast<const float4 *>(Tc + a_idx(t, 8 * s8));
+                const float4 f1 = *reinterpret_cast<const float4 *>(Tc + a_idx(t, 8 * s8 + 4));
                 uint4 hi, lo;
                 split_pair(f0.x, f0.y, hi.x, lo.x);
                 split_pair(f0.z, f0.w, hi.y, lo.y);
@@ -625,7 +650,7 @@ constexpr int kThreads = 512;                     // 8 epilogue warps (warp 0 al
 constexpr uint32_t QK_HI = 0, QK_LO = 32768;      // [Q; K] two parts, [128 t'][128 i] sw128
 constexpr uint32_t VF = 65536;                    // V^T fp32 footprint [128 j][64 t]
 constexpr uint32_t TT = 98304;                    // T image of the current chunk (16 KB)
-constexpr uint32_t PP = 114688;                   // P two parts, [64 t][64 s] K-major
+constexpr uint32_t PP = 114688;                   // P image of the current chunk (16 KB)
 constexpr uint32_t OS = 131072;                   // O staging, fp32 [64 t][128 j]
 constexpr uint32_t RAW = 163840;                  // staged rows: Q, K, V heads
 constexpr uint32_t GATES = RAW + 3 * kRawBox;     // two Gates buffers
@@ -637,7 +662,7 @@ static_assert(RAW % 1024 == 0 && kRawBox % 1024 == 0, "staged rows on 1 KB bound
 // barriers
 enum { B_RAW, B_T, B_M1, B_M2, B_M3, B_QK, B_P, B_ST, B_X, B_U, B_V, B_RAWFREE, B_OS, B_N };
 // TMEM columns
-constexpr uint32_t TS = 0, D1 = 128, R1 = 256, GG = 384, D2 = 448;
+constexpr uint32_t TS = 0, D1 = 128, R1 = 256, D2 = 448;
 }  // namespace p2
 
 // fp32 V^T footprint: float4 q (tokens 4q .. 4q+3) of value row j; the 16-byte
@@ -685,7 +710,7 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
     const uint64_t lim = a.wait_ns;
 
     if (tid == 0) {
-        const uint32_t counts[B_N] = {1, 1, 1, 1, 1, 256, 128, 256, 256, 256, 256, 256, 256};
+        const uint32_t counts[B_N] = {1, 1, 1, 1, 1, 256, 1, 256, 256, 256, 256, 256, 256};
         for (int i = 0; i < B_N; ++i)
             tc::mbar_init(bar(i), counts[i]);
         *abort = 0;
@@ -717,9 +742,6 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
         // V rows: 8 tokens x 4 channels per thread
         const int v_ch = 2 * a.Hq * kD + h * kD + 4 * lane;
         const __nv_bfloat16 *v_raw = raw != nullptr ? raw + 2 * (kRawBox / 2) : nullptr;
-        const bool pwarp = (warp & 3) < 2;      // warps 8, 9, 12, 13: TMEM lanes 0..63 (rows t of G)
-        const int pt = 32 * (warp & 1) + lane;  // P row t
-        const int psh = (warp >> 2) & 1;        // P columns s in [32 psh, 32 psh + 32)
 
         auto v_conv = [&](int c0, int n) {
             float v[8][4];
@@ -756,46 +778,6 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
         for (int c = 0; ok && c < nch; ++c) {
             const uint32_t par = c & 1;
             const int c0 = c * kC, n = min(kC, a.T - c0);
-            ok = waitb(B_M1, par, lim) && waitb(B_QK, par, lim);
-            if (!ok)
-                break;
-            tc::fence_after_sync();
-            // ---- P[t][s] = e^{Gam_t - Gam_s} (q_t . k_s) for s <= t (t < n), two parts
-            if (pwarp) {
-                const Gates *G = gbuf + (c & 1);
-                const int t = pt;
-                float o[32];
-                if (psh <= (warp & 1)) {          // warp-uniform: the block holds some s <= t
-                    float gv[32];
-                    tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + GG + 32 * psh, gv);
-                    const float gt = G->gh[t], gtl = G->gl[t];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int s = 32 * psh + e;
-                        o[e] = (s <= t && t < n) ? __fmul_rn(__fmul_rn(exp_diff(gt, gtl, G->gh[s], G->gl[s]), kInvQK2),
-                                                             gv[e])
-                                                 : 0.0f;
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        o[e] = 0.0f;
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 hi, lo;
-                    split_pair(o[8 * q], o[8 * q + 1], hi.x, lo.x);
-                    split_pair(o[8 * q + 2], o[8 * q + 3], hi.y, lo.y);
-                    split_pair(o[8 * q + 4], o[8 * q + 5], hi.z, lo.z);
-                    split_pair(o[8 * q + 6], o[8 * q + 7], hi.w, lo.w);
-                    const uint32_t off = tc::km_offset(t, 32 * psh + 8 * q, kC);
-                    *reinterpret_cast<uint4 *>(smem + PP + off) = hi;
-                    *reinterpret_cast<uint4 *>(smem + PP + 8192 + off) = lo;
-                }
-                tc::fence_smem_to_async();
-                tc::fence_before_sync();
-                tc::mbar_arrive(bar(B_P));
-            }
             if (c + 1 >= nch)
                 break;
             // ---- chunk c+1: gates, V rows (once chunk c's X has read V), Q rows, K rows
@@ -817,11 +799,11 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             conv_block<TIn, WC, 8>(a, b, c1, n1, qk_ch, 8 * qk_tb, qk_raw, v);
             l2_rows<8>(v, a.l2_eps, kQK);
             tc::mbar_arrive(bar(B_RAWFREE));
-            if (qk_part == 1) {
-                ok = waitb(B_M3, par, lim);                 // K rows free: this chunk's S update done
-                if (!ok)
-                    break;
-            }
+            // Q rows are free once this chunk's D1 product is done, K rows once its state
+            // update is
+            ok = qk_part == 0 ? waitb(B_M1, par, lim) : waitb(B_M3, par, lim);
+            if (!ok)
+                break;
             store_rows_split<8>(smem + QK_HI, smem + QK_LO, qk_part * kC + 8 * qk_tb, 2 * kC, qk_g, v);
             tc::fence_smem_to_async();
             tc::mbar_arrive(bar(B_QK));
@@ -831,7 +813,7 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
         // Lane 0 of warp 0 also issues every copy and tensor-core product, at the
         // points of its own program where their inputs are ready.
         const bool issuer = tid == 0;
-        int raw_last = -1, t_last = -1, last_commit = -1;
+        int raw_last = -1, t_last = -1, p_last = -1, last_commit = -1;
         uint32_t last_phase = 0;
         const uint32_t raw_bytes = 3u * (uint32_t)(kC + W - 1) * kD * 2;
         auto issue_raw = [&](int cc) {
@@ -846,14 +828,18 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             }
             raw_last = cc;
         };
-        auto issue_t = [&](int cc) {
-            const uint8_t *src = a.ws + (((size_t)b * a.Hv + h) * nch + cc) * kPrefillChunkImage;
-            tc::mbar_expect_tx(bar(B_T), (uint32_t)kPrefillChunkImage);
-            tc::bulk_copy_g2s(sbase + TT, src, (uint32_t)kPrefillChunkImage, bar(B_T));
+        auto issue_t = [&](int cc) {     // T image of chunk cc
+            tc::mbar_expect_tx(bar(B_T), 16384u);
+            tc::bulk_copy_g2s(sbase + TT, chunk_image(a, b, h, cc), 16384u, bar(B_T));
             t_last = cc;
         };
-        const uint32_t idG = tc::idesc_f16(128, 64), id128 = tc::idesc_f16(128, 128);
-        // G = [Q; K] K^T and D1 = S_0^T [Q; K]^T, once the [Q; K] tile and S_0^T are ready
+        auto issue_p = [&](int cc) {     // P image of chunk cc
+            tc::mbar_expect_tx(bar(B_P), 16384u);
+            tc::bulk_copy_g2s(sbase + PP, chunk_image(a, b, h, cc) + 16384, 16384u, bar(B_P));
+            p_last = cc;
+        };
+        const uint32_t id64 = tc::idesc_f16(128, 64), id128 = tc::idesc_f16(128, 128);
+        // D1 = S_0^T [Q; K]^T, once the [Q; K] tile and S_0^T are ready
         auto issue_m1 = [&](int c) -> bool {
             const uint32_t par = c & 1;
             // the first wait of the kernel takes its limit from first_wait_ns (a test hook)
@@ -869,11 +855,6 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 const uint32_t kq = (kk >> 2) * (2 * kC * 128) + (kk & 3) * 32;
                 const uint64_t a1 = tc::sdesc_sw128(sbase + QK_HI + kq);
                 const uint64_t a2 = tc::sdesc_sw128(sbase + QK_LO + kq);
-                const uint64_t b1 = tc::sdesc_sw128(sbase + QK_HI + kC * 128 + kq);
-                const uint64_t b2 = tc::sdesc_sw128(sbase + QK_LO + kC * 128 + kq);
-                tc::mma_f16(tmem + GG, a1, b1, idG, kk > 0);
-                tc::mma_f16(tmem + GG, a1, b2, idG, 1);
-                tc::mma_f16(tmem + GG, a2, b1, idG, 1);
                 const uint32_t shi = tmem + R1 + 8 * kk, slo = tmem + R1 + 64 + 8 * kk;
                 tc::mma_f16_ta(tmem + D1, shi, a1, id128, kk > 0);
                 tc::mma_f16_ta(tmem + D1, shi, a2, id128, 1);
@@ -895,9 +876,9 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 const uint64_t b1 = tc::sdesc(sbase + TT + kk * 256, 128, 1024);
                 const uint64_t b2 = tc::sdesc(sbase + TT + 8192 + kk * 256, 128, 1024);
                 const uint32_t xhi = tmem + R1 + 8 * kk, xlo = tmem + R1 + 32 + 8 * kk;
-                tc::mma_f16_ta(tmem + D2, xhi, b1, idG, kk > 0);
-                tc::mma_f16_ta(tmem + D2, xhi, b2, idG, 1);
-                tc::mma_f16_ta(tmem + D2, xlo, b1, idG, 1);
+                tc::mma_f16_ta(tmem + D2, xhi, b1, id64, kk > 0);
+                tc::mma_f16_ta(tmem + D2, xhi, b2, id64, 1);
+                tc::mma_f16_ta(tmem + D2, xlo, b1, id64, 1);
             }
             tc::mma_commit(bar(B_M2));
             last_commit = B_M2;
@@ -905,7 +886,7 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             return true;
         };
         // S^T += U'^T K (K rows read MN-major), (P U)^T = U^T P^T into D2 (U^T has been
-        // read from it); T of the next chunk
+        // read from it); T of the next chunk (this chunk's T was read by D2's product)
         auto issue_m3 = [&](int c) -> bool {
             const uint32_t par = c & 1;
             if (c + 1 < nch)     // D2 has been read (this warp waited for it): T's buffer is free
@@ -925,9 +906,9 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 const uint64_t p1d = tc::sdesc(sbase + PP + kk * 256, 128, 1024);
                 const uint64_t p2d = tc::sdesc(sbase + PP + 8192 + kk * 256, 128, 1024);
                 const uint32_t uhi = tmem + R1 + 8 * kk, ulo = tmem + R1 + 32 + 8 * kk;
-                tc::mma_f16_ta(tmem + D2, uhi, p1d, idG, kk > 0);
-                tc::mma_f16_ta(tmem + D2, uhi, p2d, idG, 1);
-                tc::mma_f16_ta(tmem + D2, ulo, p1d, idG, 1);
+                tc::mma_f16_ta(tmem + D2, uhi, p1d, id64, kk > 0);
+                tc::mma_f16_ta(tmem + D2, uhi, p2d, id64, 1);
+                tc::mma_f16_ta(tmem + D2, ulo, p1d, id64, 1);
             }
             tc::mma_commit(bar(B_M3));
             last_commit = B_M3;
@@ -937,6 +918,7 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
         if (issuer) {
             issue_raw(0);
             issue_t(0);
+            issue_p(0);
         }
         const int q4 = warp & 3, hf = warp >> 2;
         const int j = 32 * q4 + lane;
@@ -1064,6 +1046,8 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             if (!ok)
                 break;
             tc::fence_after_sync();
+            if (issuer && c + 1 < nch)   // this chunk's P has been read by its product
+                issue_p(c + 1);
             // ---- O^T row j = e^{Gam} (Q S_0)^T + (P U)^T -> token-major staging, scaled by 1/sqrt(d)
             //      (the two terms are added here, rounded, rather than in the accumulator: for a
             //      token whose readout nearly cancels this is the sum that decides its precision)
@@ -1153,6 +1137,8 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 drained &= tc::mbar_wait_ns(bar(B_RAW), raw_last & 1, lim);
             if (t_last >= 0)
                 drained &= tc::mbar_wait_ns(bar(B_T), t_last & 1, lim);
+            if (p_last >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_P), p_last & 1, lim);
             if (!drained)
                 atomicOr(&g_device_error, (int)kErrDrain);
         }

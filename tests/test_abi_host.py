@@ -114,7 +114,7 @@ def test_prefill_workspace_size_and_checks(lib):
     dims = _dims()
     cd, cp = dims.c(), _params().c()
     for T, chunks in ((1, 1), (64, 1), (65, 2), (8192, 128)):
-        assert gdn.prefill_workspace_bytes(dims, T) == 2 * 4 * chunks * 16384
+        assert gdn.prefill_workspace_bytes(dims, T) == 2 * 4 * chunks * 32768
     assert gdn.prefill_workspace_bytes(dims, 0) == 0
     assert gdn.prefill_workspace_bytes(dims, 64, 32) == 0
     need = gdn.prefill_workspace_bytes(dims, 130)
