@@ -391,7 +391,7 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t n_tokens, int32
     if (check_dims(dims, 0) != GDN_OK || n_tokens < 1 || chunk != 64)
         return 0;
     const int64_t n_chunks = ((int64_t)n_tokens + 63) / 64;
-    return (size_t)dims->n_seq * (size_t)dims->n_v_heads * (size_t)n_chunks * gdn::kPrefillChunkImage;
+    return gdn::prefill_workspace_bytes(dims->n_seq, dims->n_qk_heads, dims->n_v_heads, (int)n_chunks);
 }
 
 gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, const void *z,
@@ -461,7 +461,7 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
 }  // extern "C"
 
 namespace {
-constexpr size_t kStaticScratchBytes = (size_t)16 << 20;   // 16 MiB: 512 chunk images
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;   // 16 MiB of prefill workspace
 __device__ __align__(256) uint8_t g_prefill_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;

@@ -71,7 +71,7 @@ struct PrefillArgs {
     const void *x, *z, *alpha, *beta_logit;
     const float *conv_w, *dt, *A_log, *norm_w;
     float *out;            // [B][T][Hv][d]
-    uint8_t *ws;           // [B][Hv][n_chunks] chunk images of (I + A)^-1 and P, 32 KB each
+    uint8_t *ws;           // workspace: chunk images, then [Q; K] images (prefill.cu)
     int64_t x_stride, z_stride, gate_stride;
     int B, Hq, Hv, W, conv_dim, T, n_chunks;
     float l2_eps, rms_eps, scale;
@@ -79,8 +79,15 @@ struct PrefillArgs {
     uint64_t first_wait_ns;  // limit of the chain kernel's first wait
 };
 
-// Bytes of one chunk's images in the prefill workspace: (I + A)^-1 and P.
-constexpr size_t kPrefillChunkImage = 32768;
+// Prefill workspace: per (sequence, V head, chunk) an image of (I + A)^-1, P and
+// the chunk's gates; per (sequence, QK head, chunk) the chunk's normalised Q and
+// K rows as tensor-core operands. All images are 1 KB multiples.
+constexpr size_t kPrefillChunkImage = 34816;
+constexpr size_t kPrefillQKImage = 65536;
+inline size_t prefill_workspace_bytes(int B, int Hq, int Hv, int n_chunks)
+{
+    return (size_t)B * (size_t)n_chunks * ((size_t)Hv * kPrefillChunkImage + (size_t)Hq * kPrefillQKImage);
+}
 
 // Default limit of a bounded wait, and the test-only override of one prefill
 // wait and of the tiled conv's first tile wait (0 = the default).

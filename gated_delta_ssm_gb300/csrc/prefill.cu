@@ -118,31 +118,43 @@ __device__ __forceinline__ float exp_diff(float ah, float al, float bh, float bl
 // 2^e for an integer e in [-126, 127], exactly
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
 
-// One chunk's gate values ("fm_kernel_ssm.h" "Decay gate"; beta = sigmoid).
+// One chunk's gate values ("fm_kernel_ssm.h" "Decay gate"; beta = sigmoid),
+// formed in the chunk-parallel pass and copied whole to the chain pass.
 //
 // The chain keeps the fp32 state master scaled by a power of two, 2^rho S, with
 // rho chosen per chunk from the gates so that the scaled state stays of order
 // one however strongly it has decayed: the fp16 operand parts split from it
-// (and the update U' that adds to it) then stay in fp16's normal range. The
-// factors below fold those exact powers of two in; chunk c enters with rho_c
-// and leaves with rho_{c+1}.
+// (and the update U' that adds to it) then stay in fp16's normal range. Chunk c
+// enters with rho_c and leaves with rho_{c+1} = next_rho(G, rho_c); the chain
+// multiplies the factors below by those exact powers of two (2^-rho_c for eg,
+// bg; 2^rho_{c+1} for egc; 2^(rho_{c+1} - rho_c) for ec).
 struct Gates {
     float beta[kC];        // beta_t, 0 at or past the end of the call
     float gh[kC], gl[kC];  // Gam_t = g_0 + ... + g_t (two floats); g = 0 past the end
-    float eg[kC];          // exp(Gam_t) 2^-rho_c / 16          (scales 16 2^rho_c (Q S_0)^T)
-    float egc[kC];         // exp(Gam_C - Gam_t) 2^rho_{c+1} / 16, 0 past the end  (U' against 16 K)
-    float bg[kC];          // beta_t exp(Gam_t) 2^-rho_c / 16   (scales 16 2^rho_c (K S_0)^T)
-    float ec;              // exp(Gam_C) 2^(rho_{c+1} - rho_c)  (the scaled master's decay)
-    int rho;               // rho_c
-    int rho_next;          // rho_{c+1}
+    float eg[kC];          // exp(Gam_t) / 16                   (scales 16 (Q S_0)^T)
+    float egc[kC];         // exp(Gam_C - Gam_t) / 16, 0 past the end  (U' against 16 K)
+    float bg[kC];          // beta_t exp(Gam_t) / 16            (scales 16 (K S_0)^T)
+    float ec;              // exp(Gam_C)                        (the master's decay)
+    float lc;              // log2 exp(Gam_C)
+    float lu;              // max_t log2(beta_t exp(Gam_C - Gam_t)), -1e30 if no update
     float pad[13];
 };
+static_assert(sizeof(Gates) % 16 == 0, "gates travel by bulk copy");
 
-// Gates of tokens c0 .. c0+n-1 of sequence b, V head h, entering with state
-// scale rho; executed by one warp.
+// rho_{c+1}: with the entering scaled state of order one, the state after the
+// chunk has magnitude about max(e^{Gam_C} 2^-rho_c, max_t beta_t e^{Gam_C - Gam_t})
+// (times the values' scale); lmax is its log2 and rho_{c+1} = -lmax brings it
+// back to order one. Since 2^rho_{c+1} <= 1 / (beta_t e^{Gam_C - Gam_t}), the
+// update factors egc 2^rho_{c+1} stay bounded by 1 / (16 beta_t).
+__device__ __forceinline__ int next_rho(const Gates *G, int rho)
+{
+    const float lmax = fmaxf(G->lc - (float)rho, G->lu);
+    return (int)fminf(fmaxf(floorf(-lmax), 0.0f), 60.0f);
+}
+
+// Gates of tokens c0 .. c0+n-1 of sequence b, V head h; executed by one warp.
 template <typename TIn>
-__device__ __forceinline__ void chunk_gates(const PrefillArgs &a, int b, int h, int c0, int n,
-                                            int rho, Gates *G)
+__device__ __forceinline__ void chunk_gates(const PrefillArgs &a, int b, int h, int c0, int n, Gates *G)
 {
     const int lane = threadIdx.x & 31;
     const float dtv = __ldg(a.dt + h), alog = __ldg(a.A_log + h);
@@ -181,11 +193,6 @@ __device__ __forceinline__ void chunk_gates(const PrefillArgs &a, int b, int h, 
     G->gl[2 * lane] = g0l;
     G->gh[2 * lane + 1] = g1h;
     G->gl[2 * lane + 1] = g1l;
-    // rho_{c+1}: with the entering scaled state of order one, the state after the
-    // chunk has magnitude about max(e^{Gam_C} 2^-rho_c, max_t beta_t e^{Gam_C - Gam_t})
-    // (times the values' scale); lmax is its log2 and rho_{c+1} = -lmax brings it
-    // back to order one. Since 2^rho_{c+1} <= 1 / (beta_t e^{Gam_C - Gam_t}), the
-    // update factors egc below stay bounded by 1 / (16 beta_t).
     const float l2e = 1.4426950408889634f;
     const float dc0 = 2 * lane < n ? exp_diff(gch, gcl, g0h, g0l) : 0.0f;
     const float dc1 = 2 * lane + 1 < n ? exp_diff(gch, gcl, g1h, g1l) : 0.0f;
@@ -197,32 +204,30 @@ __device__ __forceinline__ void chunk_gates(const PrefillArgs &a, int b, int h, 
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1)
         lu = fmaxf(lu, __shfl_xor_sync(0xffffffffu, lu, m));
-    const float lold = __fmul_rn(__fadd_rn(gch, gcl), l2e) - (float)rho;   // old state, in 2^rho units
-    const float lmax = fmaxf(lold, lu);
-    const int rho_next = (int)fminf(fmaxf(floorf(-lmax), 0.0f), 60.0f);
-    const float inv_in = __fmul_rn(exp2i(-rho), kInvQK), up_out = __fmul_rn(exp2i(rho_next), kInvQK);
-    const float e0 = __fmul_rn(exp_diff(g0h, g0l, 0.0f, 0.0f), inv_in);
-    const float e1 = __fmul_rn(exp_diff(g1h, g1l, 0.0f, 0.0f), inv_in);
+    const float e0 = __fmul_rn(exp_diff(g0h, g0l, 0.0f, 0.0f), kInvQK);
+    const float e1 = __fmul_rn(exp_diff(g1h, g1l, 0.0f, 0.0f), kInvQK);
     G->eg[2 * lane] = e0;
     G->eg[2 * lane + 1] = e1;
     G->bg[2 * lane] = __fmul_rn(bv[0], e0);
     G->bg[2 * lane + 1] = __fmul_rn(bv[1], e1);
-    G->egc[2 * lane] = __fmul_rn(dc0, up_out);
-    G->egc[2 * lane + 1] = __fmul_rn(dc1, up_out);
+    G->egc[2 * lane] = __fmul_rn(dc0, kInvQK);
+    G->egc[2 * lane + 1] = __fmul_rn(dc1, kInvQK);
     if (lane == 0) {
-        G->ec = __fmul_rn(exp_diff(gch, gcl, 0.0f, 0.0f), exp2i(rho_next - rho));
-        G->rho = rho;
-        G->rho_next = rho_next;
+        G->ec = exp_diff(gch, gcl, 0.0f, 0.0f);
+        G->lc = __fmul_rn(__fadd_rn(gch, gcl), l2e);
+        G->lu = lu;
     }
 }
 
 // conv + SiLU ("fm_kernel_ssm.h", "Causal depthwise conv1d + SiLU") of the
 // NCH (4 or 8) channels ch0 .. ch0+NCH-1 for tokens t0 .. t0+7 of the chunk that
-// starts at token c0 of the call; tokens at or past n give 0. Stream index
-// s < 0 of the call reads the fp32 history, s >= T reads 0. raw: the chunk's
-// rows of this channel's 128-channel head staged in shared memory
-// ([63 + W][128] bf16, row r = token c0 - (W-1) + r), or nullptr to read x
-// directly. Taps are summed oldest first.
+// starts at token c0 of the call; tokens at or past n give 0. With four taps the
+// weights may come from a table in shared memory (wsm[e * wstride] = channel
+// ch0 + e's taps) instead of global memory. Stream index
+// s < 0 of the call reads the fp32 history, s >= T reads 0. With staged set,
+// raw_s is the shared-window address of the chunk's rows of this channel's
+// 128-channel head ([63 + W][128] bf16, row r = token c0 - (W-1) + r); otherwise
+// x is read directly. Taps are summed oldest first.
 template <int NCH, typename TIn>
 __device__ __forceinline__ void load_row(const TIn *p, float (&v)[NCH]);
 template <>
@@ -233,42 +238,37 @@ __device__ __forceinline__ void load_row<4, __nv_bfloat16>(const __nv_bfloat16 *
     v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xFFFF0000u);
 }
 template <>
-__device__ __forceinline__ void load_row<8, __nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[8])
-{
-    const uint4 u = *reinterpret_cast<const uint4 *>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        v[2 * e] = __uint_as_float(w[e] << 16);
-        v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-    }
-}
-template <>
 __device__ __forceinline__ void load_row<4, float>(const float *p, float (&v)[4])
 {
     const float4 f = *reinterpret_cast<const float4 *>(p);
     v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
 }
-template <>
-__device__ __forceinline__ void load_row<8, float>(const float *p, float (&v)[8])
+
+// Four bf16 channels of a staged row, by shared-window address (a plain shared
+// load: these rows must not queue behind the warp's global traffic). Volatile so
+// that it stays after the wait for the rows' copy.
+__device__ __forceinline__ void lds_row4(uint32_t saddr, float (&v)[4])
 {
-    const float4 f = *reinterpret_cast<const float4 *>(p);
-    const float4 g = *reinterpret_cast<const float4 *>(p + 4);
-    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-    v[4] = g.x; v[5] = g.y; v[6] = g.z; v[7] = g.w;
+    uint32_t x, y;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(saddr));
+    v[0] = __uint_as_float(x << 16); v[1] = __uint_as_float(x & 0xFFFF0000u);
+    v[2] = __uint_as_float(y << 16); v[3] = __uint_as_float(y & 0xFFFF0000u);
 }
 
 template <typename TIn, int WC, int NCH>
 __device__ __forceinline__ void conv_block(const PrefillArgs &a, int b, int c0, int n, int ch0,
-                                           int t0, const __nv_bfloat16 *raw, float (&out)[8][NCH])
+                                           int t0, bool staged, uint32_t raw_s, float (&out)[8][NCH],
+                                           const float4 *wsm = nullptr, int wstride = 0)
 {
+    static_assert(NCH == 4, "staged rows are read four channels per thread");
     const int W = WC > 0 ? WC : a.W;
     constexpr int WM = WC > 0 ? WC : kMaxW;
     float w[NCH][WM];
 #pragma unroll
     for (int e = 0; e < NCH; ++e) {
         if (WC == 4) {
-            const float4 f = __ldg(reinterpret_cast<const float4 *>(a.conv_w + (size_t)(ch0 + e) * 4));
+            const float4 f = wsm != nullptr ? wsm[e * wstride]
+                                            : __ldg(reinterpret_cast<const float4 *>(a.conv_w + (size_t)(ch0 + e) * 4));
             w[e][0] = f.x; w[e][1] = f.y; w[e][2] = f.z; w[e][3 % WM] = f.w;
         } else {
 #pragma unroll
@@ -284,36 +284,50 @@ __device__ __forceinline__ void conv_block(const PrefillArgs &a, int b, int c0, 
     const int s0 = c0 + t0 - (W - 1);              // stream index of row 0 of the window
     const bool inside = s0 >= 0 && s0 + 7 + W - 1 < a.T;   // no history, no tail rows
     const TIn *xb = static_cast<const TIn *>(a.x) + ((int64_t)b * a.T + s0) * a.x_stride + ch0;
-    const __nv_bfloat16 *rb = raw != nullptr ? raw + t0 * kD + (ch0 & (kD - 1)) : nullptr;
+    const uint32_t rb = raw_s + (uint32_t)(t0 * kD + (ch0 & (kD - 1))) * 2u;
     const float *hist = a.conv_state + ((size_t)b * a.conv_dim + ch0) * (W - 1);
-#pragma unroll
-    for (int rr = 0; rr < 7 + WM; ++rr) {
-        if (WC == 0 && rr >= 7 + W)
-            break;
-        float v[NCH];
-        const int s = s0 + rr;
-        if (inside || (s >= 0 && s < a.T)) {
-            if (rb != nullptr)
-                load_row<NCH, __nv_bfloat16>(rb + rr * kD, v);
-            else
-                load_row<NCH, TIn>(xb + (int64_t)rr * a.x_stride, v);
-        } else if (s < 0) {
-#pragma unroll
-            for (int e = 0; e < NCH; ++e)
-                v[e] = hist[(size_t)e * (W - 1) + (W - 1 + s)];
-        } else {
-#pragma unroll
-            for (int e = 0; e < NCH; ++e)
-                v[e] = 0.0f;
-        }
+    // row rr of the window feeds tap rr - t of token t
+    auto add_row = [&](int rr, const float (&v)[NCH]) {
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            const int tau = rr - t;               // tap that row rr feeds for token t
+            const int tau = rr - t;
             if (tau >= 0 && tau < WM && (WC > 0 || tau < W)) {
 #pragma unroll
                 for (int e = 0; e < NCH; ++e)
                     out[t][e] = __fmaf_rn(v[e], w[e][tau], out[t][e]);
             }
+        }
+    };
+    if (WC > 0 && staged && inside) {
+        // every row of the window is a staged row: no branch between the loads and the sums
+#pragma unroll
+        for (int rr = 0; rr < 7 + WM; ++rr) {
+            float v[NCH];
+            lds_row4(rb + (uint32_t)(rr * kD * 2), v);
+            add_row(rr, v);
+        }
+    } else {
+#pragma unroll
+        for (int rr = 0; rr < 7 + WM; ++rr) {
+            if (WC == 0 && rr >= 7 + W)
+                break;
+            float v[NCH];
+            const int s = s0 + rr;
+            if (s >= 0 && s < a.T) {
+                if (staged)
+                    lds_row4(rb + (uint32_t)(rr * kD * 2), v);
+                else
+                    load_row<NCH, TIn>(xb + (int64_t)rr * a.x_stride, v);
+            } else if (s < 0) {
+#pragma unroll
+                for (int e = 0; e < NCH; ++e)
+                    v[e] = hist[(size_t)e * (W - 1) + (W - 1 + s)];
+            } else {
+#pragma unroll
+                for (int e = 0; e < NCH; ++e)
+                    v[e] = 0.0f;
+            }
+            add_row(rr, v);
         }
     }
 #pragma unroll
@@ -404,10 +418,22 @@ static_assert(QK % 1024 == 0, "swizzled tiles on 1 KB boundaries");
 __device__ __forceinline__ int a_idx(int t, int s) { return t * kC + ((((s >> 2) ^ (t & 15))) << 2) + (s & 3); }
 
 // One chunk's image in the workspace: T = (I + A)^-1 then P, each as two fp16
-// parts of a [64][64] K-major core-matrix tile (8 KB per part).
+// parts of a [64][64] K-major core-matrix tile (8 KB per part), then the gates.
+constexpr uint32_t kImgP = 16384, kImgGates = 32768;
+static_assert(kImgGates + sizeof(Gates) <= kPrefillChunkImage, "chunk image layout");
 __device__ __forceinline__ uint8_t *chunk_image(const PrefillArgs &a, int b, int h, int c)
 {
     return a.ws + (((size_t)b * a.Hv + h) * a.n_chunks + c) * kPrefillChunkImage;
+}
+
+// The chunk's normalised Q rows then K rows of QK head hk (scaled by 16), each
+// as two fp16 parts (16 KB each) of a [64 t][128 i] 128-byte-swizzled K-major
+// tile: the chain pass copies them into shared memory as they are.
+constexpr uint32_t kQKPart = 16384, kQKRows = 2 * kQKPart;
+__device__ __forceinline__ uint8_t *qk_image(const PrefillArgs &a, int b, int hk, int c)
+{
+    return a.ws + (size_t)a.B * a.Hv * a.n_chunks * kPrefillChunkImage +
+           (((size_t)b * a.Hq + hk) * a.n_chunks + c) * kPrefillQKImage;
 }
 
 template <typename TIn, int WC>
@@ -453,9 +479,8 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
 #pragma unroll 1
         for (int part = 0; part < 2; ++part) {
             float v[8][4];
-            const __nv_bfloat16 *raw =
-                staged ? reinterpret_cast<const __nv_bfloat16 *>(smem + (part ? p1::RAWK : p1::RAWQ)) : nullptr;
-            conv_block<TIn, WC, 4>(a, b, c0, n, (part ? a.Hq * kD : 0) + hk * kD + 4 * lane, 8 * warp, raw, v);
+            conv_block<TIn, WC, 4>(a, b, c0, n, (part ? a.Hq * kD : 0) + hk * kD + 4 * lane, 8 * warp,
+                                   staged != 0, sbase + (part ? p1::RAWK : p1::RAWQ), v);
             l2_rows<4>(v, a.l2_eps, kQK);
             store_rows_split<4>(smem + p1::QK, smem + p1::QK_LO, part * kC + 8 * warp, 2 * kC, lane, v);
         }
@@ -471,6 +496,17 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
     // G = [Q; K] K^T: rows 0..63 give Q K^T (for P), rows 64..127 K K^T (for A)
     const bool mma_issued = ok;
     if (ok && tid == 0) {
+        // the chain pass's Q and K operands: rows 0..63 / 64..127 of each 8 KB column
+        // block of the tile are the two column blocks of a 64-row tile (the swizzle
+        // depends on the row within its 8-row group only)
+        uint8_t *img = qk_image(a, b, hk, c);
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {
+            const int p = i >> 2, s = (i >> 1) & 1, cb = i & 1;
+            tc::bulk_copy_s2g(img + p * kQKRows + s * kQKPart + cb * 8192,
+                              sbase + p1::QK + s * 32768 + cb * 16384 + p * 8192, 8192);
+        }
+        tc::bulk_commit();
         const uint32_t id = tc::idesc_f16(128, 64);
 #pragma unroll 1
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -489,6 +525,8 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
         atomicOr(const_cast<int *>(abort), (int)kErrUT);
         ok = false;
     }
+    if (mma_issued && tid == 0)
+        tc::bulk_wait_read();    // the tile's region is overwritten below
     tc::fence_after_sync();
     __syncthreads();
     ok = *abort == 0;
@@ -501,8 +539,16 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
 #pragma unroll 1
     for (int hp = 0; ok && hp < r; hp += 2) {
         if (warp < 2 && hp + warp < r)
-            chunk_gates<TIn>(a, b, hk * r + hp + warp, c0, n, 0, gates + warp);
+            chunk_gates<TIn>(a, b, hk * r + hp + warp, c0, n, gates + warp);
+        tc::fence_smem_to_async();
         __syncthreads();
+        if (tid == 0) {      // the gates travel with the chunk's image
+#pragma unroll 1
+            for (int u = 0; u < 2 && hp + u < r; ++u)
+                tc::bulk_copy_s2g(chunk_image(a, b, hk * r + hp + u, c) + kImgGates,
+                                  sbase + p1::GATES + u * (uint32_t)sizeof(Gates), sizeof(Gates));
+            tc::bulk_commit();
+        }
         const int hh = hp + hsel;
         // ---- P (TMEM lanes 0..63, the Q rows: warps 0, 1, 4, 5) and A (lanes 64..127, the
         //      K rows: warps 2, 3, 6, 7) of the pair's two heads, one token row per thread
@@ -512,7 +558,7 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
             const bool is_a = q4 >= 2;
             const float gt = G->gh[t], gtl = G->gl[t];
             const float rowf = is_a ? __fmul_rn(G->beta[t], kInvQK2) : kInvQK2;
-            uint8_t *pimg = chunk_image(a, b, hk * r + hh, c) + 16384;
+            uint8_t *pimg = chunk_image(a, b, hk * r + hh, c) + kImgP;
             float *A = Am + hsel * kC * kC;
             const int tmax = 32 * (q4 & 1) + 31;              // largest row of this warp
 #pragma unroll 1
@@ -629,9 +675,13 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
                 *reinterpret_cast<uint4 *>(img + 8192 + 16 * p) = lo;
             }
         }
+        if (tid == 0)
+            tc::bulk_wait_read();    // the gates' buffers are rewritten by the next pair
         __syncthreads();
     }
 
+    if (tid == 0)
+        tc::bulk_wait();             // the workspace copies are complete before the CTA ends
     if (tid == 0 && *abort) {
         atomicOr(&g_device_error, *abort);
         // the staged-row copy and the product may still be in flight
@@ -647,22 +697,30 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
 // ================================================================== pass 2
 namespace p2 {
 constexpr int kThreads = 512;                     // 8 epilogue warps (warp 0 also issues), 8 conv warps
-constexpr uint32_t QK_HI = 0, QK_LO = 32768;      // [Q; K] two parts, [128 t'][128 i] sw128
-constexpr uint32_t VF = 65536;                    // V^T fp32 footprint [128 j][64 t]
-constexpr uint32_t TT = 98304;                    // T image of the current chunk (16 KB)
-constexpr uint32_t PP = 114688;                   // P image of the current chunk (16 KB)
-constexpr uint32_t OS = 131072;                   // O staging, fp32 [64 t][128 j]
-constexpr uint32_t RAW = 163840;                  // staged rows: Q, K, V heads
-constexpr uint32_t GATES = RAW + 3 * kRawBox;     // two Gates buffers
+constexpr uint32_t QB = 0;                        // Q rows of the chunk: two parts, [64 t][128 i] sw128
+constexpr uint32_t KB = 32768;                    // K rows, two buffers (even and odd chunks)
+constexpr uint32_t VF = 98304;                    // V^T fp32 footprint [128 j][64 t]
+constexpr uint32_t TT = 131072;                   // T image of the current chunk (16 KB)
+constexpr uint32_t PP = 147456;                   // P image of the current chunk (16 KB)
+constexpr uint32_t OS = 163840;                   // O staging, fp32 [64 t][128 j]
+constexpr uint32_t RAW = 196608;                  // staged rows of the V head
+constexpr uint32_t GATES = RAW + kRawBox;         // two Gates buffers (even and odd chunks)
 constexpr uint32_t MBAR = GATES + 2 * sizeof(Gates);
-constexpr uint32_t SLOT = MBAR + 16 * 8;          // TMEM base, abort word
-constexpr uint32_t BYTES = SLOT + 16 + 1024;
+constexpr uint32_t SLOT = MBAR + 24 * 8;          // TMEM base, abort word
+constexpr uint32_t CONVW = SLOT + 16;             // 4-tap conv weights of the V head
+constexpr uint32_t BYTES = CONVW + kD * 16 + 1024;
 static_assert(BYTES <= 232448, "shared memory budget");
-static_assert(RAW % 1024 == 0 && kRawBox % 1024 == 0, "staged rows on 1 KB boundaries");
-// barriers
-enum { B_RAW, B_T, B_M1, B_M2, B_M3, B_QK, B_P, B_ST, B_X, B_U, B_V, B_RAWFREE, B_OS, B_N };
-// TMEM columns
-constexpr uint32_t TS = 0, D1 = 128, R1 = 256, D2 = 448;
+static_assert(RAW % 1024 == 0 && KB % 1024 == 0, "tiles on 1 KB boundaries");
+// barriers: copies (expected bytes), products (commits), and role hand-offs
+enum { B_Q, B_K0, B_K1, B_T, B_P, B_RAW, B_M1, B_M1Q, B_M2, B_M3, B_PU,
+       B_RAWFREE, B_V, B_OSFREE,       // 256 conv threads arrive
+       B_ST, B_X, B_U, B_OR, B_OS,     // 256 epilogue threads arrive
+       B_N };
+static_assert(B_N <= 24, "barrier slots");
+// TMEM columns: TS the fp32 state master (S^T), D1 = [(Q S_0)^T | (K S_0)^T], R1 the
+// S_0^T operand (two fp16 parts; the low part's columns later hold U'^T), XU the
+// X^T, then U^T operand (two parts), D2 = U^T, then (P U)^T
+constexpr uint32_t TS = 0, D1 = 128, R1 = 256, XU = 384, D2 = 448;
 }  // namespace p2
 
 // fp32 V^T footprint: float4 q (tokens 4q .. 4q+3) of value row j; the 16-byte
@@ -690,6 +748,24 @@ __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]
 
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 
+// Four gate values of a norm row held as loaded (raw bits), so that a load issued
+// early is waited for only where the values are used.
+template <typename T> struct ZRaw;
+template <> struct ZRaw<__nv_bfloat16> {
+    uint2 u;
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p) { u = __ldcs(reinterpret_cast<const uint2 *>(p)); }
+    __device__ __forceinline__ void get(float (&v)[4]) const
+    {
+        v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    }
+};
+template <> struct ZRaw<float> {
+    float4 f;
+    __device__ __forceinline__ void load(const float *p) { f = __ldcs(reinterpret_cast<const float4 *>(p)); }
+    __device__ __forceinline__ void get(float (&v)[4]) const { v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w; }
+};
+
 template <typename TIn, int WC>
 __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                       PrefillArgs a, int staged, int zvec)
@@ -707,12 +783,12 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
     auto bar = [&](int i) { return mb + 8u * (uint32_t)i; };
     volatile int *abort = reinterpret_cast<volatile int *>(smem + SLOT + 4);
     Gates *gbuf = reinterpret_cast<Gates *>(smem + GATES);
+    float *Os = reinterpret_cast<float *>(smem + OS);
     const uint64_t lim = a.wait_ns;
 
     if (tid == 0) {
-        const uint32_t counts[B_N] = {1, 1, 1, 1, 1, 256, 1, 256, 256, 256, 256, 256, 256};
         for (int i = 0; i < B_N; ++i)
-            tc::mbar_init(bar(i), counts[i]);
+            tc::mbar_init(bar(i), i < B_RAWFREE ? 1 : 256);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -732,191 +808,290 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
     };
 
     if (warp >= 8) {
-        // ============================================ conv warps: chunk c+1's rows, chunk c's P
+        // ============================================ conv warps: chunk c's V rows, chunk c-1's norm
         const int cw = warp - 8;
-        const __nv_bfloat16 *raw = staged ? reinterpret_cast<const __nv_bfloat16 *>(smem + RAW) : nullptr;
-        // Q / K rows: 8 tokens x 8 channels per thread (warps 0-3 of the group: Q, 4-7: K)
-        const int qk_part = cw >> 2, qk_tb = 2 * (cw & 3) + (lane >> 4), qk_g = lane & 15;
-        const int qk_ch = (qk_part ? a.Hq * kD : 0) + hk * kD + 8 * qk_g;
-        const __nv_bfloat16 *qk_raw = raw != nullptr ? raw + qk_part * (kRawBox / 2) : nullptr;
-        // V rows: 8 tokens x 4 channels per thread
-        const int v_ch = 2 * a.Hq * kD + h * kD + 4 * lane;
-        const __nv_bfloat16 *v_raw = raw != nullptr ? raw + 2 * (kRawBox / 2) : nullptr;
-
-        auto v_conv = [&](int c0, int n) {
-            float v[8][4];
-            conv_block<TIn, WC, 4>(a, b, c0, n, v_ch, 8 * cw, v_raw, v);
-            return [=](uint8_t *sm) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = 4 * lane + e;
-#pragma unroll
-                    for (int q = 0; q < 2; ++q)
-                        *reinterpret_cast<float4 *>(sm + foot_off(j, 2 * cw + q)) =
-                            make_float4(v[4 * q][e], v[4 * q + 1][e], v[4 * q + 2][e], v[4 * q + 3][e]);
-                }
-            };
-        };
-
-        // prologue: chunk 0
-        bool ok = waitb(B_RAW, 0, lim);
-        if (ok) {
-            const int n0 = min(kC, a.T);
-            if (warp == 15)
-                chunk_gates<TIn>(a, b, h, 0, n0, 0, gbuf);
-            v_conv(0, n0)(smem);
-            float v[8][8];
-            conv_block<TIn, WC, 8>(a, b, 0, n0, qk_ch, 8 * qk_tb, qk_raw, v);
-            l2_rows<8>(v, a.l2_eps, kQK);
-            store_rows_split<8>(smem + QK_HI, smem + QK_LO, qk_part * kC + 8 * qk_tb, 2 * kC, qk_g, v);
-        }
-        tc::mbar_arrive(bar(B_RAWFREE));
-        tc::fence_smem_to_async();
-        tc::mbar_arrive(bar(B_QK));
-        tc::mbar_arrive(bar(B_V));
-#pragma unroll 1
-        for (int c = 0; ok && c < nch; ++c) {
-            const uint32_t par = c & 1;
-            const int c0 = c * kC, n = min(kC, a.T - c0);
-            if (c + 1 >= nch)
-                break;
-            // ---- chunk c+1: gates, V rows (once chunk c's X has read V), Q rows, K rows
-            const int c1 = c0 + kC, n1 = min(kC, a.T - c1);
-            ok = waitb(B_RAW, (c + 1) & 1, lim);
-            if (!ok)
-                break;
-            if (warp == 15) {
-                __syncwarp();   // lane 0 wrote the previous chunk's rho_next
-                chunk_gates<TIn>(a, b, h, c1, n1, gbuf[c & 1].rho_next, gbuf + ((c + 1) & 1));
-            }
-            auto write_v = v_conv(c1, n1);
-            ok = waitb(B_X, par, lim);
-            if (!ok)
-                break;
-            write_v(smem);
-            tc::mbar_arrive(bar(B_V));
-            float v[8][8];
-            conv_block<TIn, WC, 8>(a, b, c1, n1, qk_ch, 8 * qk_tb, qk_raw, v);
-            l2_rows<8>(v, a.l2_eps, kQK);
-            tc::mbar_arrive(bar(B_RAWFREE));
-            // Q rows are free once this chunk's D1 product is done, K rows once its state
-            // update is
-            ok = qk_part == 0 ? waitb(B_M1, par, lim) : waitb(B_M3, par, lim);
-            if (!ok)
-                break;
-            store_rows_split<8>(smem + QK_HI, smem + QK_LO, qk_part * kC + 8 * qk_tb, 2 * kC, qk_g, v);
-            tc::fence_smem_to_async();
-            tc::mbar_arrive(bar(B_QK));
-        }
-    } else {
-        // ============================================ epilogue warps: value row j
-        // Lane 0 of warp 0 also issues every copy and tensor-core product, at the
-        // points of its own program where their inputs are ready.
-        const bool issuer = tid == 0;
-        int raw_last = -1, t_last = -1, p_last = -1, last_commit = -1;
-        uint32_t last_phase = 0;
-        const uint32_t raw_bytes = 3u * (uint32_t)(kC + W - 1) * kD * 2;
+        const bool raw_issuer = tid == 256;
+        int raw_last = -1;
         auto issue_raw = [&](int cc) {
-            if (staged) {
-                tc::mbar_expect_tx(bar(B_RAW), raw_bytes);
-                const int row = cc * kC - (W - 1);
-                rows_copy(&xmap, sbase + RAW, bar(B_RAW), hk * kD, row, b);
-                rows_copy(&xmap, sbase + RAW + kRawBox, bar(B_RAW), a.Hq * kD + hk * kD, row, b);
-                rows_copy(&xmap, sbase + RAW + 2 * kRawBox, bar(B_RAW), 2 * a.Hq * kD + h * kD, row, b);
-            } else {
-                tc::mbar_arrive(bar(B_RAW));
-            }
+            tc::mbar_expect_tx(bar(B_RAW), (uint32_t)(kC + W - 1) * kD * 2);
+            rows_copy(&xmap, sbase + RAW, bar(B_RAW), 2 * a.Hq * kD + h * kD, cc * kC - (W - 1), b);
             raw_last = cc;
         };
-        auto issue_t = [&](int cc) {     // T image of chunk cc
-            tc::mbar_expect_tx(bar(B_T), 16384u);
-            tc::bulk_copy_g2s(sbase + TT, chunk_image(a, b, h, cc), 16384u, bar(B_T));
+        if (staged && raw_issuer)
+            issue_raw(0);
+        // V rows: 8 tokens (8 cw ..) x 4 channels (4 lane ..) per thread; 4-tap weights
+        // read once, channel 4 l + e at float4 [e][l] so that a warp's reads of one e
+        // are consecutive
+        const int v_ch = 2 * a.Hq * kD + h * kD + 4 * lane;
+        const float4 *v_w = nullptr;
+        if (WC == 4) {
+            float4 *tab = reinterpret_cast<float4 *>(smem + CONVW);
+            for (int i = tid - 256; i < kD; i += 256)
+                tab[i] = __ldg(reinterpret_cast<const float4 *>(a.conv_w + (size_t)(v_ch - 4 * lane + 4 * (i & 31) + (i >> 5)) * 4));
+            asm volatile("bar.sync 1, 256;" ::: "memory");   // the conv warps only
+            v_w = tab + lane;
+        }
+        // gated-norm mapping: warp cw handles tokens cw, cw + 8, ...; lane holds channels 4 lane .. +3
+        const float4 nw4 = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane);
+        ZRaw<TIn> zpre[8];
+        auto z_rows = [&](int cc) {
+            return static_cast<const TIn *>(a.z) + ((int64_t)b * a.T + (int64_t)cc * kC) * a.z_stride +
+                   (int64_t)h * kD + 4 * lane;
+        };
+        // this warp's gate rows of chunk cc: brought into L2 early (a prefetch holds no
+        // register, so nothing waits on it), loaded into registers once the V rows are out
+        auto z_prefetch = [&](int cc) {
+            const int n = min(kC, a.T - cc * kC);
+            const TIn *zb = z_rows(cc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (cw + 8 * i < n)
+                    asm volatile("prefetch.global.L2 [%0];" :: "l"(zb + (int64_t)(cw + 8 * i) * a.z_stride));
+        };
+        auto z_fetch = [&](int cc) {
+            if (!zvec)
+                return;
+            const int n = min(kC, a.T - cc * kC);
+            const TIn *zb = z_rows(cc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (cw + 8 * i < n)
+                    zpre[i].load(zb + (int64_t)(cw + 8 * i) * a.z_stride);
+        };
+        // ---- gated RMSNorm ("fm_kernel_ssm.h", "Gated RMSNorm") of chunk cc's staged rows
+        auto norm = [&](int cc) {
+            const int c0 = cc * kC, n = min(kC, a.T - c0);
+            const TIn *zb = z_rows(cc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = cw + 8 * i;
+                if (t >= n)
+                    break;
+                const float4 y = *reinterpret_cast<const float4 *>(Os + t * kD + 4 * lane);
+                float ss = __fmul_rn(y.x, y.x);
+                ss = __fmaf_rn(y.y, y.y, ss);
+                ss = __fmaf_rn(y.z, y.z, ss);
+                ss = __fmaf_rn(y.w, y.w, ss);
+                ss = warp_sum32(ss);
+                const float inv = rsqrtf(__fadd_rn(__fmul_rn(ss, 1.0f / kD), a.rms_eps));
+                float zv[4];
+                if (zvec) {
+                    zpre[i].get(zv);
+                } else {
+                    const TIn *zr = zb + (int64_t)t * a.z_stride;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        zv[e] = load_act<TIn>(zr + e);
+                }
+                float4 o;
+                o.x = gated_out(y.x, inv, nw4.x, zv[0]);
+                o.y = gated_out(y.y, inv, nw4.y, zv[1]);
+                o.z = gated_out(y.z, inv, nw4.z, zv[2]);
+                o.w = gated_out(y.w, inv, nw4.w, zv[3]);
+                const int64_t row = (int64_t)b * a.T + c0 + t;
+                *reinterpret_cast<float4 *>(a.out + (row * a.Hv + h) * kD + 4 * lane) = o;
+            }
+        };
+        bool ok = true;
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+            const int c0 = c * kC, n = min(kC, a.T - c0);
+            if (c > 0)
+                z_prefetch(c - 1);
+            if (staged && !(ok = waitb(B_RAW, c & 1, lim)))
+                break;
+            float v[8][4];
+            conv_block<TIn, WC, 4>(a, b, c0, n, v_ch, 8 * cw, staged != 0, sbase + RAW, v, v_w, 32);
+            if (staged && c + 1 < nch) {
+                // the staged rows are read: the next chunk's may come in. The issuer's whole
+                // warp waits, so that the warp stays converged for the work after it.
+                tc::mbar_arrive(bar(B_RAWFREE));
+                if (cw == 0) {
+                    if ((ok = waitb(B_RAWFREE, c & 1, lim)) && raw_issuer)
+                        issue_raw(c + 1);
+                    __syncwarp();
+                }
+                if (!ok)
+                    break;
+            }
+            // V^T of chunk c, once chunk c-1's X has read the footprint
+            if (c > 0 && !(ok = waitb(B_X, (c - 1) & 1, lim)))
+                break;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = 4 * lane + e;
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    *reinterpret_cast<float4 *>(smem + foot_off(j, 2 * cw + q)) =
+                        make_float4(v[4 * q][e], v[4 * q + 1][e], v[4 * q + 2][e], v[4 * q + 3][e]);
+            }
+            tc::mbar_arrive(bar(B_V));
+            // the norm of chunk c-1, whose rows the epilogue has staged
+            if (c > 0) {
+                z_fetch(c - 1);
+                if (!(ok = waitb(B_OS, (c - 1) & 1, lim)))
+                    break;
+                norm(c - 1);
+                tc::mbar_arrive(bar(B_OSFREE));
+            }
+        }
+        if (ok && nch > 0) {
+            z_fetch(nch - 1);
+            if ((ok = waitb(B_OS, (nch - 1) & 1, lim)))
+                norm(nch - 1);
+        }
+        // drain: the staged-row copy in flight lands before the CTA ends
+        if (raw_issuer && raw_last >= 0 && !tc::mbar_wait_ns(bar(B_RAW), raw_last & 1, lim))
+            atomicOr(&g_device_error, (int)kErrDrain);
+    } else {
+        // ============================================ epilogue warps: value row j
+        // Lane 0 of warp 0 also issues every workspace copy and tensor-core product,
+        // at the points of its own program where their inputs are ready. The products
+        // the next chunk waits for (K S_0, U = T X, the state update) are issued apart
+        // from those only the readout needs ((Q S_0)^T, (P U)^T), which run on the
+        // tensor core while the epilogue works.
+        const bool issuer = tid == 0;
+        int q_last = -1, k_last0 = -1, k_last1 = -1, t_last = -1, p_last = -1, last_commit = -1;
+        uint32_t last_phase = 0;
+        auto issue_q = [&](int cc) {     // Q rows of chunk cc
+            tc::mbar_expect_tx(bar(B_Q), kQKRows);
+            tc::bulk_copy_g2s(sbase + QB, qk_image(a, b, hk, cc), kQKRows, bar(B_Q));
+            q_last = cc;
+        };
+        auto issue_k = [&](int cc) {     // K rows of chunk cc, into the buffer of its parity
+            const int kb = cc & 1;
+            tc::mbar_expect_tx(bar(B_K0 + kb), kQKRows);
+            tc::bulk_copy_g2s(sbase + KB + kb * kQKRows, qk_image(a, b, hk, cc) + kQKRows, kQKRows,
+                              bar(B_K0 + kb));
+            (kb ? k_last1 : k_last0) = cc;
+        };
+        auto issue_t = [&](int cc) {     // T image and gates of chunk cc
+            const uint8_t *img = chunk_image(a, b, h, cc);
+            tc::mbar_expect_tx(bar(B_T), 16384u + (uint32_t)sizeof(Gates));
+            tc::bulk_copy_g2s(sbase + TT, img, 16384u, bar(B_T));
+            tc::bulk_copy_g2s(sbase + GATES + (cc & 1) * (uint32_t)sizeof(Gates), img + kImgGates,
+                              (uint32_t)sizeof(Gates), bar(B_T));
             t_last = cc;
         };
         auto issue_p = [&](int cc) {     // P image of chunk cc
             tc::mbar_expect_tx(bar(B_P), 16384u);
-            tc::bulk_copy_g2s(sbase + PP, chunk_image(a, b, h, cc) + 16384, 16384u, bar(B_P));
+            tc::bulk_copy_g2s(sbase + PP, chunk_image(a, b, h, cc) + kImgP, 16384u, bar(B_P));
             p_last = cc;
         };
-        const uint32_t id64 = tc::idesc_f16(128, 64), id128 = tc::idesc_f16(128, 128);
-        // D1 = S_0^T [Q; K]^T, once the [Q; K] tile and S_0^T are ready
-        auto issue_m1 = [&](int c) -> bool {
-            const uint32_t par = c & 1;
+        auto commit = [&](int i, int c) {   // a commit tracks every product issued before it
+            tc::mma_commit(bar(i));
+            last_commit = i;
+            last_phase = c & 1;
+        };
+        const uint32_t id64 = tc::idesc_f16(128, 64);
+        const uint32_t id128 = tc::idesc_f16(128, 128);
+        // D1[:, 64..127] = S_0^T K^T, once the K rows and S_0^T are ready
+        auto issue_m1k = [&](int c) -> bool {
+            const int kb = c & 1;
             // the first wait of the kernel takes its limit from first_wait_ns (a test hook)
-            if (!waitb(B_RAWFREE, par, c == 0 ? a.first_wait_ns : lim))
-                return false;
-            if (c + 1 < nch)     // the staged rows are free since chunk c's conv: fetch chunk c+1's
-                issue_raw(c + 1);
-            if (!waitb(B_QK, par, lim) || !waitb(B_ST, par, lim))
+            if (!waitb(B_K0 + kb, (c >> 1) & 1, c == 0 ? a.first_wait_ns : lim) || !waitb(B_ST, c & 1, lim))
                 return false;
             tc::fence_after_sync();
-#pragma unroll 1
+            const uint32_t kt = sbase + KB + kb * kQKRows;
+#pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
-                const uint32_t kq = (kk >> 2) * (2 * kC * 128) + (kk & 3) * 32;
-                const uint64_t a1 = tc::sdesc_sw128(sbase + QK_HI + kq);
-                const uint64_t a2 = tc::sdesc_sw128(sbase + QK_LO + kq);
+                const uint32_t ko = (kk >> 2) * 8192 + (kk & 3) * 32;   // column block, 16 channels
                 const uint32_t shi = tmem + R1 + 8 * kk, slo = tmem + R1 + 64 + 8 * kk;
-                tc::mma_f16_ta(tmem + D1, shi, a1, id128, kk > 0);
-                tc::mma_f16_ta(tmem + D1, shi, a2, id128, 1);
-                tc::mma_f16_ta(tmem + D1, slo, a1, id128, 1);
+                const uint64_t k1 = tc::sdesc_sw128(kt + ko), k2 = tc::sdesc_sw128(kt + kQKPart + ko);
+                tc::mma_f16_ta(tmem + D1 + kC, shi, k1, id64, kk > 0);
+                tc::mma_f16_ta(tmem + D1 + kC, shi, k2, id64, 1);
+                tc::mma_f16_ta(tmem + D1 + kC, slo, k1, id64, 1);
             }
-            tc::mma_commit(bar(B_M1));
-            last_commit = B_M1;
-            last_phase = par;
+            commit(B_M1, c);
             return true;
         };
-        // D2 = X^T T^T, once every value row's X^T is in TMEM and T has arrived
-        auto issue_m2 = [&](int c) -> bool {
-            const uint32_t par = c & 1;
-            if (!waitb(B_X, par, lim) || !waitb(B_T, par, lim))
+        // D1[:, 0..63] = S_0^T Q^T, once the Q rows are in and the previous chunk's readout
+        // has read these columns
+        auto issue_m1q = [&](int c) -> bool {
+            if ((c > 0 && !waitb(B_OR, (c - 1) & 1, lim)) || !waitb(B_Q, c & 1, lim))
                 return false;
             tc::fence_after_sync();
-#pragma unroll 1
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint32_t ko = (kk >> 2) * 8192 + (kk & 3) * 32;
+                const uint32_t shi = tmem + R1 + 8 * kk, slo = tmem + R1 + 64 + 8 * kk;
+                const uint64_t q1 = tc::sdesc_sw128(sbase + QB + ko), q2 = tc::sdesc_sw128(sbase + QB + kQKPart + ko);
+                tc::mma_f16_ta(tmem + D1, shi, q1, id64, kk > 0);
+                tc::mma_f16_ta(tmem + D1, shi, q2, id64, 1);
+                tc::mma_f16_ta(tmem + D1, slo, q1, id64, 1);
+            }
+            commit(B_M1Q, c);
+            return true;
+        };
+        // D2 = X^T T^T, once every value row's X^T is in TMEM and T has arrived; the Q rows
+        // of the next chunk once this chunk's (Q S_0)^T has read them (that product also
+        // has to finish before U'^T overwrites the low part of S_0^T)
+        auto issue_m2 = [&](int c) -> bool {
+            if (!waitb(B_X, c & 1, lim) || !waitb(B_T, c & 1, lim) || !waitb(B_M1Q, c & 1, lim))
+                return false;
+            tc::fence_after_sync();
+            if (c + 1 < nch)
+                issue_q(c + 1);
+#pragma unroll
             for (int kk = 0; kk < kC / 16; ++kk) {
                 const uint64_t b1 = tc::sdesc(sbase + TT + kk * 256, 128, 1024);
                 const uint64_t b2 = tc::sdesc(sbase + TT + 8192 + kk * 256, 128, 1024);
-                const uint32_t xhi = tmem + R1 + 8 * kk, xlo = tmem + R1 + 32 + 8 * kk;
+                const uint32_t xhi = tmem + XU + 8 * kk, xlo = tmem + XU + 32 + 8 * kk;
                 tc::mma_f16_ta(tmem + D2, xhi, b1, id64, kk > 0);
                 tc::mma_f16_ta(tmem + D2, xhi, b2, id64, 1);
                 tc::mma_f16_ta(tmem + D2, xlo, b1, id64, 1);
             }
-            tc::mma_commit(bar(B_M2));
-            last_commit = B_M2;
-            last_phase = par;
+            commit(B_M2, c);
             return true;
         };
-        // S^T += U'^T K (K rows read MN-major), (P U)^T = U^T P^T into D2 (U^T has been
-        // read from it); T of the next chunk (this chunk's T was read by D2's product)
+        // S^T += U'^T K (K rows read MN-major), then (P U)^T = U^T P^T into D2 (U^T has been
+        // read from it); T and gates of the next chunk first (this chunk's T was read by
+        // D2's product, and its gates' buffer last served chunk c-1)
         auto issue_m3 = [&](int c) -> bool {
-            const uint32_t par = c & 1;
-            if (c + 1 < nch)     // D2 has been read (this warp waited for it): T's buffer is free
+            if (c + 1 < nch)
                 issue_t(c + 1);
-            if (!waitb(B_U, par, lim) || !waitb(B_P, par, lim))
+            if (!waitb(B_U, c & 1, lim) || !waitb(B_P, c & 1, lim))
                 return false;
             tc::fence_after_sync();
-#pragma unroll 1
+            const uint32_t kt = sbase + KB + (c & 1) * kQKRows;
+#pragma unroll
             for (int kk = 0; kk < kC / 16; ++kk) {
-                const uint32_t koff = kC * 128 + kk * 2048;    // K rows 16kk.. : 8-row groups 1 KB apart
-                const uint64_t k1 = tc::sdesc_sw128_mn(sbase + QK_HI + koff, 2 * kC * 128, 1024);
-                const uint64_t k2 = tc::sdesc_sw128_mn(sbase + QK_LO + koff, 2 * kC * 128, 1024);
+                const uint32_t koff = kk * 2048;    // K rows 16kk.. : 8-row groups 1 KB apart
+                const uint64_t k1 = tc::sdesc_sw128_mn(kt + koff, 8192, 1024);
+                const uint64_t k2 = tc::sdesc_sw128_mn(kt + kQKPart + koff, 8192, 1024);
                 const uint32_t uphi = tmem + R1 + 64 + 8 * kk, uplo = tmem + R1 + 96 + 8 * kk;
                 tc::mma_f16_ta(tmem + TS, uphi, k1, id128 | tc::kIdescTransB, 1);
                 tc::mma_f16_ta(tmem + TS, uphi, k2, id128 | tc::kIdescTransB, 1);
                 tc::mma_f16_ta(tmem + TS, uplo, k1, id128 | tc::kIdescTransB, 1);
+            }
+            commit(B_M3, c);
+#pragma unroll
+            for (int kk = 0; kk < kC / 16; ++kk) {
                 const uint64_t p1d = tc::sdesc(sbase + PP + kk * 256, 128, 1024);
                 const uint64_t p2d = tc::sdesc(sbase + PP + 8192 + kk * 256, 128, 1024);
-                const uint32_t uhi = tmem + R1 + 8 * kk, ulo = tmem + R1 + 32 + 8 * kk;
+                const uint32_t uhi = tmem + XU + 8 * kk, ulo = tmem + XU + 32 + 8 * kk;
                 tc::mma_f16_ta(tmem + D2, uhi, p1d, id64, kk > 0);
                 tc::mma_f16_ta(tmem + D2, uhi, p2d, id64, 1);
                 tc::mma_f16_ta(tmem + D2, ulo, p1d, id64, 1);
             }
-            tc::mma_commit(bar(B_M3));
-            last_commit = B_M3;
-            last_phase = par;
+            commit(B_PU, c);
             return true;
         };
+        // warp 0 runs the issuer's step; all its lanes learn whether it succeeded
+        auto warp0_issue = [&](auto &&step, int c) -> bool {
+            bool res = true;
+            if (warp == 0) {
+                if (issuer)
+                    res = step(c);
+                res = __shfl_sync(0xffffffffu, res, 0);
+            }
+            return res;
+        };
         if (issuer) {
-            issue_raw(0);
+            issue_k(0);
+            if (nch > 1)
+                issue_k(1);
+            issue_q(0);
             issue_t(0);
             issue_p(0);
         }
@@ -924,7 +1099,21 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
         const int j = 32 * q4 + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
         float *state_row = a.state + (((size_t)b * a.Hv + h) * kD + j) * kD + 64 * hf;
-        float *Os = reinterpret_cast<float *>(smem + OS);
+        // the S_0^T operand (R1, two parts) from the fp32 master (TS)
+        auto state_operand = [&]() {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float sv[16];
+                tc::tmem_ld16(tl + TS + 64 * hf + 16 * k, sv);
+                uint32_t hi[8], lo[8];
+                pack_split16(sv, hi, lo);
+                tmem_st8u(tl + R1 + 32 * hf + 8 * k, hi);
+                tmem_st8u(tl + R1 + 64 + 32 * hf + 8 * k, lo);
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            tc::mbar_arrive(bar(B_ST));
+        };
         // prologue: entering state -> fp32 master (TS) and the S_0^T operand (R1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -935,33 +1124,20 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 v16[e] = f.x; v16[e + 1] = f.y; v16[e + 2] = f.z; v16[e + 3] = f.w;
             }
             tc::tmem_st16(tl + TS + 64 * hf + 16 * k, v16);
-            uint32_t hi[8], lo[8];
-            pack_split16(v16, hi, lo);
-            tmem_st8u(tl + R1 + 32 * hf + 8 * k, hi);
-            tmem_st8u(tl + R1 + 64 + 32 * hf + 8 * k, lo);
         }
-        tc::tmem_wait_st();
-        tc::fence_before_sync();
-        tc::mbar_arrive(bar(B_ST));
-        // gated-norm mapping: warp w handles tokens w, w + 8, ...; lane holds channels 4 lane .. +3
-        const float4 nw4 = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane);
-        bool ok = true;
+        state_operand();
+        bool ok = warp0_issue(issue_m1k, 0) && warp0_issue(issue_m1q, 0);
+        int rho = 0;   // this chunk's state scale
 #pragma unroll 1
-        for (int c = 0; c < nch; ++c) {
+        for (int c = 0; ok && c < nch; ++c) {
             const uint32_t par = c & 1;
-            const int c0 = c * kC, n = min(kC, a.T - c0);
-            if (warp == 0) {
-                if (issuer)
-                    ok = issue_m1(c);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok)
-                    break;
-            }
-            ok = waitb(B_M1, par, lim) && waitb(B_V, par, lim);
+            ok = waitb(B_M1, par, lim) && waitb(B_V, par, lim) && waitb(B_T, par, lim);
             if (!ok)
                 break;
             tc::fence_after_sync();
             const Gates *G = gbuf + (c & 1);
+            const int rho_next = next_rho(G, rho);
+            const float s_in = exp2i(-rho), s_out = exp2i(rho_next);
             // ---- X^T[j][t] = beta_t V[t][j] - beta_t e^{Gam_t} (K S_0)[t][j]; the state master
             //      scaled by e^{Gam_C} ahead of this chunk's update
 #pragma unroll
@@ -974,18 +1150,18 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 for (int qq = 0; qq < 4; ++qq) {
                     const float4 f = *reinterpret_cast<const float4 *>(smem + foot_off(j, tb0 / 4 + qq));
                     const float4 bt = ld4(G->beta + tb0 + 4 * qq), bg = ld4(G->bg + tb0 + 4 * qq);
-                    x[4 * qq + 0] = __fsub_rn(__fmul_rn(bt.x, f.x), __fmul_rn(bg.x, ks[4 * qq + 0]));
-                    x[4 * qq + 1] = __fsub_rn(__fmul_rn(bt.y, f.y), __fmul_rn(bg.y, ks[4 * qq + 1]));
-                    x[4 * qq + 2] = __fsub_rn(__fmul_rn(bt.z, f.z), __fmul_rn(bg.z, ks[4 * qq + 2]));
-                    x[4 * qq + 3] = __fsub_rn(__fmul_rn(bt.w, f.w), __fmul_rn(bg.w, ks[4 * qq + 3]));
+                    x[4 * qq + 0] = __fsub_rn(__fmul_rn(bt.x, f.x), __fmul_rn(__fmul_rn(bg.x, s_in), ks[4 * qq + 0]));
+                    x[4 * qq + 1] = __fsub_rn(__fmul_rn(bt.y, f.y), __fmul_rn(__fmul_rn(bg.y, s_in), ks[4 * qq + 1]));
+                    x[4 * qq + 2] = __fsub_rn(__fmul_rn(bt.z, f.z), __fmul_rn(__fmul_rn(bg.z, s_in), ks[4 * qq + 2]));
+                    x[4 * qq + 3] = __fsub_rn(__fmul_rn(bt.w, f.w), __fmul_rn(__fmul_rn(bg.w, s_in), ks[4 * qq + 3]));
                 }
                 uint32_t hi[8], lo[8];
                 pack_split16(x, hi, lo);
-                tmem_st8u(tl + R1 + tb0 / 2, hi);
-                tmem_st8u(tl + R1 + 32 + tb0 / 2, lo);
+                tmem_st8u(tl + XU + tb0 / 2, hi);
+                tmem_st8u(tl + XU + 32 + tb0 / 2, lo);
             }
             {
-                const float ec = G->ec;
+                const float ec = __fmul_rn(G->ec, exp2i(rho_next - rho));
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     float sv[16];
@@ -999,16 +1175,11 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             tc::tmem_wait_st();
             tc::fence_before_sync();
             tc::mbar_arrive(bar(B_X));
-            if (warp == 0) {
-                if (issuer)
-                    ok = issue_m2(c);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok)
-                    break;
-            }
+            if (!(ok = warp0_issue(issue_m2, c)))
+                break;
             // ---- U = T X (from D2): U^T for the output product, U'^T = U^T diag(e^{Gam_C - Gam})
-            ok = waitb(B_M2, par, lim);
-            if (!ok)
+            //      for the state update
+            if (!(ok = waitb(B_M2, par, lim)))
                 break;
             tc::fence_after_sync();
 #pragma unroll
@@ -1018,15 +1189,15 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 tc::tmem_ld16(tl + D2 + tb0, u);
                 uint32_t hi[8], lo[8];
                 pack_split16(u, hi, lo);
-                tmem_st8u(tl + R1 + tb0 / 2, hi);
-                tmem_st8u(tl + R1 + 32 + tb0 / 2, lo);
+                tmem_st8u(tl + XU + tb0 / 2, hi);
+                tmem_st8u(tl + XU + 32 + tb0 / 2, lo);
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
                     const float4 g4 = ld4(G->egc + tb0 + 4 * qq);
-                    u[4 * qq + 0] = __fmul_rn(u[4 * qq + 0], g4.x);
-                    u[4 * qq + 1] = __fmul_rn(u[4 * qq + 1], g4.y);
-                    u[4 * qq + 2] = __fmul_rn(u[4 * qq + 2], g4.z);
-                    u[4 * qq + 3] = __fmul_rn(u[4 * qq + 3], g4.w);
+                    u[4 * qq + 0] = __fmul_rn(u[4 * qq + 0], __fmul_rn(g4.x, s_out));
+                    u[4 * qq + 1] = __fmul_rn(u[4 * qq + 1], __fmul_rn(g4.y, s_out));
+                    u[4 * qq + 2] = __fmul_rn(u[4 * qq + 2], __fmul_rn(g4.z, s_out));
+                    u[4 * qq + 3] = __fmul_rn(u[4 * qq + 3], __fmul_rn(g4.w, s_out));
                 }
                 pack_split16(u, hi, lo);
                 tmem_st8u(tl + R1 + 64 + tb0 / 2, hi);
@@ -1035,22 +1206,40 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             tc::tmem_wait_st();
             tc::fence_before_sync();
             tc::mbar_arrive(bar(B_U));
-            if (warp == 0) {
-                if (issuer)
-                    ok = issue_m3(c);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok)
-                    break;
-            }
-            ok = waitb(B_M3, par, lim);
-            if (!ok)
+            if (!(ok = warp0_issue(issue_m3, c)))
+                break;
+            // ---- the updated state: the next chunk's S_0^T operand and its first product
+            if (!(ok = waitb(B_M3, par, lim)))
                 break;
             tc::fence_after_sync();
-            if (issuer && c + 1 < nch)   // this chunk's P has been read by its product
-                issue_p(c + 1);
-            // ---- O^T row j = e^{Gam} (Q S_0)^T + (P U)^T -> token-major staging, scaled by 1/sqrt(d)
+            if (issuer && c + 2 < nch)   // this chunk's K rows have been read by both products
+                issue_k(c + 2);
+            if (c + 1 < nch) {
+                state_operand();
+                if (!(ok = warp0_issue(issue_m1k, c + 1)))
+                    break;
+            } else {
+                // ---- final state back to HBM (S^T rows = the library layout), unscaled
+                const float us = exp2i(-rho_next);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float sv[16];
+                    tc::tmem_ld16(tl + TS + 64 * hf + 16 * k, sv);
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4 *>(state_row + 16 * k + e) =
+                            make_float4(__fmul_rn(sv[e], us), __fmul_rn(sv[e + 1], us),
+                                        __fmul_rn(sv[e + 2], us), __fmul_rn(sv[e + 3], us));
+                }
+            }
+            // ---- O^T row j = e^{Gam} (Q S_0)^T + (P U)^T, scaled by 1/sqrt(d)
             //      (the two terms are added here, rounded, rather than in the accumulator: for a
-            //      token whose readout nearly cancels this is the sum that decides its precision)
+            //      token whose readout nearly cancels this is the sum that decides its precision).
+            //      (P U)^T's commit also covers (Q S_0)^T, issued before it.
+            if (!(ok = waitb(B_PU, par, lim)))
+                break;
+            tc::fence_after_sync();
+            float o[32];
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
                 const int tb0 = 32 * hf + 16 * p;
@@ -1064,77 +1253,40 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int k = 4 * qq + e;
-                        Os[(tb0 + k) * kD + j] = __fmul_rn(__fmaf_rn(qs[k], egv[e], pu[k]), a.scale);
+                        o[16 * p + k] = __fmul_rn(__fmaf_rn(qs[k], __fmul_rn(egv[e], s_in), pu[k]), a.scale);
                     }
                 }
             }
+            tc::fence_before_sync();
+            tc::mbar_arrive(bar(B_OR));
             if (c + 1 < nch) {
-                // ---- next chunk's S_0^T operand from the updated state master
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float sv[16];
-                    tc::tmem_ld16(tl + TS + 64 * hf + 16 * k, sv);
-                    uint32_t hi[8], lo[8];
-                    pack_split16(sv, hi, lo);
-                    tmem_st8u(tl + R1 + 32 * hf + 8 * k, hi);
-                    tmem_st8u(tl + R1 + 64 + 32 * hf + 8 * k, lo);
-                }
-                tc::tmem_wait_st();
-                tc::fence_before_sync();
-                tc::mbar_arrive(bar(B_ST));
-            } else {
-                // ---- final state back to HBM (S^T rows = the library layout), unscaled
-                const float us = exp2i(-G->rho_next);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float sv[16];
-                    tc::tmem_ld16(tl + TS + 64 * hf + 16 * k, sv);
-#pragma unroll
-                    for (int e = 0; e < 16; e += 4)
-                        *reinterpret_cast<float4 *>(state_row + 16 * k + e) =
-                            make_float4(__fmul_rn(sv[e], us), __fmul_rn(sv[e + 1], us),
-                                        __fmul_rn(sv[e + 2], us), __fmul_rn(sv[e + 3], us));
-                }
+                if (issuer)                // this chunk's P has been read by its product
+                    issue_p(c + 1);
+                if (!(ok = warp0_issue(issue_m1q, c + 1)))
+                    break;
             }
-            tc::mbar_arrive(bar(B_OS));
-            ok = waitb(B_OS, par, lim);
-            if (!ok)
+            // ---- token-major staging for the conv warps' norm, once they have read chunk c-1's
+            if (c > 0 && !(ok = waitb(B_OSFREE, (c - 1) & 1, lim)))
                 break;
-            // ---- gated RMSNorm ("fm_kernel_ssm.h", "Gated RMSNorm"): warp per token row
-#pragma unroll 1
-            for (int t = warp; t < n; t += 8) {
-                const float4 y = *reinterpret_cast<const float4 *>(Os + t * kD + 4 * lane);
-                float ss = __fmul_rn(y.x, y.x);
-                ss = __fmaf_rn(y.y, y.y, ss);
-                ss = __fmaf_rn(y.z, y.z, ss);
-                ss = __fmaf_rn(y.w, y.w, ss);
-                ss = warp_sum32(ss);
-                const float inv = rsqrtf(__fadd_rn(__fmul_rn(ss, 1.0f / kD), a.rms_eps));
-                const int64_t row = (int64_t)b * a.T + c0 + t;
-                const TIn *zr = static_cast<const TIn *>(a.z) + row * a.z_stride + (int64_t)h * kD + 4 * lane;
-                float zv[4];
-                if (zvec) {
-                    load_row<4, TIn>(zr, zv);
-                } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        zv[e] = load_act<TIn>(zr + e);
-                }
-                float4 o;
-                o.x = gated_out(y.x, inv, nw4.x, zv[0]);
-                o.y = gated_out(y.y, inv, nw4.y, zv[1]);
-                o.z = gated_out(y.z, inv, nw4.z, zv[2]);
-                o.w = gated_out(y.w, inv, nw4.w, zv[3]);
-                *reinterpret_cast<float4 *>(a.out + (row * a.Hv + h) * kD + 4 * lane) = o;
-            }
+            for (int p = 0; p < 2; ++p)
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    Os[(32 * hf + 16 * p + k) * kD + j] = o[16 * p + k];
+            tc::mbar_arrive(bar(B_OS));
+            rho = rho_next;
         }
         if (issuer) {
             // drain: copies and products in flight finish before the CTA releases TMEM
             bool drained = true;
             if (last_commit >= 0)   // a commit tracks every product issued before it
                 drained &= tc::mbar_wait_ns(bar(last_commit), last_phase, lim);
-            if (raw_last >= 0)
-                drained &= tc::mbar_wait_ns(bar(B_RAW), raw_last & 1, lim);
+            if (q_last >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_Q), q_last & 1, lim);
+            if (k_last0 >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_K0), (k_last0 >> 1) & 1, lim);
+            if (k_last1 >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_K1), (k_last1 >> 1) & 1, lim);
             if (t_last >= 0)
                 drained &= tc::mbar_wait_ns(bar(B_T), t_last & 1, lim);
             if (p_last >= 0)

@@ -191,6 +191,19 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
 }
 
+// One contiguous shared -> global copy (same alignment rules), tracked by the
+// issuing thread's bulk async-groups: commit them with bulk_commit, then
+// bulk_wait_read before the source is overwritten and bulk_wait before the
+// thread exits (the copies finish by themselves; these waits end with them).
+__device__ __forceinline__ void bulk_copy_s2g(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(dst), "r"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // TMEM allocation: executed by one whole warp; the base address lands in *slot.
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_saddr, uint32_t ncols)
 {

@@ -308,10 +308,12 @@ gdn_status gdn_verify_commit_kn(float *state, float *conv_state, const float *st
                                 const gdn_dims *dims, int32_t n_draft, gdn_stream_t stream);
 
 /*
- * Workspace bytes gdn_prefill_chunked needs for these dims and n_tokens:
- * 32 KB of per-chunk operand images per (sequence, V head, 64-token chunk),
- * i.e. n_seq * n_v_heads * ceil(n_tokens / 64) * 32768. Returns 0 for invalid
- * dims, n_tokens < 1 or chunk != 64.
+ * Workspace bytes gdn_prefill_chunked needs for these dims and n_tokens: per
+ * (sequence, 64-token chunk) a 34 KB image per V head (the chunk's
+ * (I + A)^-1, decayed Q K^T and gates) and a 64 KB image per QK head (its
+ * normalised Q and K rows as tensor-core operands), i.e.
+ * n_seq * ceil(n_tokens / 64) * (34816 * n_v_heads + 65536 * n_qk_heads).
+ * Returns 0 for invalid dims, n_tokens < 1 or chunk != 64.
  */
 size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t n_tokens, int32_t chunk);
 
@@ -331,9 +333,9 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims *dims, int32_t n_tokens, int32
  *              meaningless on return. Calls that overlap on the GPU need
  *              separate workspaces.
  * Runs as three launches on `stream`: every chunk's state-independent
- * operands (its (I + A)^-1 transform and decayed Q K^T) in parallel into the
- * workspace, the sequential pass over the chunks of each (sequence, V head),
- * and the conv-history update.
+ * operands (its normalised Q and K rows, (I + A)^-1 transform, decayed Q K^T
+ * and gates) in parallel into the workspace, the sequential pass over the
+ * chunks of each (sequence, V head), and the conv-history update.
  * chunk must be 64. x, params->conv_w and out must be 16-byte aligned, with x
  * rows a multiple of 16 bytes apart (x_stride * element size). Agrees with the
  * sequential scan within float32 rounding, not bit for bit.
@@ -356,8 +358,9 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
  *
  * The workspace is a fixed 16 MiB array inside the library (a static device
  * variable): every GPU on which the library is loaded holds it until the
- * process exits, and it serves up to 512 chunk images, i.e.
- * n_seq * n_v_heads * ceil(n_tokens / 64) <= 512. Larger calls return
+ * process exits, and it serves calls whose gdn_prefill_workspace_bytes is at
+ * most 16 MiB (e.g. one sequence of 2048 tokens with 2 QK and 4 V heads, or
+ * 16 x 64 tokens with 4 QK and 8 V heads). Larger calls return
  * GDN_ERR_UNSUPPORTED (the reason is in gdn_last_cuda_error()) and launch
  * nothing. The library itself allocates nothing either.
  *

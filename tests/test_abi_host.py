@@ -110,11 +110,11 @@ def test_prefill_rejects_bad_chunk_and_tokens(lib):
 
 
 def test_prefill_workspace_size_and_checks(lib):
-    # one 16 KB image per (sequence, V head, 64-token chunk)
+    # per (sequence, 64-token chunk): a 34 KB image per V head and a 64 KB image per QK head
     dims = _dims()
     cd, cp = dims.c(), _params().c()
     for T, chunks in ((1, 1), (64, 1), (65, 2), (8192, 128)):
-        assert gdn.prefill_workspace_bytes(dims, T) == 2 * 4 * chunks * 32768
+        assert gdn.prefill_workspace_bytes(dims, T) == 2 * chunks * (4 * 34816 + 2 * 65536)
     assert gdn.prefill_workspace_bytes(dims, 0) == 0
     assert gdn.prefill_workspace_bytes(dims, 64, 32) == 0
     need = gdn.prefill_workspace_bytes(dims, 130)

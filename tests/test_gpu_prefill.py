@@ -125,7 +125,7 @@ def test_prefill_explicit_workspace_contents_do_not_matter():
     ref = run_oracle(shape, inp, readout=True)
     dims = dims_of(shape)
     nbytes = gdn.prefill_workspace_bytes(dims, shape.T)
-    assert nbytes == shape.B * shape.Hv * 4 * 32768
+    assert nbytes == shape.B * 4 * (shape.Hv * 34816 + shape.Hq * 65536)
     ws = torch.full((nbytes + 4096,), 0xFF, dtype=torch.uint8, device="cuda")   # NaN bit patterns
     outs = []
     for _ in range(2):

@@ -71,7 +71,7 @@ def test_noalloc_prefill_matches_the_workspace_entry_point_twice_in_a_row():
 
 def test_noalloc_prefill_rejects_work_beyond_its_scratch():
     fn = _noalloc_fn()
-    # 2 sequences x 4 V heads x 129 chunks = 1032 chunk images > 512
+    # 2 sequences x 129 chunks x (4 x 34 KB + 2 x 64 KB) = 68 MB > 16 MiB
     shape = synth.Shape(B=2, T=129 * 64, Hq=2, Hv=4, warm=True)
     dims = dims_of(shape)
     assert gdn.prefill_workspace_bytes(dims, shape.T) > STATIC_SCRATCH
