@@ -86,8 +86,9 @@ class Params:
     rms_eps: float = 1e-6
 
     def c(self) -> _CParams:
-        return _CParams(_ptr(self.conv_w), _ptr(self.dt), _ptr(self.A_log), _ptr(self.norm_w),
-                        self.l2_eps, self.rms_eps)
+        return _CParams(_dev(self.conv_w, "params.conv_w", _F32), _dev(self.dt, "params.dt", _F32),
+                        _dev(self.A_log, "params.A_log", _F32),
+                        _dev(self.norm_w, "params.norm_w", _F32), self.l2_eps, self.rms_eps)
 
 
 def library_path() -> str:
@@ -133,6 +134,9 @@ def load():
         L.gdn_prefill_workspace_bytes.argtypes = [pd, i32, i32]
         L.gdn_testing_set_first_wait_ns.restype = None
         L.gdn_testing_set_first_wait_ns.argtypes = [_ct.c_uint64]
+        L.gdn_testing_row_splits.restype = None
+        L.gdn_testing_row_splits.argtypes = [i32, i32, i32, i32, _ct.POINTER(_ct.c_int32),
+                                             _ct.POINTER(_ct.c_int32)]
         L.gdn_check_device.restype = _ct.c_int
         L.gdn_check_device.argtypes = [_ct.POINTER(_ct.c_int32)]
         L.gdn_status_string.restype = _ct.c_char_p
@@ -155,12 +159,62 @@ def version() -> str:
 
 
 # ------------------------------------------------------------------ marshalling helpers
-def _ptr(t) -> int | None:
-    if t is None:
-        return None
-    if isinstance(t, int):
+def _torch_dtypes(*names):
+    import torch
+    return tuple(getattr(torch, n) for n in names)
+
+
+_F32, _ACT, _I32 = ("float32",), ("float32", "bfloat16"), ("int32",)
+
+
+def _dev(t, name: str, dtypes=None, row_stride: int | None = None) -> int | None:
+    """Device address of a tensor argument, once it is known to be safe to hand to a kernel:
+    of one of `dtypes` (torch dtype names), laid out as the call reads it (contiguous, or, when
+    row_stride is given, elements contiguous within a row and every leading index a whole
+    number of rows of row_stride elements), and a CUDA tensor on the current device. None
+    stays None; an int is taken as a raw device address, unchecked."""
+    if t is None or isinstance(t, int):
         return t
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch tensor, got {type(t).__name__}")
+    if dtypes is not None and t.dtype not in _torch_dtypes(*dtypes):
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {' or '.join(dtypes)}")
+    if row_stride is None:
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: tensor must be contiguous")
+    elif t.numel() > 0:
+        if t.dim() == 0 or t.stride(-1) != 1:
+            raise ValueError(f"{name}: elements of a row must be contiguous")
+        expected = row_stride
+        for d in range(t.dim() - 2, -1, -1):
+            if t.size(d) > 1 and t.stride(d) != expected:
+                raise ValueError(f"{name}: dimension {d} steps {t.stride(d)} elements, the "
+                                 f"row stride makes it {expected}")
+            expected *= t.size(d)
+    if not t.is_cuda:
+        raise ValueError(f"{name}: tensor is on {t.device}, not on a CUDA device")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name}: tensor is on {t.device}, the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
     return t.data_ptr()
+
+
+def _ptr(t) -> int | None:
+    """Address of an untyped buffer (a workspace): contiguous, CUDA, current device."""
+    return _dev(t, "workspace")
+
+
+def _acts(x, z, alpha, beta_logit, cd) -> tuple:
+    """The activation inputs of a layer call: one dtype (float32 or bfloat16) for all four,
+    rows of x, z and the gates at the strides of dims."""
+    if x is not None and not isinstance(x, int):
+        for t, nm in ((z, "z"), (alpha, "alpha"), (beta_logit, "beta_logit")):
+            if t is not None and not isinstance(t, int) and t.dtype != x.dtype:
+                raise TypeError(f"{nm}: dtype {t.dtype}, x is {x.dtype}")
+    return (_dev(x, "x", _ACT, cd.x_stride), _dev(z, "z", _ACT, cd.z_stride),
+            _dev(alpha, "alpha", _ACT, cd.gate_stride),
+            _dev(beta_logit, "beta_logit", _ACT, cd.gate_stride))
 
 
 def _dtype(t) -> int:
@@ -189,15 +243,19 @@ def _check(status: int, fn: str):
 
 # ------------------------------------------------------------------ entry points
 def decay_gate(alpha, dt, A_log, g, rows: int, n_heads: int, alpha_stride: int = 0, stream=None):
-    _check(load().gdn_decay_gate(_ptr(alpha), _dtype(alpha), alpha_stride or n_heads, _ptr(dt),
-                                 _ptr(A_log), _ptr(g), rows, n_heads, _stream(stream)),
+    _check(load().gdn_decay_gate(_dev(alpha, "alpha", _ACT, alpha_stride or n_heads), _dtype(alpha),
+                                 alpha_stride or n_heads, _dev(dt, "dt", _F32),
+                                 _dev(A_log, "A_log", _F32), _dev(g, "g", _F32), rows, n_heads,
+                                 _stream(stream)),
            "gdn_decay_gate")
 
 
 def conv_update(conv_state, x, conv_w, out, dims: Dims, n_tokens: int = 1, l2_eps: float = 1e-6,
                 stream=None):
     cd = dims.c()
-    _check(load().gdn_conv_update(_ptr(conv_state), _ptr(x), _dtype(x), _ptr(conv_w), _ptr(out),
+    _check(load().gdn_conv_update(_dev(conv_state, "conv_state", _F32),
+                                  _dev(x, "x", _ACT, cd.x_stride), _dtype(x),
+                                  _dev(conv_w, "conv_w", _F32), _dev(out, "out", _F32),
                                   _ct.byref(cd), n_tokens, l2_eps, _stream(stream)),
            "gdn_conv_update")
 
@@ -205,56 +263,61 @@ def conv_update(conv_state, x, conv_w, out, dims: Dims, n_tokens: int = 1, l2_ep
 def recurrence_decode(state, q, k, v, qkv_stride: int, g, beta, y, dims: Dims, scale: float,
                       stream=None):
     cd = dims.c()
-    _check(load().gdn_recurrence_decode(_ptr(state), _ptr(q), _ptr(k), _ptr(v), qkv_stride,
-                                        _ptr(g), _ptr(beta), _ptr(y), _ct.byref(cd), scale,
-                                        _stream(stream)),
+    _check(load().gdn_recurrence_decode(_dev(state, "state", _F32),
+                                        _dev(q, "q", _F32, qkv_stride), _dev(k, "k", _F32, qkv_stride),
+                                        _dev(v, "v", _F32, qkv_stride), qkv_stride,
+                                        _dev(g, "g", _F32), _dev(beta, "beta", _F32),
+                                        _dev(y, "y", _F32), _ct.byref(cd), scale, _stream(stream)),
            "gdn_recurrence_decode")
 
 
 def gated_norm(y, norm_w, z, out, rows: int, n_v_heads: int, head_dim: int = 128,
                z_stride: int = 0, eps: float = 1e-6, stream=None):
-    _check(load().gdn_gated_norm(_ptr(y), _ptr(norm_w), _ptr(z), _dtype(z),
-                                 z_stride or n_v_heads * head_dim, _ptr(out), rows, n_v_heads,
-                                 head_dim, eps, _stream(stream)),
+    zs = z_stride or n_v_heads * head_dim
+    _check(load().gdn_gated_norm(_dev(y, "y", _F32), _dev(norm_w, "norm_w", _F32),
+                                 _dev(z, "z", _ACT, zs), _dtype(z), zs, _dev(out, "out", _F32),
+                                 rows, n_v_heads, head_dim, eps, _stream(stream)),
            "gdn_gated_norm")
 
 
 def decode_step(state, conv_state, x, z, alpha, beta_logit, params: Params, out, dims: Dims,
                 stream=None):
     cd, cp = dims.c(), params.c()
-    _check(load().gdn_decode_step(_ptr(state), _ptr(conv_state), _ptr(x), _ptr(z), _ptr(alpha),
-                                  _ptr(beta_logit), _dtype(x), _ct.byref(cp), _ptr(out),
-                                  _ct.byref(cd), _stream(stream)),
+    _check(load().gdn_decode_step(_dev(state, "state", _F32), _dev(conv_state, "conv_state", _F32),
+                                  *_acts(x, z, alpha, beta_logit, cd), _dtype(x), _ct.byref(cp),
+                                  _dev(out, "out", _F32), _ct.byref(cd), _stream(stream)),
            "gdn_decode_step")
 
 
 def decode_step_bf16_state(state, conv_state, x, z, alpha, beta_logit, params: Params, out,
                            dims: Dims, stream=None):
     """state and out are bfloat16 tensors; see gdn_decode_step_bf16_state."""
-    import torch
-    if state.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
-        raise TypeError("state and out must be bfloat16")
     cd, cp = dims.c(), params.c()
-    _check(load().gdn_decode_step_bf16_state(_ptr(state), _ptr(conv_state), _ptr(x), _ptr(z),
-                                             _ptr(alpha), _ptr(beta_logit), _dtype(x),
-                                             _ct.byref(cp), _ptr(out), _ct.byref(cd),
-                                             _stream(stream)),
+    _check(load().gdn_decode_step_bf16_state(_dev(state, "state", ("bfloat16",)),
+                                             _dev(conv_state, "conv_state", _F32),
+                                             *_acts(x, z, alpha, beta_logit, cd), _dtype(x),
+                                             _ct.byref(cp), _dev(out, "out", ("bfloat16",)),
+                                             _ct.byref(cd), _stream(stream)),
            "gdn_decode_step_bf16_state")
 
 
 def verify_k2(state, conv_state, state_snap, conv_snap, x, z, alpha, beta_logit, params: Params,
               out, dims: Dims, stream=None):
     cd, cp = dims.c(), params.c()
-    _check(load().gdn_verify_k2(_ptr(state), _ptr(conv_state), _ptr(state_snap), _ptr(conv_snap),
-                                _ptr(x), _ptr(z), _ptr(alpha), _ptr(beta_logit), _dtype(x),
-                                _ct.byref(cp), _ptr(out), _ct.byref(cd), _stream(stream)),
+    _check(load().gdn_verify_k2(_dev(state, "state", _F32), _dev(conv_state, "conv_state", _F32),
+                                _dev(state_snap, "state_snap", _F32),
+                                _dev(conv_snap, "conv_snap", _F32),
+                                *_acts(x, z, alpha, beta_logit, cd), _dtype(x), _ct.byref(cp),
+                                _dev(out, "out", _F32), _ct.byref(cd), _stream(stream)),
            "gdn_verify_k2")
 
 
 def verify_commit(state, conv_state, state_snap, conv_snap, n_accept, dims: Dims, stream=None):
     cd = dims.c()
-    _check(load().gdn_verify_commit(_ptr(state), _ptr(conv_state), _ptr(state_snap),
-                                    _ptr(conv_snap), _ptr(n_accept), _ct.byref(cd),
+    _check(load().gdn_verify_commit(_dev(state, "state", _F32), _dev(conv_state, "conv_state", _F32),
+                                    _dev(state_snap, "state_snap", _F32),
+                                    _dev(conv_snap, "conv_snap", _F32),
+                                    _dev(n_accept, "n_accept", _I32), _ct.byref(cd),
                                     _stream(stream)),
            "gdn_verify_commit")
 
@@ -274,11 +337,12 @@ def prefill_chunked(state, conv_state, x, z, alpha, beta_logit, params: Params, 
         import torch
         nbytes = prefill_workspace_bytes(dims, n_tokens, chunk)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+    ws = _ptr(workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(load().gdn_prefill_chunked(_ptr(state), _ptr(conv_state), _ptr(x), _ptr(z), _ptr(alpha),
-                                      _ptr(beta_logit), _dtype(x), _ct.byref(cp), _ptr(out),
-                                      _ct.byref(cd), n_tokens, chunk, _ptr(workspace), ws_bytes,
-                                      _stream(stream)),
+    _check(load().gdn_prefill_chunked(_dev(state, "state", _F32), _dev(conv_state, "conv_state", _F32),
+                                      *_acts(x, z, alpha, beta_logit, cd), _dtype(x), _ct.byref(cp),
+                                      _dev(out, "out", _F32), _ct.byref(cd), n_tokens, chunk, ws,
+                                      ws_bytes, _stream(stream)),
            "gdn_prefill_chunked")
 
 
@@ -288,38 +352,54 @@ def testing_set_first_wait_ns(ns: int):
     load().gdn_testing_set_first_wait_ns(int(ns))
 
 
+def testing_row_splits(n_seq: int, n_v_heads: int, r: int, sms: int) -> tuple:
+    """Test hook (include/gdn_testing.h): (decode, scan) row slices per V head the launchers
+    choose on a device with `sms` SMs. Host-only."""
+    d, s = _ct.c_int32(0), _ct.c_int32(0)
+    load().gdn_testing_row_splits(n_seq, n_v_heads, r, sms, _ct.byref(d), _ct.byref(s))
+    return d.value, s.value
+
+
 def recurrence_scan(state, q, k, v, qkv_stride: int, g, beta, y, dims: Dims, n_tokens: int,
                     scale: float, stream=None):
     cd = dims.c()
-    _check(load().gdn_recurrence_scan(_ptr(state), _ptr(q), _ptr(k), _ptr(v), qkv_stride,
-                                      _ptr(g), _ptr(beta), _ptr(y), _ct.byref(cd), n_tokens,
-                                      scale, _stream(stream)),
+    _check(load().gdn_recurrence_scan(_dev(state, "state", _F32),
+                                      _dev(q, "q", _F32, qkv_stride), _dev(k, "k", _F32, qkv_stride),
+                                      _dev(v, "v", _F32, qkv_stride), qkv_stride,
+                                      _dev(g, "g", _F32), _dev(beta, "beta", _F32),
+                                      _dev(y, "y", _F32), _ct.byref(cd), n_tokens, scale,
+                                      _stream(stream)),
            "gdn_recurrence_scan")
 
 
 def layer_scan(state, conv_state, x, z, alpha, beta_logit, params: Params, out, dims: Dims,
                n_tokens: int, stream=None):
     cd, cp = dims.c(), params.c()
-    _check(load().gdn_layer_scan(_ptr(state), _ptr(conv_state), _ptr(x), _ptr(z), _ptr(alpha),
-                                 _ptr(beta_logit), _dtype(x), _ct.byref(cp), _ptr(out),
-                                 _ct.byref(cd), n_tokens, _stream(stream)),
+    _check(load().gdn_layer_scan(_dev(state, "state", _F32), _dev(conv_state, "conv_state", _F32),
+                                 *_acts(x, z, alpha, beta_logit, cd), _dtype(x), _ct.byref(cp),
+                                 _dev(out, "out", _F32), _ct.byref(cd), n_tokens,
+                                 _stream(stream)),
            "gdn_layer_scan")
 
 
 def verify_kn(state, conv_state, state_snap, conv_snap, x, z, alpha, beta_logit, params: Params,
               out, dims: Dims, n_draft: int, stream=None):
     cd, cp = dims.c(), params.c()
-    _check(load().gdn_verify_kn(_ptr(state), _ptr(conv_state), _ptr(state_snap), _ptr(conv_snap),
-                                _ptr(x), _ptr(z), _ptr(alpha), _ptr(beta_logit), _dtype(x),
-                                _ct.byref(cp), _ptr(out), _ct.byref(cd), n_draft,
-                                _stream(stream)),
+    _check(load().gdn_verify_kn(_dev(state, "state", _F32), _dev(conv_state, "conv_state", _F32),
+                                _dev(state_snap, "state_snap", _F32),
+                                _dev(conv_snap, "conv_snap", _F32),
+                                *_acts(x, z, alpha, beta_logit, cd), _dtype(x), _ct.byref(cp),
+                                _dev(out, "out", _F32), _ct.byref(cd), n_draft, _stream(stream)),
            "gdn_verify_kn")
 
 
 def verify_commit_kn(state, conv_state, state_snap, conv_snap, n_accept, dims: Dims, n_draft: int,
                      stream=None):
     cd = dims.c()
-    _check(load().gdn_verify_commit_kn(_ptr(state), _ptr(conv_state), _ptr(state_snap),
-                                       _ptr(conv_snap), _ptr(n_accept), _ct.byref(cd), n_draft,
+    _check(load().gdn_verify_commit_kn(_dev(state, "state", _F32),
+                                       _dev(conv_state, "conv_state", _F32),
+                                       _dev(state_snap, "state_snap", _F32),
+                                       _dev(conv_snap, "conv_snap", _F32),
+                                       _dev(n_accept, "n_accept", _I32), _ct.byref(cd), n_draft,
                                        _stream(stream)),
            "gdn_verify_commit_kn")

@@ -1,7 +1,7 @@
 // abi.cu -- the extern "C" entry points of libgdn (declared in include/gdn.h):
 // host-side argument validation, then one launch on the caller's stream.
-// Nothing here allocates, synchronises or keeps state between calls (the
-// last-error text is thread-local).
+// Nothing here allocates, synchronises or keeps state between calls, beyond
+// the thread-local last-error text and a per-device cache of the SM count.
 #include <stdio.h>
 #include <string.h>
 
@@ -16,11 +16,26 @@
 namespace gdn {
 namespace {
 std::atomic<uint64_t> g_first_wait_ns{0};
+constexpr int kMaxSmDevices = 64;
+std::atomic<int> g_sm_count[kMaxSmDevices];   // 0 until queried
 }
 uint64_t first_wait_override_ns()
 {
     const uint64_t v = g_first_wait_ns.load(std::memory_order_relaxed);
     return v != 0 ? v : kDefaultWaitNs;
+}
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 1;
+    if (dev >= 0 && dev < kMaxSmDevices && (n = g_sm_count[dev].load(std::memory_order_relaxed)) > 0)
+        return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return 1;   // the launch that follows reports the device's error
+    if (dev >= 0 && dev < kMaxSmDevices)
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 }  // namespace gdn
 
@@ -133,6 +148,7 @@ gdn_status fused_common(void *state, float *conv_state, float *state_snap, float
     a.l2_eps = params->l2_eps;
     a.rms_eps = params->rms_eps;
     a.scale = 1.0f / sqrtf((float)dims->head_dim);
+    a.sm_count = gdn::sm_count();
     if (bf16_state)
         return from_cuda(gdn::launch_decode_fused_bf16_state(a, act_dtype == GDN_BF16,
                                                              as_cuda(stream)));
@@ -517,6 +533,13 @@ gdn_status gdn_prefill_chunked_noalloc(float *state, float *conv_state, const vo
 void gdn_testing_set_first_wait_ns(uint64_t ns)
 {
     gdn::g_first_wait_ns.store(ns, std::memory_order_relaxed);
+}
+
+void gdn_testing_row_splits(int32_t n_seq, int32_t n_v_heads, int32_t r, int32_t sms,
+                            int32_t *decode_split, int32_t *scan_split)
+{
+    *decode_split = gdn::pick_nsplit(n_seq, n_v_heads, r, sms);
+    *scan_split = gdn::scan_nsplit(n_seq, n_v_heads, r, sms);
 }
 
 gdn_status gdn_check_device(int32_t *code)

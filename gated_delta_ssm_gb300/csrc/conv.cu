@@ -332,9 +332,7 @@ cudaError_t launch_tiles(const CUtensorMap &map, const ConvArgs &a, cudaStream_t
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, L::bytes);
         return n > 0 ? n : 1;
     }();
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = sm_count();
     const int n_tiles = (a.T + kTT - 1) / kTT;
     const int64_t n_items = (int64_t)a.B * n_tiles * (a.conv_dim / kD);
     if (n_items > INT32_MAX)

@@ -22,6 +22,12 @@ namespace cg = cooperative_groups;
 
 namespace gdn {
 
+// Bit 16: gdn_verify_commit saw an accepted count outside 1..2 (that sequence
+// was left unchanged). No kernel in this file waits on anything but hardware
+// barriers. Read and cleared by take_decode_device_error.
+static __device__ int g_decode_error;
+constexpr int kErrAcceptRange = 16;
+
 // ------------------------------------------------------------------ decay gate
 template <typename TIn>
 __global__ void __launch_bounds__(256) decay_gate_kernel(const TIn *alpha, int64_t alpha_stride,
@@ -159,11 +165,11 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
     load_rows<NG>(state + head_off + warp_off, st);
     if constexpr (sizeof(TS) == 2) {
         // bf16 rows (3 CTAs per SM): also prefetch into L2 the state block of the
-        // CTA 152 places later in launch order, about a third of a wave ahead
+        // CTA one SM count later in launch order, about a third of a wave ahead
         // (measured: 52.3 -> 49.8 us per 64 x 48-head step; for float32 rows the
         // same prefetch slows the step, 84 -> 89 us, so it is not issued there)
         if (threadIdx.x < 4) {
-            const long long L = (long long)blockIdx.y * gridDim.x + blockIdx.x + 152;
+            const long long L = (long long)blockIdx.y * gridDim.x + blockIdx.x + a.sm_count;
             if (L < (long long)gridDim.x * gridDim.y) {
                 const int bb = (int)(L / gridDim.x), xx = (int)(L % gridDim.x);
                 const TS *src = state + (((size_t)bb * a.Hv + xx / NSPLIT) * kD +
@@ -316,7 +322,13 @@ __global__ void __launch_bounds__(256) verify_commit_kernel(float *state, float 
                                                             int64_t state_elems, int64_t hist_elems)
 {
     const int b = blockIdx.y;
-    if (__ldg(n_accept + b) != 1)
+    const int n = __ldg(n_accept + b);
+    if (n < 1 || n > 2) {
+        if (blockIdx.x == 0 && threadIdx.x == 0)
+            atomicOr(&g_decode_error, kErrAcceptRange);
+        return;
+    }
+    if (n == 2)
         return;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -329,25 +341,11 @@ __global__ void __launch_bounds__(256) verify_commit_kernel(float *state, float 
 }
 
 // ------------------------------------------------------------------ host launchers
-#ifndef GDN_DECODE_TARGET_CTAS
-#define GDN_DECODE_TARGET_CTAS (4 * 152)
-#endif
-
-static int pick_nsplit(int B, int Hv, int r)
-{
-    // Enough CTAs to keep every SM streaming, within an 8-CTA cluster.
-    const int target = GDN_DECODE_TARGET_CTAS;
-    int ns = 1;
-    while (ns < 4 && (int64_t)B * Hv * ns < target && r * ns * 2 <= 8)
-        ns *= 2;
-    return ns;
-}
-
 template <typename TIn, int NTOK, typename TS = float>
 static cudaError_t fused_dispatch(const FusedArgs &a, cudaStream_t s)
 {
     const int r = a.Hv / a.Hq;
-    const int ns = pick_nsplit(a.B, a.Hv, r);
+    const int ns = pick_nsplit(a.B, a.Hv, r, a.sm_count);
     const dim3 grid(a.Hv * ns, a.B, 1);
     switch (ns) {
     case 1: return launch_cluster(decode_fused_kernel<TIn, NTOK, 1, TS>, grid, r, s, a);
@@ -386,7 +384,7 @@ cudaError_t launch_decay_gate(const void *alpha, bool bf16, int64_t alpha_stride
 cudaError_t launch_recurrence_decode(const RecArgs &a, cudaStream_t s)
 {
     const int r = a.Hv / a.Hq;
-    const int ns = pick_nsplit(a.B, a.Hv, r);
+    const int ns = pick_nsplit(a.B, a.Hv, r, sm_count());
     const dim3 grid(a.Hv * ns, a.B, 1);
     switch (ns) {
     case 1: recurrence_decode_kernel<1><<<grid, 256, 0, s>>>(a); break;
@@ -413,9 +411,14 @@ cudaError_t launch_gated_norm(const float *y, const float *w, const void *z, boo
 
 cudaError_t take_decode_device_error(int *code)
 {
-    // no kernel in this file waits on anything but hardware barriers
-    *code = 0;
-    return cudaSuccess;
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_decode_error, sizeof(int));
+    if (e == cudaSuccess && v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_decode_error, &zero, sizeof(int));
+    }
+    *code = v;
+    return e;
 }
 
 cudaError_t launch_verify_commit(float *state, float *conv_state, const float *state_snap,

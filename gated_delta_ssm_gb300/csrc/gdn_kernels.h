@@ -18,6 +18,7 @@ struct FusedArgs {
     int64_t x_stride, z_stride, gate_stride;
     int B, Hq, Hv, W, conv_dim;
     float l2_eps, rms_eps, scale;
+    int sm_count;          // SMs of the device (the bf16-state step's L2 prefetch distance)
 };
 
 struct ConvArgs {
@@ -87,6 +88,32 @@ constexpr size_t kPrefillQKImage = 65536;
 inline size_t prefill_workspace_bytes(int B, int Hq, int Hv, int n_chunks)
 {
     return (size_t)B * (size_t)n_chunks * ((size_t)Hv * kPrefillChunkImage + (size_t)Hq * kPrefillQKImage);
+}
+
+// Streaming multiprocessors of the current device, queried once per device.
+int sm_count();
+
+// Row slices per head of the single-token decode: enough CTAs (about four per
+// SM) to keep every SM streaming state, within an 8-CTA cluster (r CTAs share a
+// QK head, ns slices per head).
+inline int pick_nsplit(int B, int Hv, int r, int sms)
+{
+    int ns = 1;
+    while (ns < 4 && (int64_t)B * Hv * ns < 4 * (int64_t)sms && r * ns * 2 <= 8)
+        ns *= 2;
+    return ns;
+}
+
+// Row slices per head of the token-serial scans: as many as fill one wave of 2
+// CTAs per SM without spilling into a second (a token-serial CTA's duration is
+// its token count, so a partial second wave would double the time), within an
+// 8-CTA cluster.
+inline int scan_nsplit(int B, int Hv, int r, int sms)
+{
+    int ns = 1;
+    while (ns < 4 && (int64_t)B * Hv * ns * 2 <= 2 * (int64_t)sms && r * ns * 2 <= 8)
+        ns *= 2;
+    return ns;
 }
 
 // Default limit of a bounded wait, and the test-only override of one prefill

@@ -318,23 +318,11 @@ __global__ void __launch_bounds__(256) commit_kn_kernel(float *state, float *con
         conv_state[(size_t)b * hist_elems + i] = hsrc[i];
 }
 
-// Row slices per head: as many as fill one wave of 2 CTAs per SM without
-// spilling into a second (a token-serial CTA's duration is its token count,
-// so a partial second wave would double the time), within an 8-CTA cluster.
-int scan_nsplit(int B, int Hv, int r)
-{
-    const int64_t wave = 2 * 152;
-    int ns = 1;
-    while (ns < 4 && (int64_t)B * Hv * ns * 2 <= wave && r * ns * 2 <= 8)
-        ns *= 2;
-    return ns;
-}
-
 template <typename TIn>
 cudaError_t layer_scan_dispatch(const LayerScanArgs &a, cudaStream_t s)
 {
     const int r = a.Hv / a.Hq;
-    const int ns = scan_nsplit(a.B, a.Hv, r);
+    const int ns = scan_nsplit(a.B, a.Hv, r, sm_count());
     const dim3 grid(a.Hv * ns, a.B, 1);
     switch (ns) {
     case 1: return launch_cluster(layer_scan_kernel<TIn, 1>, grid, r, s, a);
@@ -347,7 +335,7 @@ cudaError_t layer_scan_dispatch(const LayerScanArgs &a, cudaStream_t s)
 
 cudaError_t launch_recurrence_scan(const RecScanArgs &a, cudaStream_t s)
 {
-    const int ns = scan_nsplit(a.B, a.Hv, 1);
+    const int ns = scan_nsplit(a.B, a.Hv, 1, sm_count());
     const dim3 grid(a.Hv * ns, a.B, 1);
     switch (ns) {
     case 1: recurrence_scan_kernel<1><<<grid, 256, 0, s>>>(a); break;

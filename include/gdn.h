@@ -224,8 +224,9 @@ gdn_status gdn_verify_k2(float *state, float *conv_state, float *state_snap, flo
  * Per sequence b with n_accept[b] (device int32 [B]):
  *   1 -> state[b] <- state_snap[b], conv_state[b] <- conv_snap[b]
  *        (bit-exact state after one decode step);
- *   2 -> nothing (state already holds both positions).
- * Any other value leaves sequence b unchanged, like 2.
+ *   2 -> nothing (state already holds both positions);
+ *   otherwise sequence b is left unchanged and bit 16 is set in the
+ *   device-side error word (see gdn_check_device).
  * Errors: INVALID_ARG (null, bad dims), UNSUPPORTED (d).
  */
 gdn_status gdn_verify_commit(float *state, float *conv_state, const float *state_snap,
@@ -387,7 +388,8 @@ gdn_status gdn_prefill_chunked_noalloc(float *state, float *conv_state, const vo
  *   bit 1   the chunked prefill's sequential pass gave up a wait
  *   bit 2   the chunked prefill's per-chunk transform pass gave up a wait
  *   bit 8   a copy or product the prefill issued did not finish in its drain
- *   bit 16  gdn_verify_commit_kn saw an accepted count outside 1..K
+ *   bit 16  gdn_verify_commit saw an accepted count outside 1..2, or
+ *           gdn_verify_commit_kn one outside 1..K
  *   bit 64  the multi-token conv gave up its tile-copy wait
  * The one wait not bounded by the library is the hardware's tensor-memory
  * allocation at the start of the prefill kernels, which lasts until CTAs of

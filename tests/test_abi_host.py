@@ -132,6 +132,29 @@ def test_testing_header_hook_is_exported(lib):
         assert hasattr(lib, name), name
 
 
+def test_row_splits_follow_the_sm_count(lib):
+    # the launchers size their grids from the device's SM count, not a fixed 152
+    for sms in (20, 132, 148, 152, 160, 170):
+        for B in (1, 2, 4, 32, 64):
+            for Hv in (8, 32, 48):
+                for r in (1, 2, 4):
+                    dec, scan = gdn.testing_row_splits(B, Hv, r, sms)
+                    assert dec in (1, 2, 4) and scan in (1, 2, 4)
+                    assert r * dec <= 8 and r * scan <= 8        # one cluster of r x split CTAs
+                    # the scans never spill a partial second wave of 2 CTAs per SM by splitting
+                    assert scan == 1 or B * Hv * scan <= 2 * sms
+                    # and split as far as that allows
+                    if scan < 4 and r * scan * 2 <= 8:
+                        assert B * Hv * scan * 2 > 2 * sms
+                    # the decode splits until about four CTAs per SM (or the cluster limit)
+                    if dec < 4 and r * dec * 2 <= 8:
+                        assert B * Hv * dec >= 4 * sms
+    # the GB300's 152 SMs: the benchmarked shapes keep their splits
+    assert gdn.testing_row_splits(1, 32, 2, 152) == (4, 4)     # one sequence, 16 / 32 heads
+    assert gdn.testing_row_splits(64, 48, 3, 152) == (1, 1)    # 64 sequences, 16 / 48 heads
+    assert gdn.testing_row_splits(32, 32, 2, 152) == (1, 1)    # 32 sequences, 16 / 32 heads
+
+
 def test_other_entry_points_validate(lib):
     cd = _dims().c()
     assert lib.gdn_decay_gate(None, 0, 4, FAKE, FAKE, FAKE, 1, 4, None) == gdn.GDN_ERR_INVALID_ARG

@@ -131,17 +131,23 @@ def test_verify_k2_matches_oracle_and_decode_bitwise():
     assert torch.equal(dev["hist"], want_hist)
 
 
-def test_commit_ignores_other_accept_values():
+def test_commit_flags_other_accept_values_and_leaves_them_unchanged():
     shape = synth.Shape(B=4, T=2, Hq=1, Hv=2, warm=True)
     inp = synth.make_inputs(shape, seed=9)
     dev = device_inputs(shape, inp)
     snap = torch.zeros_like(dev["state"])
     hsnap = torch.zeros_like(dev["hist"])
     before = dev["state"].clone(), dev["hist"].clone()
+    assert gdn.check_device() == 0
+    # 2 is a valid count (keep both positions); 0, 3 and -1 are out of range
     acc = torch.tensor([0, 2, 3, -1], dtype=torch.int32, device="cuda")
     gdn.verify_commit(dev["state"], dev["hist"], snap, hsnap, acc, dims_of(shape))
-    torch.cuda.synchronize()
+    assert gdn.check_device() == 16
     assert torch.equal(dev["state"], before[0]) and torch.equal(dev["hist"], before[1])
+    # valid counts only: nothing flagged
+    acc = torch.tensor([2, 2, 2, 2], dtype=torch.int32, device="cuda")
+    gdn.verify_commit(dev["state"], dev["hist"], snap, hsnap, acc, dims_of(shape))
+    assert gdn.check_device() == 0
 
 
 # ------------------------------------------------------------------ standalone parts
