@@ -696,7 +696,12 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
 
 // ================================================================== pass 2
 namespace p2 {
-constexpr int kThreads = 512;                     // 8 epilogue warps (warp 0 also issues), 8 conv warps
+// warps 0-7: epilogue (two per TMEM lane quarter); warp 8: the issuer; warps 9-12: the
+// V conv and the gated norm (16 tokens each). At most four warps share a scheduler, so
+// every thread keeps 128 registers.
+constexpr int kIssuerWarp = 8, kConvWarp0 = 9, kConvWarps = 8;
+constexpr int kConvThreads = 32 * kConvWarps, kConvTok = kC / kConvWarps;
+constexpr int kThreads = 32 * (kConvWarp0 + kConvWarps);
 constexpr uint32_t QB = 0;                        // Q rows of the chunk: two parts, [64 t][128 i] sw128
 constexpr uint32_t KB = 32768;                    // K rows, two buffers (even and odd chunks)
 constexpr uint32_t VF = 98304;                    // V^T fp32 footprint [128 j][64 t]
@@ -712,8 +717,8 @@ constexpr uint32_t BYTES = CONVW + kD * 16 + 1024;
 static_assert(BYTES <= 232448, "shared memory budget");
 static_assert(RAW % 1024 == 0 && KB % 1024 == 0, "tiles on 1 KB boundaries");
 // barriers: copies (expected bytes), products (commits), and role hand-offs
-enum { B_Q, B_K0, B_K1, B_T, B_P, B_RAW, B_M1, B_M1Q, B_M2, B_M3, B_PU,
-       B_RAWFREE, B_V, B_OSFREE,       // 256 conv threads arrive
+enum { B_Q, B_K0, B_K1, B_T, B_G, B_P, B_RAW, B_M1, B_M1Q, B_M2, B_M3, B_PU,
+       B_RAWFREE, B_V, B_OSFREE,       // the conv threads arrive
        B_ST, B_X, B_U, B_OR, B_OS,     // 256 epilogue threads arrive
        B_N };
 static_assert(B_N <= 24, "barrier slots");
@@ -788,7 +793,7 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
 
     if (tid == 0) {
         for (int i = 0; i < B_N; ++i)
-            tc::mbar_init(bar(i), i < B_RAWFREE ? 1 : 256);
+            tc::mbar_init(bar(i), i < B_RAWFREE ? 1 : i < B_ST ? kConvThreads : 256);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -807,10 +812,10 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
         return false;
     };
 
-    if (warp >= 8) {
+    if (warp >= kConvWarp0) {
         // ============================================ conv warps: chunk c's V rows, chunk c-1's norm
-        const int cw = warp - 8;
-        const bool raw_issuer = tid == 256;
+        const int cw = warp - kConvWarp0;
+        const bool raw_issuer = tid == 32 * kConvWarp0;
         int raw_last = -1;
         auto issue_raw = [&](int cc) {
             tc::mbar_expect_tx(bar(B_RAW), (uint32_t)(kC + W - 1) * kD * 2);
@@ -819,21 +824,24 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
         };
         if (staged && raw_issuer)
             issue_raw(0);
-        // V rows: 8 tokens (8 cw ..) x 4 channels (4 lane ..) per thread; 4-tap weights
+        // V rows: 16 tokens (16 cw ..) x 4 channels (4 lane ..) per thread; 4-tap weights
         // read once, channel 4 l + e at float4 [e][l] so that a warp's reads of one e
         // are consecutive
         const int v_ch = 2 * a.Hq * kD + h * kD + 4 * lane;
         const float4 *v_w = nullptr;
         if (WC == 4) {
             float4 *tab = reinterpret_cast<float4 *>(smem + CONVW);
-            for (int i = tid - 256; i < kD; i += 256)
+            for (int i = tid - 32 * kConvWarp0; i < kD; i += kConvThreads)
                 tab[i] = __ldg(reinterpret_cast<const float4 *>(a.conv_w + (size_t)(v_ch - 4 * lane + 4 * (i & 31) + (i >> 5)) * 4));
-            asm volatile("bar.sync 1, 256;" ::: "memory");   // the conv warps only
+            asm volatile("bar.sync 1, %0;" :: "n"(kConvThreads) : "memory");   // the conv warps only
             v_w = tab + lane;
         }
-        // gated-norm mapping: warp cw handles tokens cw, cw + 8, ...; lane holds channels 4 lane .. +3
+        // gated-norm mapping: warp cw handles tokens cw, cw + 4, ...; lane holds channels 4 lane .. +3
         const float4 nw4 = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane);
-        ZRaw<TIn> zpre[8];
+        // bf16 gate rows are held in registers from their load to the norm (2 per row);
+        // float rows are loaded where they are used
+        constexpr bool kZPre = sizeof(TIn) == 2;
+        ZRaw<TIn> zpre[kZPre ? kConvTok : 1];
         auto z_rows = [&](int cc) {
             return static_cast<const TIn *>(a.z) + ((int64_t)b * a.T + (int64_t)cc * kC) * a.z_stride +
                    (int64_t)h * kD + 4 * lane;
@@ -844,52 +852,71 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             const int n = min(kC, a.T - cc * kC);
             const TIn *zb = z_rows(cc);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (cw + 8 * i < n)
-                    asm volatile("prefetch.global.L2 [%0];" :: "l"(zb + (int64_t)(cw + 8 * i) * a.z_stride));
+            for (int i = 0; i < kConvTok; ++i)
+                if (cw + kConvWarps * i < n)
+                    asm volatile("prefetch.global.L2 [%0];" :: "l"(zb + (int64_t)(cw + kConvWarps * i) * a.z_stride));
         };
         auto z_fetch = [&](int cc) {
-            if (!zvec)
+            if (!zvec || !kZPre)
                 return;
             const int n = min(kC, a.T - cc * kC);
             const TIn *zb = z_rows(cc);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (cw + 8 * i < n)
-                    zpre[i].load(zb + (int64_t)(cw + 8 * i) * a.z_stride);
+            for (int i = 0; i < kConvTok; ++i)
+                if (cw + kConvWarps * i < n)
+                    zpre[kZPre ? i : 0].load(zb + (int64_t)(cw + kConvWarps * i) * a.z_stride);
         };
-        // ---- gated RMSNorm ("fm_kernel_ssm.h", "Gated RMSNorm") of chunk cc's staged rows
+        // ---- gated RMSNorm ("fm_kernel_ssm.h", "Gated RMSNorm") of chunk cc's staged rows,
+        //      four rows at a time with no branch between them, so that their latencies
+        //      overlap; rows at or past the end of the call are computed but not stored
         auto norm = [&](int cc) {
             const int c0 = cc * kC, n = min(kC, a.T - c0);
             const TIn *zb = z_rows(cc);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int t = cw + 8 * i;
-                if (t >= n)
-                    break;
-                const float4 y = *reinterpret_cast<const float4 *>(Os + t * kD + 4 * lane);
-                float ss = __fmul_rn(y.x, y.x);
-                ss = __fmaf_rn(y.y, y.y, ss);
-                ss = __fmaf_rn(y.z, y.z, ss);
-                ss = __fmaf_rn(y.w, y.w, ss);
-                ss = warp_sum32(ss);
-                const float inv = rsqrtf(__fadd_rn(__fmul_rn(ss, 1.0f / kD), a.rms_eps));
-                float zv[4];
-                if (zvec) {
-                    zpre[i].get(zv);
-                } else {
-                    const TIn *zr = zb + (int64_t)t * a.z_stride;
+            for (int g = 0; g < kConvTok; g += 4) {
+                float4 y[4];
+                float ss[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        zv[e] = load_act<TIn>(zr + e);
+                for (int r = 0; r < 4; ++r) {
+                    const int t = cw + kConvWarps * (g + r);
+                    y[r] = *reinterpret_cast<const float4 *>(Os + t * kD + 4 * lane);
+                    ss[r] = __fmul_rn(y[r].x, y[r].x);
+                    ss[r] = __fmaf_rn(y[r].y, y[r].y, ss[r]);
+                    ss[r] = __fmaf_rn(y[r].z, y[r].z, ss[r]);
+                    ss[r] = __fmaf_rn(y[r].w, y[r].w, ss[r]);
                 }
-                float4 o;
-                o.x = gated_out(y.x, inv, nw4.x, zv[0]);
-                o.y = gated_out(y.y, inv, nw4.y, zv[1]);
-                o.z = gated_out(y.z, inv, nw4.z, zv[2]);
-                o.w = gated_out(y.w, inv, nw4.w, zv[3]);
-                const int64_t row = (int64_t)b * a.T + c0 + t;
-                *reinterpret_cast<float4 *>(a.out + (row * a.Hv + h) * kD + 4 * lane) = o;
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        ss[r] = __fadd_rn(ss[r], __shfl_xor_sync(0xffffffffu, ss[r], m));
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int t = cw + kConvWarps * (g + r);
+                    const bool live = t < n;
+                    const float inv = rsqrtf(__fadd_rn(__fmul_rn(ss[r], 1.0f / kD), a.rms_eps));
+                    float zv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    const TIn *zr = zb + (int64_t)t * a.z_stride;
+                    if (zvec && kZPre) {
+                        zpre[kZPre ? g + r : 0].get(zv);
+                    } else if (live) {
+                        if (zvec) {
+                            load_row<4, TIn>(zr, zv);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                zv[e] = load_act<TIn>(zr + e);
+                        }
+                    }
+                    float4 o;
+                    o.x = gated_out(y[r].x, inv, nw4.x, zv[0]);
+                    o.y = gated_out(y[r].y, inv, nw4.y, zv[1]);
+                    o.z = gated_out(y[r].z, inv, nw4.z, zv[2]);
+                    o.w = gated_out(y[r].w, inv, nw4.w, zv[3]);
+                    const int64_t row = (int64_t)b * a.T + c0 + t;
+                    if (live)
+                        *reinterpret_cast<float4 *>(a.out + (row * a.Hv + h) * kD + 4 * lane) = o;
+                }
             }
         };
         bool ok = true;
@@ -900,8 +927,28 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 z_prefetch(c - 1);
             if (staged && !(ok = waitb(B_RAW, c & 1, lim)))
                 break;
-            float v[8][4];
-            conv_block<TIn, WC, 4>(a, b, c0, n, v_ch, 8 * cw, staged != 0, sbase + RAW, v, v_w, 32);
+            // V^T of chunk c, 8 tokens at a time, written once chunk c-1's X has read the
+            // footprint
+            bool x_seen = c == 0;
+#pragma unroll
+            for (int k = 0; k < kConvTok / 8; ++k) {
+                float v[8][4];
+                conv_block<TIn, WC, 4>(a, b, c0, n, v_ch, kConvTok * cw + 8 * k, staged != 0, sbase + RAW,
+                                       v, v_w, 32);
+                if (!x_seen && !(ok = x_seen = waitb(B_X, (c - 1) & 1, lim)))
+                    break;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 4 * lane + e;
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        *reinterpret_cast<float4 *>(smem + foot_off(j, kConvTok / 4 * cw + 2 * k + q)) =
+                            make_float4(v[4 * q][e], v[4 * q + 1][e], v[4 * q + 2][e], v[4 * q + 3][e]);
+                }
+            }
+            if (!ok)
+                break;
+            tc::mbar_arrive(bar(B_V));
             if (staged && c + 1 < nch) {
                 // the staged rows are read: the next chunk's may come in. The issuer's whole
                 // warp waits, so that the warp stays converged for the work after it.
@@ -914,18 +961,6 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 if (!ok)
                     break;
             }
-            // V^T of chunk c, once chunk c-1's X has read the footprint
-            if (c > 0 && !(ok = waitb(B_X, (c - 1) & 1, lim)))
-                break;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j = 4 * lane + e;
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-                    *reinterpret_cast<float4 *>(smem + foot_off(j, 2 * cw + q)) =
-                        make_float4(v[4 * q][e], v[4 * q + 1][e], v[4 * q + 2][e], v[4 * q + 3][e]);
-            }
-            tc::mbar_arrive(bar(B_V));
             // the norm of chunk c-1, whose rows the epilogue has staged
             if (c > 0) {
                 z_fetch(c - 1);
@@ -943,158 +978,198 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
         // drain: the staged-row copy in flight lands before the CTA ends
         if (raw_issuer && raw_last >= 0 && !tc::mbar_wait_ns(bar(B_RAW), raw_last & 1, lim))
             atomicOr(&g_device_error, (int)kErrDrain);
-    } else {
-        // ============================================ epilogue warps: value row j
-        // Lane 0 of warp 0 also issues every workspace copy and tensor-core product,
-        // at the points of its own program where their inputs are ready. The products
-        // the next chunk waits for (K S_0, U = T X, the state update) are issued apart
-        // from those only the readout needs ((Q S_0)^T, (P U)^T), which run on the
-        // tensor core while the epilogue works.
-        const bool issuer = tid == 0;
-        int q_last = -1, k_last0 = -1, k_last1 = -1, t_last = -1, p_last = -1, last_commit = -1;
-        uint32_t last_phase = 0;
-        auto issue_q = [&](int cc) {     // Q rows of chunk cc
-            tc::mbar_expect_tx(bar(B_Q), kQKRows);
-            tc::bulk_copy_g2s(sbase + QB, qk_image(a, b, hk, cc), kQKRows, bar(B_Q));
-            q_last = cc;
-        };
-        auto issue_k = [&](int cc) {     // K rows of chunk cc, into the buffer of its parity
-            const int kb = cc & 1;
-            tc::mbar_expect_tx(bar(B_K0 + kb), kQKRows);
-            tc::bulk_copy_g2s(sbase + KB + kb * kQKRows, qk_image(a, b, hk, cc) + kQKRows, kQKRows,
-                              bar(B_K0 + kb));
-            (kb ? k_last1 : k_last0) = cc;
-        };
-        auto issue_t = [&](int cc) {     // T image and gates of chunk cc
-            const uint8_t *img = chunk_image(a, b, h, cc);
-            tc::mbar_expect_tx(bar(B_T), 16384u + (uint32_t)sizeof(Gates));
-            tc::bulk_copy_g2s(sbase + TT, img, 16384u, bar(B_T));
-            tc::bulk_copy_g2s(sbase + GATES + (cc & 1) * (uint32_t)sizeof(Gates), img + kImgGates,
-                              (uint32_t)sizeof(Gates), bar(B_T));
-            t_last = cc;
-        };
-        auto issue_p = [&](int cc) {     // P image of chunk cc
-            tc::mbar_expect_tx(bar(B_P), 16384u);
-            tc::bulk_copy_g2s(sbase + PP, chunk_image(a, b, h, cc) + kImgP, 16384u, bar(B_P));
-            p_last = cc;
-        };
-        auto commit = [&](int i, int c) {   // a commit tracks every product issued before it
-            tc::mma_commit(bar(i));
-            last_commit = i;
-            last_phase = c & 1;
-        };
-        const uint32_t id64 = tc::idesc_f16(128, 64);
-        const uint32_t id128 = tc::idesc_f16(128, 128);
-        // D1[:, 64..127] = S_0^T K^T, once the K rows and S_0^T are ready
-        auto issue_m1k = [&](int c) -> bool {
-            const int kb = c & 1;
-            // the first wait of the kernel takes its limit from first_wait_ns (a test hook)
-            if (!waitb(B_K0 + kb, (c >> 1) & 1, c == 0 ? a.first_wait_ns : lim) || !waitb(B_ST, c & 1, lim))
-                return false;
-            tc::fence_after_sync();
-            const uint32_t kt = sbase + KB + kb * kQKRows;
+    } else if (warp == kIssuerWarp) {
+        // ============================================ issuer: every workspace copy and product
+        // Lane 0 walks the chunks, issuing each copy and product as soon as its inputs are
+        // ready and its destination is free. The products the next chunk waits for (K S_0,
+        // U = T X, the state update) go out apart from those only the readout needs
+        // ((Q S_0)^T, (P U)^T), which run on the tensor core while the epilogue works.
+        if (lane == 0) {
+            int q_last = -1, k_last0 = -1, k_last1 = -1, t_last = -1, g_last = -1, p_last = -1;
+            int last_commit = -1;
+            uint32_t last_phase = 0;
+            auto issue_q = [&](int cc) {     // Q rows of chunk cc
+                tc::mbar_expect_tx(bar(B_Q), kQKRows);
+                tc::bulk_copy_g2s(sbase + QB, qk_image(a, b, hk, cc), kQKRows, bar(B_Q));
+                q_last = cc;
+            };
+            auto issue_k = [&](int cc) {     // K rows of chunk cc, into the buffer of its parity
+                const int kb = cc & 1;
+                tc::mbar_expect_tx(bar(B_K0 + kb), kQKRows);
+                tc::bulk_copy_g2s(sbase + KB + kb * kQKRows, qk_image(a, b, hk, cc) + kQKRows, kQKRows,
+                                  bar(B_K0 + kb));
+                (kb ? k_last1 : k_last0) = cc;
+            };
+            auto issue_t = [&](int cc) {     // T image of chunk cc
+                tc::mbar_expect_tx(bar(B_T), 16384u);
+                tc::bulk_copy_g2s(sbase + TT, chunk_image(a, b, h, cc), 16384u, bar(B_T));
+                t_last = cc;
+            };
+            auto issue_g = [&](int cc) {     // gates of chunk cc, into the buffer of its parity
+                tc::mbar_expect_tx(bar(B_G), (uint32_t)sizeof(Gates));
+                tc::bulk_copy_g2s(sbase + GATES + (cc & 1) * (uint32_t)sizeof(Gates),
+                                  chunk_image(a, b, h, cc) + kImgGates, (uint32_t)sizeof(Gates), bar(B_G));
+                g_last = cc;
+            };
+            auto issue_p = [&](int cc) {     // P image of chunk cc
+                tc::mbar_expect_tx(bar(B_P), 16384u);
+                tc::bulk_copy_g2s(sbase + PP, chunk_image(a, b, h, cc) + kImgP, 16384u, bar(B_P));
+                p_last = cc;
+            };
+            auto commit = [&](int i, int c) {   // a commit tracks every product issued before it
+                tc::mma_commit(bar(i));
+                last_commit = i;
+                last_phase = c & 1;
+            };
+            const uint32_t id64 = tc::idesc_f16(128, 64);
+            const uint32_t id128 = tc::idesc_f16(128, 128);
+            // D1[:, 64..127] = S_0^T K^T, once the K rows and S_0^T are ready
+            auto issue_m1k = [&](int c) -> bool {
+                const int kb = c & 1;
+                // the first wait of the kernel takes its limit from first_wait_ns (a test hook)
+                if (!waitb(B_K0 + kb, (c >> 1) & 1, c == 0 ? a.first_wait_ns : lim) ||
+                    !waitb(B_ST, c & 1, lim))
+                    return false;
+                tc::fence_after_sync();
+                const uint32_t kt = sbase + KB + kb * kQKRows;
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-                const uint32_t ko = (kk >> 2) * 8192 + (kk & 3) * 32;   // column block, 16 channels
-                const uint32_t shi = tmem + R1 + 8 * kk, slo = tmem + R1 + 64 + 8 * kk;
-                const uint64_t k1 = tc::sdesc_sw128(kt + ko), k2 = tc::sdesc_sw128(kt + kQKPart + ko);
-                tc::mma_f16_ta(tmem + D1 + kC, shi, k1, id64, kk > 0);
-                tc::mma_f16_ta(tmem + D1 + kC, shi, k2, id64, 1);
-                tc::mma_f16_ta(tmem + D1 + kC, slo, k1, id64, 1);
-            }
-            commit(B_M1, c);
-            return true;
-        };
-        // D1[:, 0..63] = S_0^T Q^T, once the Q rows are in and the previous chunk's readout
-        // has read these columns
-        auto issue_m1q = [&](int c) -> bool {
-            if ((c > 0 && !waitb(B_OR, (c - 1) & 1, lim)) || !waitb(B_Q, c & 1, lim))
-                return false;
-            tc::fence_after_sync();
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t ko = (kk >> 2) * 8192 + (kk & 3) * 32;   // column block, 16 channels
+                    const uint32_t shi = tmem + R1 + 8 * kk, slo = tmem + R1 + 64 + 8 * kk;
+                    const uint64_t k1 = tc::sdesc_sw128(kt + ko), k2 = tc::sdesc_sw128(kt + kQKPart + ko);
+                    tc::mma_f16_ta(tmem + D1 + kC, shi, k1, id64, kk > 0);
+                    tc::mma_f16_ta(tmem + D1 + kC, shi, k2, id64, 1);
+                    tc::mma_f16_ta(tmem + D1 + kC, slo, k1, id64, 1);
+                }
+                commit(B_M1, c);
+                return true;
+            };
+            // D1[:, 0..63] = S_0^T Q^T, once the Q rows are in and the previous chunk's readout
+            // has read these columns
+            auto issue_m1q = [&](int c) -> bool {
+                if ((c > 0 && !waitb(B_OR, (c - 1) & 1, lim)) || !waitb(B_Q, c & 1, lim))
+                    return false;
+                tc::fence_after_sync();
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-                const uint32_t ko = (kk >> 2) * 8192 + (kk & 3) * 32;
-                const uint32_t shi = tmem + R1 + 8 * kk, slo = tmem + R1 + 64 + 8 * kk;
-                const uint64_t q1 = tc::sdesc_sw128(sbase + QB + ko), q2 = tc::sdesc_sw128(sbase + QB + kQKPart + ko);
-                tc::mma_f16_ta(tmem + D1, shi, q1, id64, kk > 0);
-                tc::mma_f16_ta(tmem + D1, shi, q2, id64, 1);
-                tc::mma_f16_ta(tmem + D1, slo, q1, id64, 1);
-            }
-            commit(B_M1Q, c);
-            return true;
-        };
-        // D2 = X^T T^T, once every value row's X^T is in TMEM and T has arrived; the Q rows
-        // of the next chunk once this chunk's (Q S_0)^T has read them (that product also
-        // has to finish before U'^T overwrites the low part of S_0^T)
-        auto issue_m2 = [&](int c) -> bool {
-            if (!waitb(B_X, c & 1, lim) || !waitb(B_T, c & 1, lim) || !waitb(B_M1Q, c & 1, lim))
-                return false;
-            tc::fence_after_sync();
-            if (c + 1 < nch)
-                issue_q(c + 1);
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t ko = (kk >> 2) * 8192 + (kk & 3) * 32;
+                    const uint32_t shi = tmem + R1 + 8 * kk, slo = tmem + R1 + 64 + 8 * kk;
+                    const uint64_t q1 = tc::sdesc_sw128(sbase + QB + ko);
+                    const uint64_t q2 = tc::sdesc_sw128(sbase + QB + kQKPart + ko);
+                    tc::mma_f16_ta(tmem + D1, shi, q1, id64, kk > 0);
+                    tc::mma_f16_ta(tmem + D1, shi, q2, id64, 1);
+                    tc::mma_f16_ta(tmem + D1, slo, q1, id64, 1);
+                }
+                commit(B_M1Q, c);
+                return true;
+            };
+            // D2 = X^T T^T, once every value row's X^T is in TMEM and T has arrived; the next
+            // chunk's gates (every value row has read chunk c-1's) and its Q rows once this
+            // chunk's (Q S_0)^T has read them (that product also has to finish before U'^T
+            // overwrites the low part of S_0^T)
+            auto issue_m2 = [&](int c) -> bool {
+                if (!waitb(B_X, c & 1, lim))
+                    return false;
+                if (c + 1 < nch)
+                    issue_g(c + 1);
+                if (!waitb(B_T, c & 1, lim) || !waitb(B_M1Q, c & 1, lim))
+                    return false;
+                tc::fence_after_sync();
+                if (c + 1 < nch)
+                    issue_q(c + 1);
 #pragma unroll
-            for (int kk = 0; kk < kC / 16; ++kk) {
-                const uint64_t b1 = tc::sdesc(sbase + TT + kk * 256, 128, 1024);
-                const uint64_t b2 = tc::sdesc(sbase + TT + 8192 + kk * 256, 128, 1024);
-                const uint32_t xhi = tmem + XU + 8 * kk, xlo = tmem + XU + 32 + 8 * kk;
-                tc::mma_f16_ta(tmem + D2, xhi, b1, id64, kk > 0);
-                tc::mma_f16_ta(tmem + D2, xhi, b2, id64, 1);
-                tc::mma_f16_ta(tmem + D2, xlo, b1, id64, 1);
-            }
-            commit(B_M2, c);
-            return true;
-        };
-        // S^T += U'^T K (K rows read MN-major), then (P U)^T = U^T P^T into D2 (U^T has been
-        // read from it); T and gates of the next chunk first (this chunk's T was read by
-        // D2's product, and its gates' buffer last served chunk c-1)
-        auto issue_m3 = [&](int c) -> bool {
-            if (c + 1 < nch)
-                issue_t(c + 1);
-            if (!waitb(B_U, c & 1, lim) || !waitb(B_P, c & 1, lim))
-                return false;
-            tc::fence_after_sync();
-            const uint32_t kt = sbase + KB + (c & 1) * kQKRows;
+                for (int kk = 0; kk < kC / 16; ++kk) {
+                    const uint64_t b1 = tc::sdesc(sbase + TT + kk * 256, 128, 1024);
+                    const uint64_t b2 = tc::sdesc(sbase + TT + 8192 + kk * 256, 128, 1024);
+                    const uint32_t xhi = tmem + XU + 8 * kk, xlo = tmem + XU + 32 + 8 * kk;
+                    tc::mma_f16_ta(tmem + D2, xhi, b1, id64, kk > 0);
+                    tc::mma_f16_ta(tmem + D2, xhi, b2, id64, 1);
+                    tc::mma_f16_ta(tmem + D2, xlo, b1, id64, 1);
+                }
+                commit(B_M2, c);
+                return true;
+            };
+            // the next chunk's T once D2's product has read this chunk's; then S^T += U'^T K (K
+            // rows read MN-major) and (P U)^T = U^T P^T into D2 (U^T has been read from it)
+            auto issue_m3 = [&](int c) -> bool {
+                if (!waitb(B_M2, c & 1, lim))
+                    return false;
+                if (c + 1 < nch)
+                    issue_t(c + 1);
+                if (!waitb(B_U, c & 1, lim) || !waitb(B_P, c & 1, lim))
+                    return false;
+                tc::fence_after_sync();
+                const uint32_t kt = sbase + KB + (c & 1) * kQKRows;
 #pragma unroll
-            for (int kk = 0; kk < kC / 16; ++kk) {
-                const uint32_t koff = kk * 2048;    // K rows 16kk.. : 8-row groups 1 KB apart
-                const uint64_t k1 = tc::sdesc_sw128_mn(kt + koff, 8192, 1024);
-                const uint64_t k2 = tc::sdesc_sw128_mn(kt + kQKPart + koff, 8192, 1024);
-                const uint32_t uphi = tmem + R1 + 64 + 8 * kk, uplo = tmem + R1 + 96 + 8 * kk;
-                tc::mma_f16_ta(tmem + TS, uphi, k1, id128 | tc::kIdescTransB, 1);
-                tc::mma_f16_ta(tmem + TS, uphi, k2, id128 | tc::kIdescTransB, 1);
-                tc::mma_f16_ta(tmem + TS, uplo, k1, id128 | tc::kIdescTransB, 1);
-            }
-            commit(B_M3, c);
+                for (int kk = 0; kk < kC / 16; ++kk) {
+                    const uint32_t koff = kk * 2048;    // K rows 16kk.. : 8-row groups 1 KB apart
+                    const uint64_t k1 = tc::sdesc_sw128_mn(kt + koff, 8192, 1024);
+                    const uint64_t k2 = tc::sdesc_sw128_mn(kt + kQKPart + koff, 8192, 1024);
+                    const uint32_t uphi = tmem + R1 + 64 + 8 * kk, uplo = tmem + R1 + 96 + 8 * kk;
+                    tc::mma_f16_ta(tmem + TS, uphi, k1, id128 | tc::kIdescTransB, 1);
+                    tc::mma_f16_ta(tmem + TS, uphi, k2, id128 | tc::kIdescTransB, 1);
+                    tc::mma_f16_ta(tmem + TS, uplo, k1, id128 | tc::kIdescTransB, 1);
+                }
+                commit(B_M3, c);
 #pragma unroll
-            for (int kk = 0; kk < kC / 16; ++kk) {
-                const uint64_t p1d = tc::sdesc(sbase + PP + kk * 256, 128, 1024);
-                const uint64_t p2d = tc::sdesc(sbase + PP + 8192 + kk * 256, 128, 1024);
-                const uint32_t uhi = tmem + XU + 8 * kk, ulo = tmem + XU + 32 + 8 * kk;
-                tc::mma_f16_ta(tmem + D2, uhi, p1d, id64, kk > 0);
-                tc::mma_f16_ta(tmem + D2, uhi, p2d, id64, 1);
-                tc::mma_f16_ta(tmem + D2, ulo, p1d, id64, 1);
-            }
-            commit(B_PU, c);
-            return true;
-        };
-        // warp 0 runs the issuer's step; all its lanes learn whether it succeeded
-        auto warp0_issue = [&](auto &&step, int c) -> bool {
-            bool res = true;
-            if (warp == 0) {
-                if (issuer)
-                    res = step(c);
-                res = __shfl_sync(0xffffffffu, res, 0);
-            }
-            return res;
-        };
-        if (issuer) {
+                for (int kk = 0; kk < kC / 16; ++kk) {
+                    const uint64_t p1d = tc::sdesc(sbase + PP + kk * 256, 128, 1024);
+                    const uint64_t p2d = tc::sdesc(sbase + PP + 8192 + kk * 256, 128, 1024);
+                    const uint32_t uhi = tmem + XU + 8 * kk, ulo = tmem + XU + 32 + 8 * kk;
+                    tc::mma_f16_ta(tmem + D2, uhi, p1d, id64, kk > 0);
+                    tc::mma_f16_ta(tmem + D2, uhi, p2d, id64, 1);
+                    tc::mma_f16_ta(tmem + D2, ulo, p1d, id64, 1);
+                }
+                commit(B_PU, c);
+                return true;
+            };
             issue_k(0);
             if (nch > 1)
                 issue_k(1);
             issue_q(0);
+            issue_g(0);
             issue_t(0);
             issue_p(0);
+            bool ok = issue_m1k(0) && issue_m1q(0);
+#pragma unroll 1
+            for (int c = 0; ok && c < nch; ++c) {
+                if (!(ok = issue_m2(c) && issue_m3(c)) || c + 1 >= nch)
+                    break;
+                // this chunk's K rows have been read by both of its products
+                if (!(ok = waitb(B_M3, c & 1, lim)))
+                    break;
+                if (c + 2 < nch)
+                    issue_k(c + 2);
+                if (!(ok = issue_m1k(c + 1)))
+                    break;
+                // this chunk's P has been read by its product
+                if (!(ok = waitb(B_PU, c & 1, lim)))
+                    break;
+                issue_p(c + 1);
+                ok = issue_m1q(c + 1);
+            }
+            // drain: copies and products in flight finish before the CTA releases TMEM
+            bool drained = true;
+            if (last_commit >= 0)
+                drained &= tc::mbar_wait_ns(bar(last_commit), last_phase, lim);
+            if (q_last >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_Q), q_last & 1, lim);
+            if (k_last0 >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_K0), (k_last0 >> 1) & 1, lim);
+            if (k_last1 >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_K1), (k_last1 >> 1) & 1, lim);
+            if (t_last >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_T), t_last & 1, lim);
+            if (g_last >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_G), g_last & 1, lim);
+            if (p_last >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_P), p_last & 1, lim);
+            if (!drained)
+                atomicOr(&g_device_error, (int)kErrDrain);
         }
+        __syncwarp();
+    } else {
+        // ============================================ epilogue warps: value row j
         const int q4 = warp & 3, hf = warp >> 2;
         const int j = 32 * q4 + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
@@ -1126,12 +1201,12 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             tc::tmem_st16(tl + TS + 64 * hf + 16 * k, v16);
         }
         state_operand();
-        bool ok = warp0_issue(issue_m1k, 0) && warp0_issue(issue_m1q, 0);
+        bool ok = true;
         int rho = 0;   // this chunk's state scale
 #pragma unroll 1
         for (int c = 0; ok && c < nch; ++c) {
             const uint32_t par = c & 1;
-            ok = waitb(B_M1, par, lim) && waitb(B_V, par, lim) && waitb(B_T, par, lim);
+            ok = waitb(B_M1, par, lim) && waitb(B_V, par, lim) && waitb(B_G, par, lim);
             if (!ok)
                 break;
             tc::fence_after_sync();
@@ -1175,8 +1250,6 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             tc::tmem_wait_st();
             tc::fence_before_sync();
             tc::mbar_arrive(bar(B_X));
-            if (!(ok = warp0_issue(issue_m2, c)))
-                break;
             // ---- U = T X (from D2): U^T for the output product, U'^T = U^T diag(e^{Gam_C - Gam})
             //      for the state update
             if (!(ok = waitb(B_M2, par, lim)))
@@ -1206,18 +1279,12 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             tc::tmem_wait_st();
             tc::fence_before_sync();
             tc::mbar_arrive(bar(B_U));
-            if (!(ok = warp0_issue(issue_m3, c)))
-                break;
-            // ---- the updated state: the next chunk's S_0^T operand and its first product
+            // ---- the updated state: the next chunk's S_0^T operand (its first product follows)
             if (!(ok = waitb(B_M3, par, lim)))
                 break;
             tc::fence_after_sync();
-            if (issuer && c + 2 < nch)   // this chunk's K rows have been read by both products
-                issue_k(c + 2);
             if (c + 1 < nch) {
                 state_operand();
-                if (!(ok = warp0_issue(issue_m1k, c + 1)))
-                    break;
             } else {
                 // ---- final state back to HBM (S^T rows = the library layout), unscaled
                 const float us = exp2i(-rho_next);
@@ -1259,12 +1326,6 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             }
             tc::fence_before_sync();
             tc::mbar_arrive(bar(B_OR));
-            if (c + 1 < nch) {
-                if (issuer)                // this chunk's P has been read by its product
-                    issue_p(c + 1);
-                if (!(ok = warp0_issue(issue_m1q, c + 1)))
-                    break;
-            }
             // ---- token-major staging for the conv warps' norm, once they have read chunk c-1's
             if (c > 0 && !(ok = waitb(B_OSFREE, (c - 1) & 1, lim)))
                 break;
@@ -1276,25 +1337,6 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             tc::mbar_arrive(bar(B_OS));
             rho = rho_next;
         }
-        if (issuer) {
-            // drain: copies and products in flight finish before the CTA releases TMEM
-            bool drained = true;
-            if (last_commit >= 0)   // a commit tracks every product issued before it
-                drained &= tc::mbar_wait_ns(bar(last_commit), last_phase, lim);
-            if (q_last >= 0)
-                drained &= tc::mbar_wait_ns(bar(B_Q), q_last & 1, lim);
-            if (k_last0 >= 0)
-                drained &= tc::mbar_wait_ns(bar(B_K0), (k_last0 >> 1) & 1, lim);
-            if (k_last1 >= 0)
-                drained &= tc::mbar_wait_ns(bar(B_K1), (k_last1 >> 1) & 1, lim);
-            if (t_last >= 0)
-                drained &= tc::mbar_wait_ns(bar(B_T), t_last & 1, lim);
-            if (p_last >= 0)
-                drained &= tc::mbar_wait_ns(bar(B_P), p_last & 1, lim);
-            if (!drained)
-                atomicOr(&g_device_error, (int)kErrDrain);
-        }
-        __syncwarp();
     }
 
     // ---- teardown
