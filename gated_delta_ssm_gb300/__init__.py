@@ -19,7 +19,8 @@ import threading as _th
 __all__ = [
     "Dims", "Params", "GdnError", "load", "library_path",
     "decay_gate", "conv_update", "recurrence_decode", "gated_norm",
-    "decode_step", "verify_k2", "verify_commit", "prefill_chunked", "prefill_workspace_bytes",
+    "decode_step", "decode_step_select", "verify_k2", "verify_commit", "prefill_chunked",
+    "prefill_workspace_bytes",
     "recurrence_scan",
     "layer_scan", "verify_kn", "verify_commit_kn", "decode_step_bf16_state", "check_device",
     "version",
@@ -115,6 +116,8 @@ def load():
             "gdn_decode_step": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, vp],
             "gdn_decode_step_bf16_state": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, vp],
             "gdn_verify_k2": [vp, vp, vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, vp],
+            "gdn_decode_step_select": [vp, vp, vp, vp, i32, vp, i32, vp, vp, vp, vp, _ct.c_int, pp,
+                                       vp, pd, vp],
             "gdn_verify_commit": [vp, vp, vp, vp, vp, pd, vp],
             "gdn_prefill_chunked": [vp, vp, vp, vp, vp, vp, _ct.c_int, pp, vp, pd, i32, i32, vp,
                                     _ct.c_size_t, vp],
@@ -299,6 +302,23 @@ def decode_step_bf16_state(state, conv_state, x, z, alpha, beta_logit, params: P
                                              _ct.byref(cp), _dev(out, "out", ("bfloat16",)),
                                              _ct.byref(cd), _stream(stream)),
            "gdn_decode_step_bf16_state")
+
+
+def decode_step_select(state, conv_state, state_snap, conv_snap, conv_snap_entries: int, n_accept,
+                       n_draft: int, x, z, alpha, beta_logit, params: Params, out, dims: Dims,
+                       stream=None):
+    """The step after a K-token verify, each sequence starting from the snapshot its accepted
+    count selects; see gdn_decode_step_select."""
+    cd, cp = dims.c(), params.c()
+    _check(load().gdn_decode_step_select(_dev(state, "state", _F32),
+                                         _dev(conv_state, "conv_state", _F32),
+                                         _dev(state_snap, "state_snap", _F32),
+                                         _dev(conv_snap, "conv_snap", _F32), conv_snap_entries,
+                                         _dev(n_accept, "n_accept", _I32), n_draft,
+                                         *_acts(x, z, alpha, beta_logit, cd), _dtype(x),
+                                         _ct.byref(cp), _dev(out, "out", _F32), _ct.byref(cd),
+                                         _stream(stream)),
+           "gdn_decode_step_select")
 
 
 def verify_k2(state, conv_state, state_snap, conv_snap, x, z, alpha, beta_logit, params: Params,

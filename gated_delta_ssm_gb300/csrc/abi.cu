@@ -104,7 +104,9 @@ int conv_dim_of(const gdn_dims *d) { return (2 * d->n_qk_heads + d->n_v_heads) *
 gdn_status fused_common(void *state, float *conv_state, float *state_snap, float *conv_snap,
                         const void *x, const void *z, const void *alpha, const void *beta_logit,
                         gdn_dtype act_dtype, const gdn_params *params, void *out,
-                        const gdn_dims *dims, int ntok, bool bf16_state, gdn_stream_t stream)
+                        const gdn_dims *dims, int ntok, bool bf16_state, gdn_stream_t stream,
+                        const int32_t *n_accept = nullptr, int n_draft = 0,
+                        int conv_snap_entries = 0)
 {
     gdn_status st = check_dims(dims, 7);
     if (st != GDN_OK)
@@ -149,6 +151,9 @@ gdn_status fused_common(void *state, float *conv_state, float *state_snap, float
     a.rms_eps = params->rms_eps;
     a.scale = 1.0f / sqrtf((float)dims->head_dim);
     a.sm_count = gdn::sm_count();
+    a.n_accept = n_accept;
+    a.n_draft = n_draft;
+    a.conv_snap_entries = conv_snap_entries;
     if (bf16_state)
         return from_cuda(gdn::launch_decode_fused_bf16_state(a, act_dtype == GDN_BF16,
                                                              as_cuda(stream)));
@@ -202,6 +207,13 @@ gdn_status layer_scan_common(float *state, float *conv_state, float *state_snap,
     a.rms_eps = params->rms_eps;
     a.scale = 1.0f / sqrtf((float)dims->head_dim);
     return from_cuda(gdn::launch_layer_scan(a, act_dtype == GDN_BF16, as_cuda(stream)));
+}
+
+// [p, p + pb) and [q, q + qb) share a byte
+bool overlaps(const void *p, size_t pb, const void *q, size_t qb)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), c = reinterpret_cast<uintptr_t>(q);
+    return a < c + qb && c < a + pb;
 }
 
 }  // namespace
@@ -303,6 +315,34 @@ gdn_status gdn_decode_step_bf16_state(void *state, float *conv_state, const void
 {
     return fused_common(state, conv_state, nullptr, nullptr, x, z, alpha, beta_logit, act_dtype,
                         params, out, dims, 1, true, stream);
+}
+
+gdn_status gdn_decode_step_select(float *state, float *conv_state, const float *state_snap,
+                                  const float *conv_snap, int32_t conv_snap_entries,
+                                  const int32_t *n_accept, int32_t n_draft, const void *x,
+                                  const void *z, const void *alpha, const void *beta_logit,
+                                  gdn_dtype act_dtype, const gdn_params *params, float *out,
+                                  const gdn_dims *dims, gdn_stream_t stream)
+{
+    gdn_status st = check_dims(dims, 7);
+    if (st != GDN_OK)
+        return st;
+    if (!n_accept || n_draft < 1)
+        return GDN_ERR_INVALID_ARG;
+    if (n_draft > 1) {
+        if (!state_snap || !conv_snap || (conv_snap_entries != n_draft - 1 && conv_snap_entries != n_draft))
+            return GDN_ERR_INVALID_ARG;
+        const size_t B = (size_t)dims->n_seq, d = (size_t)dims->head_dim;
+        const size_t sbytes = B * dims->n_v_heads * d * d * 4;
+        const size_t hbytes = B * (size_t)conv_dim_of(dims) * (size_t)(dims->d_conv - 1) * 4;
+        const size_t ssnap = sbytes * (size_t)(n_draft - 1), hsnap = hbytes * (size_t)conv_snap_entries;
+        if (overlaps(state, sbytes, state_snap, ssnap) || overlaps(conv_state, hbytes, conv_snap, hsnap) ||
+            overlaps(state, sbytes, conv_snap, hsnap) || overlaps(conv_state, hbytes, state_snap, ssnap))
+            return GDN_ERR_INVALID_ARG;
+    }
+    return fused_common(state, conv_state, const_cast<float *>(state_snap), const_cast<float *>(conv_snap),
+                        x, z, alpha, beta_logit, act_dtype, params, out, dims, 1, false, stream,
+                        n_accept, n_draft, n_draft > 1 ? conv_snap_entries : 0);
 }
 
 gdn_status gdn_verify_k2(float *state, float *conv_state, float *state_snap, float *conv_snap,

@@ -159,10 +159,30 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
     // (1) this warp's state rows: loads in flight during the prologue
     const size_t head_off = ((size_t)b * a.Hv + h) * kD * kD;
     const size_t warp_off = (size_t)(row0 + warp * RPW) * kD;
+    // Where the entering state and conv window are read: the live arrays, or, in the
+    // step that follows a K-token verify, the snapshot sequence b's accepted count n
+    // selects (n < K: the state after its n accepted tokens). The results always go to
+    // the live arrays, so the rollback costs no copy.
+    const TS *src_rows = state + head_off;
+    const float *src_hist = histb;
+    if (NTOK == 1 && a.n_accept != nullptr) {
+        const int K = a.n_draft;
+        int n = __ldg(a.n_accept + b);
+        if (n < 1 || n > K) {
+            if (blockIdx.x == 0 && tid == 0)
+                atomicOr(&g_decode_error, kErrAcceptRange);
+            n = K;
+        }
+        if (n < K) {
+            src_rows = static_cast<const TS *>(a.state_snap) +
+                       (((size_t)b * (K - 1) + (n - 1)) * a.Hv + h) * kD * kD;
+            src_hist = a.conv_snap + ((size_t)b * a.conv_snap_entries + (n - 1)) * cd * (W - 1);
+        }
+    }
     // float32 rows as float4; bf16 rows stay packed (half the registers: 3 CTAs per SM)
     using Reg = typename std::conditional<sizeof(TS) == 4, float4, uint2>::type;
     Reg st[NG][4];
-    load_rows<NG>(state + head_off + warp_off, st);
+    load_rows<NG>(src_rows + warp_off, st);
     if constexpr (sizeof(TS) == 2) {
         // bf16 rows (3 CTAs per SM): also prefetch into L2 the state block of the
         // CTA one SM count later in launch order, about a third of a wave ahead
@@ -188,10 +208,10 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
     const int c_qk = (is_k ? a.Hq * kD : 0) + hk * kD + (tid & (kD - 1));
     const int c_v = 2 * a.Hq * kD + h * kD + row0 + tid;
     ConvWindow<NTOK> wqk, wv;
-    conv_window_load<TIn, NTOK>(histb + (size_t)c_qk * (W - 1), xb + c_qk, a.x_stride,
+    conv_window_load<TIn, NTOK>(src_hist + (size_t)c_qk * (W - 1), xb + c_qk, a.x_stride,
                                 a.conv_w + (size_t)c_qk * W, W, wqk);
     if (tid < ROWS)
-        conv_window_load<TIn, NTOK>(histb + (size_t)c_v * (W - 1), xb + c_v, a.x_stride,
+        conv_window_load<TIn, NTOK>(src_hist + (size_t)c_v * (W - 1), xb + c_v, a.x_stride,
                                     a.conv_w + (size_t)c_v * W, W, wv);
     float zj[NTOK], nw = 0.0f;
     if (tid < ROWS) {

@@ -19,6 +19,11 @@ struct FusedArgs {
     int B, Hq, Hv, W, conv_dim;
     float l2_eps, rms_eps, scale;
     int sm_count;          // SMs of the device (the bf16-state step's L2 prefetch distance)
+    // single-token step after a K-token verify (null: read state / conv_state): sequence b
+    // starts from snapshot n-1 (state_snap [B][K-1][Hv][d][d], conv_snap [B][E][conv_dim][W-1])
+    // when n = n_accept[b] < K, else from state / conv_state
+    const int32_t *n_accept;
+    int n_draft, conv_snap_entries;
 };
 
 struct ConvArgs {

@@ -234,6 +234,33 @@ gdn_status gdn_verify_commit(float *state, float *conv_state, const float *state
                              const gdn_dims *dims, gdn_stream_t stream);
 
 /*
+ * The single-token step that follows a K-token verify (gdn_verify_k2, K = 2,
+ * or gdn_verify_kn, K = n_draft) with the rollback folded in ("ssm_mamba.rs",
+ * gdn_verify_fused_conv_k2: the position-0 snapshot is the rollback point,
+ * and the generic form issues no copies). Sequence b starts from the state
+ * after its n = n_accept[b] accepted tokens (device int32 [B]):
+ *   n < K   state_snap entry n-1 (float [B][K-1][Hv][d][d]) and conv_snap
+ *           entry n-1 (float [B][E][conv_dim][W-1], E = conv_snap_entries:
+ *           K-1 for gdn_verify_k2's snapshots, K for gdn_verify_kn's);
+ *   n = K   state and conv_state;
+ *   otherwise state and conv_state, and bit 16 is set in the device-side
+ *           error word (see gdn_check_device).
+ * The step's results go to state, conv_state and out exactly as in
+ * gdn_decode_step, so this call equals gdn_verify_commit (gdn_verify_commit_kn)
+ * followed by gdn_decode_step, bit for bit, without the commit's copy. With
+ * K = 1 the snapshots are not read (may be NULL). The snapshots are only read
+ * and may not overlap state or conv_state.
+ * Errors: INVALID_ARG (null, n_draft < 1, conv_snap_entries not K-1 or K,
+ * overlapping snapshots, bad dims), UNSUPPORTED as gdn_decode_step.
+ */
+gdn_status gdn_decode_step_select(float *state, float *conv_state, const float *state_snap,
+                                  const float *conv_snap, int32_t conv_snap_entries,
+                                  const int32_t *n_accept, int32_t n_draft, const void *x,
+                                  const void *z, const void *alpha, const void *beta_logit,
+                                  gdn_dtype act_dtype, const gdn_params *params, float *out,
+                                  const gdn_dims *dims, gdn_stream_t stream);
+
+/*
  * Sequential scan of the recurrence over n_tokens tokens of every sequence
  * ("fm_kernel_ssm.h", "Delta-rule recurrence": the naive sequential scan,
  * kept as the permanent correctness reference for the chunked path). Each
@@ -389,7 +416,7 @@ gdn_status gdn_prefill_chunked_noalloc(float *state, float *conv_state, const vo
  *   bit 2   the chunked prefill's per-chunk transform pass gave up a wait
  *   bit 8   a copy or product the prefill issued did not finish in its drain
  *   bit 16  gdn_verify_commit saw an accepted count outside 1..2, or
- *           gdn_verify_commit_kn one outside 1..K
+ *           gdn_verify_commit_kn / gdn_decode_step_select one outside 1..K
  *   bit 64  the multi-token conv gave up its tile-copy wait
  * The one wait not bounded by the library is the hardware's tensor-memory
  * allocation at the start of the prefill kernels, which lasts until CTAs of

@@ -28,8 +28,9 @@ void gdn_testing_set_first_wait_ns(uint64_t ns);
  * The row slices per V head that the launchers choose for n_seq sequences of
  * n_v_heads V heads, r = n_v_heads / n_qk_heads, on a device with sms SMs:
  * *decode_split for the single-token decode step, *scan_split for the
- * token-serial scans (gdn_layer_scan, gdn_recurrence_scan). Host-only: no
- * device is touched, so the choice can be tested for any SM count.
+ * token-serial scans (gdn_layer_scan, gdn_recurrence_scan); the verify steps use
+ * *decode_split too. Host-only: no device is touched, so the choice can be
+ * tested for any SM count.
  */
 void gdn_testing_row_splits(int32_t n_seq, int32_t n_v_heads, int32_t r, int32_t sms,
                             int32_t *decode_split, int32_t *scan_split);

@@ -184,6 +184,23 @@ def test_scan_entry_points_validate(lib):
     assert lib.gdn_layer_scan(*layer[:9], ct.byref(bad_w), 3, None) == gdn.GDN_ERR_UNSUPPORTED
 
 
+def test_select_step_validates(lib):
+    # every case below fails on the host before a launch (the pointers are never dereferenced)
+    cd, cp = _dims().c(), _params().c()
+    tail = [FAKE] * 4 + [gdn.GDN_F32, ct.byref(cp), FAKE, ct.byref(cd), None]
+    G = 1 << 30                      # far apart: no overlap between these ranges
+    st, conv, ss, cs, acc = FAKE, FAKE + G, FAKE + 2 * G, FAKE + 3 * G, FAKE + 4 * G
+    sel = lambda *a: lib.gdn_decode_step_select(*a, *tail)
+    assert sel(st, conv, ss, cs, 2, None, 2) == gdn.GDN_ERR_INVALID_ARG        # no counts
+    assert sel(st, conv, ss, cs, 2, acc, 0) == gdn.GDN_ERR_INVALID_ARG         # n_draft < 1
+    assert sel(st, conv, None, cs, 2, acc, 3) == gdn.GDN_ERR_INVALID_ARG       # no state snapshots
+    assert sel(st, conv, ss, None, 3, acc, 3) == gdn.GDN_ERR_INVALID_ARG       # no conv snapshots
+    assert sel(st, conv, ss, cs, 1, acc, 3) == gdn.GDN_ERR_INVALID_ARG         # entries not K-1 or K
+    assert sel(st, conv, ss, cs, 4, acc, 3) == gdn.GDN_ERR_INVALID_ARG
+    assert sel(st, conv, st + 64, cs, 3, acc, 3) == gdn.GDN_ERR_INVALID_ARG    # snapshot inside state
+    assert sel(st, conv, ss, conv + 64, 3, acc, 3) == gdn.GDN_ERR_INVALID_ARG  # inside conv_state
+
+
 def test_verify_kn_requires_distinct_snapshots(lib):
     cd, cp = _dims().c(), _params().c()
     tail = [FAKE] * 4 + [gdn.GDN_F32, ct.byref(cp), FAKE, ct.byref(cd)]
