@@ -20,22 +20,39 @@ __device__ __forceinline__ void cluster_wait_acquire()
 }
 
 // 256-thread CTAs in clusters of csize along x (no cluster attribute when csize == 1).
+// With dependent set, the kernel is a programmatic dependent of the previous kernel in
+// the stream: it may start once that kernel's CTAs have all signalled (or ended), and
+// must wait (griddepcontrol.wait) before it reads anything that kernel writes.
 template <typename K, typename A>
-static cudaError_t launch_cluster(K kernel, dim3 grid, int csize, cudaStream_t s, const A &args)
+static cudaError_t launch_cluster(K kernel, dim3 grid, int csize, cudaStream_t s, const A &args,
+                                  bool dependent = false)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (csize > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = csize;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (dependent) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = csize > 1 ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, args);
 }
+
+// The two halves of a programmatic dependency, in a kernel launched as above.
+__device__ __forceinline__ void wait_previous_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
 }  // namespace gdn

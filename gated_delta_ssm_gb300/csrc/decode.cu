@@ -156,9 +156,40 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
     const TIn *xb = static_cast<const TIn *>(a.x) + tok0 * a.x_stride;
     float *histb = a.conv_state + (size_t)b * cd * (W - 1);
 
-    // (1) this warp's state rows: loads in flight during the prologue
     const size_t head_off = ((size_t)b * a.Hv + h) * kD * kD;
     const size_t warp_off = (size_t)(row0 + warp * RPW) * kD;
+
+    // (1) this call's own inputs, which no earlier step writes: the conv window's new
+    // rows and taps, z, the norm gain and the gate inputs. The launch is a programmatic
+    // dependent of the previous kernel in the stream, so these loads may overlap that
+    // kernel's tail when it is an earlier step.
+    const bool is_k = tid >= kD;
+    const int c_qk = (is_k ? a.Hq * kD : 0) + hk * kD + (tid & (kD - 1));
+    const int c_v = 2 * a.Hq * kD + h * kD + row0 + tid;
+    ConvWindow<NTOK> wqk, wv;
+    conv_window_load_x<TIn, NTOK>(xb + c_qk, a.x_stride, a.conv_w + (size_t)c_qk * W, W, wqk);
+    if (tid < ROWS)
+        conv_window_load_x<TIn, NTOK>(xb + c_v, a.x_stride, a.conv_w + (size_t)c_v * W, W, wv);
+    float zj[NTOK], nw = 0.0f;
+    if (tid < ROWS) {
+#pragma unroll
+        for (int p = 0; p < NTOK; ++p)
+            zj[p] = load_act<TIn>(static_cast<const TIn *>(a.z) + (tok0 + p) * a.z_stride +
+                                  (int64_t)h * kD + row0 + tid);
+        nw = __ldg(a.norm_w + row0 + tid);
+    }
+    float g_alpha = 0.0f, g_bl = 0.0f, g_dt = 0.0f, g_alog = 0.0f;
+    const bool gate_thread = tid >= ROWS && tid < ROWS + NTOK;
+    if (gate_thread) {
+        const int64_t row = tok0 + (tid - ROWS);
+        g_alpha = load_act<TIn>(static_cast<const TIn *>(a.alpha) + row * a.gate_stride + h);
+        g_bl = load_act<TIn>(static_cast<const TIn *>(a.beta_logit) + row * a.gate_stride + h);
+        g_dt = __ldg(a.dt + h);
+        g_alog = __ldg(a.A_log + h);
+    }
+
+    // (2) what an earlier step writes (state, conv history) once that step has finished
+    wait_previous_grid();
     // Where the entering state and conv window are read: the live arrays, or, in the
     // step that follows a K-token verify, the snapshot sequence b's accepted count n
     // selects (n < K: the state after its n accepted tokens). The results always go to
@@ -179,7 +210,8 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
             src_hist = a.conv_snap + ((size_t)b * a.conv_snap_entries + (n - 1)) * cd * (W - 1);
         }
     }
-    // float32 rows as float4; bf16 rows stay packed (half the registers: 3 CTAs per SM)
+    // this warp's state rows, float32 as float4; bf16 rows stay packed (half the
+    // registers: 3 CTAs per SM)
     using Reg = typename std::conditional<sizeof(TS) == 4, float4, uint2>::type;
     Reg st[NG][4];
     load_rows<NG>(src_rows + warp_off, st);
@@ -202,34 +234,9 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
             }
         }
     }
-
-    // (2) conv windows: Q/K channel (every thread), V channel (threads < ROWS); gate inputs
-    const bool is_k = tid >= kD;
-    const int c_qk = (is_k ? a.Hq * kD : 0) + hk * kD + (tid & (kD - 1));
-    const int c_v = 2 * a.Hq * kD + h * kD + row0 + tid;
-    ConvWindow<NTOK> wqk, wv;
-    conv_window_load<TIn, NTOK>(src_hist + (size_t)c_qk * (W - 1), xb + c_qk, a.x_stride,
-                                a.conv_w + (size_t)c_qk * W, W, wqk);
+    conv_window_load_hist<NTOK>(src_hist + (size_t)c_qk * (W - 1), W, wqk);
     if (tid < ROWS)
-        conv_window_load<TIn, NTOK>(src_hist + (size_t)c_v * (W - 1), xb + c_v, a.x_stride,
-                                    a.conv_w + (size_t)c_v * W, W, wv);
-    float zj[NTOK], nw = 0.0f;
-    if (tid < ROWS) {
-#pragma unroll
-        for (int p = 0; p < NTOK; ++p)
-            zj[p] = load_act<TIn>(static_cast<const TIn *>(a.z) + (tok0 + p) * a.z_stride +
-                                  (int64_t)h * kD + row0 + tid);
-        nw = __ldg(a.norm_w + row0 + tid);
-    }
-    float g_alpha = 0.0f, g_bl = 0.0f, g_dt = 0.0f, g_alog = 0.0f;
-    const bool gate_thread = tid >= ROWS && tid < ROWS + NTOK;
-    if (gate_thread) {
-        const int64_t row = tok0 + (tid - ROWS);
-        g_alpha = load_act<TIn>(static_cast<const TIn *>(a.alpha) + row * a.gate_stride + h);
-        g_bl = load_act<TIn>(static_cast<const TIn *>(a.beta_logit) + row * a.gate_stride + h);
-        g_dt = __ldg(a.dt + h);
-        g_alog = __ldg(a.A_log + h);
-    }
+        conv_window_load_hist<NTOK>(src_hist + (size_t)c_v * (W - 1), W, wv);
 
     // (3) conv + SiLU; every read of the shared Q/K history is now complete: the
     // arrive below issues after the arithmetic that consumed those loads (a
@@ -272,6 +279,9 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
                                            : nullptr,
                                   sk, sq, sv, ROWS, sdecay, sbeta, sy, warp * RPW, a.scale,
                                   state + head_off + warp_off);
+    // this CTA's state stores are issued: the next step in the stream may start its
+    // prologue (it waits for this whole grid before it reads what this one writes)
+    allow_next_grid();
     __syncthreads();
 
     // (6) gated RMSNorm: 32-row block partials, combined in block order
@@ -368,9 +378,9 @@ static cudaError_t fused_dispatch(const FusedArgs &a, cudaStream_t s)
     const int ns = pick_nsplit(a.B, a.Hv, r, a.sm_count);
     const dim3 grid(a.Hv * ns, a.B, 1);
     switch (ns) {
-    case 1: return launch_cluster(decode_fused_kernel<TIn, NTOK, 1, TS>, grid, r, s, a);
-    case 2: return launch_cluster(decode_fused_kernel<TIn, NTOK, 2, TS>, grid, r * 2, s, a);
-    default: return launch_cluster(decode_fused_kernel<TIn, NTOK, 4, TS>, grid, r * 4, s, a);
+    case 1: return launch_cluster(decode_fused_kernel<TIn, NTOK, 1, TS>, grid, r, s, a, true);
+    case 2: return launch_cluster(decode_fused_kernel<TIn, NTOK, 2, TS>, grid, r * 2, s, a, true);
+    default: return launch_cluster(decode_fused_kernel<TIn, NTOK, 4, TS>, grid, r * 4, s, a, true);
     }
 }
 
