@@ -27,7 +27,10 @@ __all__ = [
 ]
 
 _PKG = _os.path.dirname(_os.path.abspath(__file__))
-_LIB_PATH = _os.path.join(_PKG, "libgdn.so")
+# GDN_CHECKED=1 selects the checked build (index range checks reported as device error
+# bit 32; see gdn_check_device)
+_LIB_PATH = _os.path.join(_PKG, "libgdn_checked.so" if _os.environ.get("GDN_CHECKED") == "1"
+                          else "libgdn.so")
 _lib = None
 _lock = _th.Lock()
 

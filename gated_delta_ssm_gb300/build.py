@@ -1,8 +1,11 @@
-"""Build libgdn.so (the CUDA kernels + C ABI) in-tree for sm_103a.
+"""Build libgdn.so (the CUDA kernels + C ABI) in-tree for sm_103a, and its
+checked variant libgdn_checked.so (-DGDN_CHECKS: the kernels range-check their
+index arithmetic and report a failure as a device error bit).
 
-Each .cu file compiles in parallel to an object under ``_build/``; the objects
-link into ``gated_delta_ssm_gb300/libgdn.so``. A source newer than the
-library triggers a rebuild. Run ``python -m gated_delta_ssm_gb300.build``.
+Each .cu file compiles in parallel, once per variant, to an object under
+``_build/``; the objects link into ``gated_delta_ssm_gb300/libgdn.so`` and
+``gated_delta_ssm_gb300/libgdn_checked.so``. A source newer than a library
+triggers a rebuild. Run ``python -m gated_delta_ssm_gb300.build``.
 """
 from __future__ import annotations
 
@@ -18,6 +21,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
+LIB_CHECKED = os.path.join(PKG, "libgdn_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
               "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]
@@ -40,10 +44,13 @@ def _deps() -> list[str]:
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
-        return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in _deps())
+    for lib in (LIB, LIB_CHECKED):
+        if not os.path.exists(lib):
+            return False
+        t = os.path.getmtime(lib)
+        if any(os.path.getmtime(p) > t for p in _deps()):
+            return False
+    return True
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
@@ -53,9 +60,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     os.makedirs(BUILD, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
-    def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
+    variants = ((LIB, BUILD, []), (LIB_CHECKED, os.path.join(BUILD, "checked"), ["-DGDN_CHECKS"]))
+    for _, objdir, _ in variants:
+        os.makedirs(objdir, exist_ok=True)
+
+    def compile_one(job) -> str:
+        src, objdir, defs = job
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *defs, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
@@ -63,14 +75,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             sys.stderr.write(r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
-        objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
+    jobs = [(src, objdir, defs) for _, objdir, defs in variants for src in sources()]
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        objs = list(ex.map(compile_one, jobs))
+    n = len(sources())
+    for k, (lib, _, _) in enumerate(variants):
+        tmp = lib + f".tmp{os.getpid()}"
+        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs[k * n:(k + 1) * n], "-lcudart"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB
 
 

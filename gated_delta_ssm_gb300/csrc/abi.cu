@@ -492,6 +492,7 @@ gdn_status gdn_prefill_chunked(float *state, float *conv_state, const void *x, c
     a.norm_w = params->norm_w;
     a.out = out;
     a.ws = static_cast<uint8_t *>(workspace);
+    a.ws_bytes = workspace_bytes;
     a.x_stride = dims->x_stride;
     a.z_stride = dims->z_stride;
     a.gate_stride = dims->gate_stride;

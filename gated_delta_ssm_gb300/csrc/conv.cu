@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(kD) conv_update_kernel(ConvArgs a)
     const int c = blockIdx.x * kD + tid;
     const bool is_qk = blockIdx.x < 2 * a.Hq;
     const int W = a.W;
+    GDN_CHECK(g_conv_error, b < a.B && c < a.conv_dim);
     float *hist_c = a.conv_state + ((size_t)b * a.conv_dim + c) * (W - 1);
     const TIn *x_c = static_cast<const TIn *>(a.x) + (int64_t)b * a.T * a.x_stride + c;
     const float *w_c = a.conv_w + (size_t)c * W;
@@ -74,6 +75,7 @@ __global__ void __launch_bounds__(256) conv_tokens_kernel(ConvArgs a)
     const bool is_qk = blockIdx.x < 2 * a.Hq;
     const int W = a.W, T = a.T;
     const int t0 = (blockIdx.y * 2 + tg) * TPT;
+    GDN_CHECK(g_conv_error, b < a.B && c < a.conv_dim && blockIdx.y * 2 * TPT < T);
     float *hist_c = a.conv_state + ((size_t)b * a.conv_dim + c) * (W - 1);
     const TIn *x_c = static_cast<const TIn *>(a.x) + (int64_t)b * T * a.x_stride + c;
 
@@ -222,6 +224,7 @@ __global__ void __launch_bounds__(256) conv_tiles_kernel(const __grid_constant__
         const int head = item % n_heads, rest = item / n_heads;
         const int t0 = (rest % n_tiles) * kTT, b = rest / n_tiles;
         const int c = head * kD + i;
+        GDN_CHECK(g_conv_error, b < a.B && c < a.conv_dim && t0 < T);
         const bool is_qk = head < 2 * a.Hq;
         const TIn *tl = reinterpret_cast<const TIn *>(smem + buf * L::tile) + i;   // column i
         float w[kMaxW];

@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(256) decay_gate_kernel(const TIn *alpha, int64
         return;
     const int64_t r = i / H;
     const int h = (int)(i % H);
+    GDN_CHECK(g_decode_error, r < rows && h < H);
     g[i] = decay_gate_f(load_act<TIn>(alpha + r * alpha_stride + h), __ldg(dt + h), __ldg(A_log + h));
 }
 
@@ -58,6 +59,7 @@ __global__ void __launch_bounds__(256, 2) recurrence_decode_kernel(RecArgs a)
     const int h = blockIdx.x / NSPLIT, split = blockIdx.x % NSPLIT;
     const int hk = h / (a.Hv / a.Hq);
     const int row0 = split * ROWS;
+    GDN_CHECK(g_decode_error, b < a.B && h < a.Hv && hk < a.Hq && row0 + ROWS <= kD);
     float *rows = a.state + (((size_t)b * a.Hv + h) * kD + row0 + warp * RPW) * kD;
     float4 r[NG][4];
     load_rows<NG>(rows, r);
@@ -92,6 +94,7 @@ __global__ void __launch_bounds__(256) gated_norm_kernel(const float *y, const f
         return;
     const int64_t row = gw / Hv;
     const int h = (int)(gw % Hv);
+    GDN_CHECK(g_decode_error, row < rows && h < Hv);
     const float *yr = y + gw * kD;
     float yv[4], bp[4];
 #pragma unroll
@@ -158,6 +161,8 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
 
     const size_t head_off = ((size_t)b * a.Hv + h) * kD * kD;
     const size_t warp_off = (size_t)(row0 + warp * RPW) * kD;
+    GDN_CHECK(g_decode_error, b < a.B && h < a.Hv && hk < a.Hq && split < NSPLIT && row0 + ROWS <= kD &&
+                                  crank < csize);
 
     // (1) this call's own inputs, which no earlier step writes: the conv window's new
     // rows and taps, z, the norm gain and the gate inputs. The launch is a programmatic
@@ -166,6 +171,7 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
     const bool is_k = tid >= kD;
     const int c_qk = (is_k ? a.Hq * kD : 0) + hk * kD + (tid & (kD - 1));
     const int c_v = 2 * a.Hq * kD + h * kD + row0 + tid;
+    GDN_CHECK(g_decode_error, c_qk < 2 * a.Hq * kD && (tid >= ROWS || (c_v >= 2 * a.Hq * kD && c_v < cd)));
     ConvWindow<NTOK> wqk, wv;
     conv_window_load_x<TIn, NTOK>(xb + c_qk, a.x_stride, a.conv_w + (size_t)c_qk * W, W, wqk);
     if (tid < ROWS)
@@ -205,6 +211,7 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
             n = K;
         }
         if (n < K) {
+            GDN_CHECK(g_decode_error, n - 1 < K - 1 && n - 1 < a.conv_snap_entries);
             src_rows = static_cast<const TS *>(a.state_snap) +
                        (((size_t)b * (K - 1) + (n - 1)) * a.Hv + h) * kD * kD;
             src_hist = a.conv_snap + ((size_t)b * a.conv_snap_entries + (n - 1)) * cd * (W - 1);

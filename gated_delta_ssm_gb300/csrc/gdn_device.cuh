@@ -37,6 +37,24 @@ __device__ __forceinline__ void st_stream(float *p, float4 v)
     __stcs(reinterpret_cast<float4 *>(p), v);
 }
 
+// ------------------------------------------------------------------ checked build
+// Range checks of the kernels' index arithmetic, compiled in by -DGDN_CHECKS (the
+// checked library, libgdn_checked.so): a failing check sets bit 32 of the file's
+// device-side error word (read by gdn_check_device) and the kernel goes on, so that a
+// test sees the bit instead of a trap. Without the define the checks vanish.
+constexpr int kErrRange = 32;
+#ifdef GDN_CHECKS
+#define GDN_CHECK(word, cond)                   \
+    do {                                        \
+        if (!(cond))                            \
+            atomicOr(&(word), gdn::kErrRange);  \
+    } while (0)
+#else
+#define GDN_CHECK(word, cond) \
+    do {                      \
+    } while (0)
+#endif
+
 // ------------------------------------------------------------------ scalar maps
 // silu(x) = x * sigmoid(x) = x / (1 + e^-x), from the hardware exponential and
 // the fast divide: a few ulp (about 1e-6 relative for |x| < 20), cheap enough

@@ -78,6 +78,7 @@ struct PrefillArgs {
     const float *conv_w, *dt, *A_log, *norm_w;
     float *out;            // [B][T][Hv][d]
     uint8_t *ws;           // workspace: chunk images, then [Q; K] images (prefill.cu)
+    size_t ws_bytes;
     int64_t x_stride, z_stride, gate_stride;
     int B, Hq, Hv, W, conv_dim, T, n_chunks;
     float l2_eps, rms_eps, scale;

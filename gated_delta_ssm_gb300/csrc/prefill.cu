@@ -458,6 +458,9 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
     const int r = a.Hv / a.Hq;
     const int W = WC > 0 ? WC : a.W;
     const int c0 = c * kC, n = min(kC, a.T - c0);
+    GDN_CHECK(g_device_error, c < a.n_chunks && hk < a.Hq && b < a.B && n >= 1 && c0 + n <= a.T &&
+                                  qk_image(a, b, hk, c) + kPrefillQKImage <= a.ws + a.ws_bytes &&
+                                  chunk_image(a, b, hk * r + r - 1, c) + kPrefillChunkImage <= a.ws + a.ws_bytes);
     const uint32_t sbase = tc::smem_addr(smem);
     const uint32_t mb_raw = sbase + p1::MBAR, mb_mma = sbase + p1::MBAR + 8;
     Gates *gates = reinterpret_cast<Gates *>(smem + p1::GATES);
@@ -798,6 +801,9 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
     const int r = a.Hv / a.Hq, hk = h / r;
     const int W = WC > 0 ? WC : a.W;
     const int nch = a.n_chunks;
+    GDN_CHECK(g_device_error, h < a.Hv && b < a.B && hk < a.Hq && (nch - 1) * kC < a.T &&
+                                  qk_image(a, b, hk, nch - 1) + kPrefillQKImage <= a.ws + a.ws_bytes &&
+                                  chunk_image(a, b, h, nch - 1) + kPrefillChunkImage <= a.ws + a.ws_bytes);
     const uint32_t sbase = tc::smem_addr(smem);
     const uint32_t mb = sbase + MBAR;
     auto bar = [&](int i) { return mb + 8u * (uint32_t)i; };

@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(256, 2) recurrence_scan_kernel(RecScanArgs a)
     const int h = blockIdx.x / NSPLIT, split = blockIdx.x % NSPLIT;
     const int hk = h / (a.Hv / a.Hq);
     const int row0 = split * ROWS;
+    GDN_CHECK(g_seq_error, b < a.B && h < a.Hv && hk < a.Hq && row0 + ROWS <= kD);
     float *rows = a.state + (((size_t)b * a.Hv + h) * kD + row0 + warp * RPW) * kD;
     float4 st[NG][4];
     load_rows<NG>(rows, st);
@@ -154,6 +155,7 @@ __global__ void __launch_bounds__(256, 2) layer_scan_kernel(LayerScanArgs a)
 
     const size_t head_off = ((size_t)b * a.Hv + h) * kD * kD;
     const size_t warp_off = (size_t)(row0 + warp * RPW) * kD;
+    GDN_CHECK(g_seq_error, b < a.B && h < a.Hv && hk < a.Hq && row0 + ROWS <= kD && crank < csize);
     float4 st[NG][4];
     load_rows<NG>(a.state + head_off + warp_off, st);
 

@@ -417,6 +417,8 @@ gdn_status gdn_prefill_chunked_noalloc(float *state, float *conv_state, const vo
  *   bit 8   a copy or product the prefill issued did not finish in its drain
  *   bit 16  gdn_verify_commit saw an accepted count outside 1..2, or
  *           gdn_verify_commit_kn / gdn_decode_step_select one outside 1..K
+ *   bit 32  (checked build only, libgdn_checked.so) a kernel's index
+ *           arithmetic left the range its arguments allow
  *   bit 64  the multi-token conv gave up its tile-copy wait
  * The one wait not bounded by the library is the hardware's tensor-memory
  * allocation at the start of the prefill kernels, which lasts until CTAs of
