@@ -20,6 +20,7 @@ the data path); value = all ranks' state bytes / the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -494,9 +495,11 @@ class Gpu:
         return {"us": m * 1e6, "GBps": nbytes / m / 1e9, "algorithmic_bytes": nbytes}
 
     # -- chunked prefill
-    def prefill(self, steps, warmup):
+    def prefill(self, steps, warmup, tokens=None):
         torch, gdn = self.torch, self.gdn
         shape = synth.WORKLOADS["prefill"]
+        if tokens:
+            shape = dataclasses.replace(shape, T=int(tokens))
         inp = synth.make_inputs(shape, seed=4)
         d = self.upload(shape, inp)
         dims, prm = self.dims(shape), self.params(d)
@@ -602,6 +605,8 @@ def main(argv=None):
                                        "verify_kn", "conv_tokens", "prefill"],
                     help="run one secondary workload alone and print its figures (for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-tokens", type=int, default=None,
+                    help="with --only prefill: tokens per sequence (a smaller case for profiler captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -615,7 +620,7 @@ def main(argv=None):
               "verify_kn": lambda: gpu.verify_kn(args.steps, args.warmup),
               "decode_b64_bf16_state": lambda: gpu.decode_b64_bf16_state(args.steps, args.warmup),
               "conv_tokens": lambda: gpu.conv_tokens(args.steps, args.warmup),
-              "prefill": lambda: gpu.prefill(args.steps, args.warmup)}[args.only]
+              "prefill": lambda: gpu.prefill(args.steps, args.warmup, args.prefill_tokens)}[args.only]
         print(json.dumps({"workload": args.only, **fn()}), flush=True)
         return 0
     dist = init_dist(world, "nccl")
