@@ -22,7 +22,8 @@ __device__ __forceinline__ void cluster_wait_acquire()
 // 256-thread CTAs in clusters of csize along x (no cluster attribute when csize == 1).
 // With dependent set, the kernel is a programmatic dependent of the previous kernel in
 // the stream: it may start once that kernel's CTAs have all signalled (or ended), and
-// must wait (griddepcontrol.wait) before it reads anything that kernel writes.
+// waits (griddepcontrol.wait) before it reads anything that kernel may write (only
+// constant layer parameters are read before the wait).
 template <typename K, typename A>
 static cudaError_t launch_cluster(K kernel, dim3 grid, int csize, cudaStream_t s, const A &args,
                                   bool dependent = false)

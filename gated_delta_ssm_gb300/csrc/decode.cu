@@ -116,8 +116,9 @@ __global__ void __launch_bounds__(256) gated_norm_kernel(const float *y, const f
 // NTOK = 1: one decode step. NTOK = 2: K=2 verify, snapshot after token 0.
 //
 // Order of a CTA's work, chosen so that no fence ever waits on the state
-// loads or stores: (1) state-row loads, (2) conv-window, gate, z and norm-gain
-// loads, one memory round trip; (3) conv + SiLU, then cluster arrive (every
+// loads or stores: (0) wait for the previous kernel in the stream (the launch
+// is a programmatic dependent of it); (1) conv-window, gate, z and norm-gain
+// loads, (2) state-row and conv-history loads, one memory round trip; (3) conv + SiLU, then cluster arrive (every
 // read of the shared Q/K history is done); (4) L2, gates; (5) recurrence in
 // registers, each 4-row group stored as soon as it is stepped (its stores
 // overlap the later groups' arithmetic); (6) gated norm (row slices of a head
@@ -164,60 +165,97 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
     GDN_CHECK(g_decode_error, b < a.B && h < a.Hv && hk < a.Hq && split < NSPLIT && row0 + ROWS <= kD &&
                                   crank < csize);
 
-    // (1) this call's own inputs, which no earlier step writes: the conv window's new
-    // rows and taps, z, the norm gain and the gate inputs. The launch is a programmatic
-    // dependent of the previous kernel in the stream, so these loads may overlap that
-    // kernel's tail when it is an earlier step.
+    // (0) the layer parameters: the conv taps, the norm gain, dt and A_log. The launch is
+    // a programmatic dependent of the previous kernel in the stream, so the CTA may be
+    // resident while that kernel finishes; these loads are the only reads issued before
+    // it has completed (the parameters are constant across steps and no kernel just
+    // before a step writes them). Everything else may come from that kernel: the
+    // activations from the projection before the step, the state and the conv history
+    // from the previous step.
     const bool is_k = tid >= kD;
     const int c_qk = (is_k ? a.Hq * kD : 0) + hk * kD + (tid & (kD - 1));
     const int c_v = 2 * a.Hq * kD + h * kD + row0 + tid;
     GDN_CHECK(g_decode_error, c_qk < 2 * a.Hq * kD && (tid >= ROWS || (c_v >= 2 * a.Hq * kD && c_v < cd)));
     ConvWindow<NTOK> wqk, wv;
-    conv_window_load_x<TIn, NTOK>(xb + c_qk, a.x_stride, a.conv_w + (size_t)c_qk * W, W, wqk);
-    if (tid < ROWS)
-        conv_window_load_x<TIn, NTOK>(xb + c_v, a.x_stride, a.conv_w + (size_t)c_v * W, W, wv);
-    float zj[NTOK], nw = 0.0f;
-    if (tid < ROWS) {
 #pragma unroll
-        for (int p = 0; p < NTOK; ++p)
-            zj[p] = load_act<TIn>(static_cast<const TIn *>(a.z) + (tok0 + p) * a.z_stride +
-                                  (int64_t)h * kD + row0 + tid);
-        nw = __ldg(a.norm_w + row0 + tid);
+    for (int tau = 0; tau < kMaxW; ++tau) {
+        wqk.w[tau] = tau < W ? __ldg(a.conv_w + (size_t)c_qk * W + tau) : 0.0f;
+        wv.w[tau] = (tid < ROWS && tau < W) ? __ldg(a.conv_w + (size_t)c_v * W + tau) : 0.0f;
     }
-    float g_alpha = 0.0f, g_bl = 0.0f, g_dt = 0.0f, g_alog = 0.0f;
+    const float nw = tid < ROWS ? __ldg(a.norm_w + row0 + tid) : 0.0f;
     const bool gate_thread = tid >= ROWS && tid < ROWS + NTOK;
+    float g_alpha = 0.0f, g_bl = 0.0f, g_dt = 0.0f, g_alog = 0.0f;
     if (gate_thread) {
-        const int64_t row = tok0 + (tid - ROWS);
-        g_alpha = load_act<TIn>(static_cast<const TIn *>(a.alpha) + row * a.gate_stride + h);
-        g_bl = load_act<TIn>(static_cast<const TIn *>(a.beta_logit) + row * a.gate_stride + h);
         g_dt = __ldg(a.dt + h);
         g_alog = __ldg(a.A_log + h);
     }
-
-    // (2) what an earlier step writes (state, conv history) once that step has finished
     wait_previous_grid();
-    // Where the entering state and conv window are read: the live arrays, or, in the
+
+    // (1) the conv windows' new rows, z and the gate inputs
+    float zj[NTOK];
+    auto load_inputs = [&]() {
+#pragma unroll
+        for (int e = 0; e < kMaxW - 1 + NTOK; ++e) {
+            if (e >= W - 1 && e < W - 1 + NTOK) {
+                wqk.win[e] = load_act<TIn>(xb + c_qk + (int64_t)(e - (W - 1)) * a.x_stride);
+                if (tid < ROWS)
+                    wv.win[e] = load_act<TIn>(xb + c_v + (int64_t)(e - (W - 1)) * a.x_stride);
+            } else if (e >= W - 1 + NTOK) {
+                wqk.win[e] = 0.0f;
+                wv.win[e] = 0.0f;
+            }
+        }
+        if (tid < ROWS) {
+#pragma unroll
+            for (int p = 0; p < NTOK; ++p)
+                zj[p] = load_act<TIn>(static_cast<const TIn *>(a.z) + (tok0 + p) * a.z_stride +
+                                      (int64_t)h * kD + row0 + tid);
+        }
+        if (gate_thread) {
+            const int64_t row = tok0 + (tid - ROWS);
+            g_alpha = load_act<TIn>(static_cast<const TIn *>(a.alpha) + row * a.gate_stride + h);
+            g_bl = load_act<TIn>(static_cast<const TIn *>(a.beta_logit) + row * a.gate_stride + h);
+        }
+    };
+    // (2) where the entering state and conv window are read: the live arrays, or, in the
     // step that follows a K-token verify, the snapshot sequence b's accepted count n
     // selects (n < K: the state after its n accepted tokens). The results always go to
-    // the live arrays, so the rollback costs no copy.
+    // the live arrays, so the rollback costs no copy. Then the conv windows' history.
     const TS *src_rows = state + head_off;
     const float *src_hist = histb;
-    if (NTOK == 1 && a.n_accept != nullptr) {
-        const int K = a.n_draft;
-        int n = __ldg(a.n_accept + b);
-        if (n < 1 || n > K) {
-            if (blockIdx.x == 0 && tid == 0)
-                atomicOr(&g_decode_error, kErrAcceptRange);
-            n = K;
+    auto load_hist = [&]() {
+        if (NTOK == 1 && a.n_accept != nullptr) {
+            const int K = a.n_draft;
+            int n = __ldg(a.n_accept + b);
+            if (n < 1 || n > K) {
+                if (blockIdx.x == 0 && tid == 0)
+                    atomicOr(&g_decode_error, kErrAcceptRange);
+                n = K;
+            }
+            if (n < K) {
+                GDN_CHECK(g_decode_error, n - 1 < K - 1 && n - 1 < a.conv_snap_entries);
+                src_rows = static_cast<const TS *>(a.state_snap) +
+                           (((size_t)b * (K - 1) + (n - 1)) * a.Hv + h) * kD * kD;
+                src_hist = a.conv_snap + ((size_t)b * a.conv_snap_entries + (n - 1)) * cd * (W - 1);
+            }
         }
-        if (n < K) {
-            GDN_CHECK(g_decode_error, n - 1 < K - 1 && n - 1 < a.conv_snap_entries);
-            src_rows = static_cast<const TS *>(a.state_snap) +
-                       (((size_t)b * (K - 1) + (n - 1)) * a.Hv + h) * kD * kD;
-            src_hist = a.conv_snap + ((size_t)b * a.conv_snap_entries + (n - 1)) * cd * (W - 1);
-        }
+        conv_window_load_hist<NTOK>(src_hist + (size_t)c_qk * (W - 1), W, wqk);
+        if (tid < ROWS)
+            conv_window_load_hist<NTOK>(src_hist + (size_t)c_v * (W - 1), W, wv);
+    };
+    // Which group is requested first is a measured choice per form: the history first
+    // for float32 rows with a whole head per CTA (batched decode 75.7 -> 69.6 us per
+    // step, two-token verify 45.2 -> 43.2 us per launch), the new rows first otherwise
+    // (single-sequence decode 4.56 -> 3.93 us per step, bf16 state 50.8 -> 48.7 us).
+    if constexpr (NSPLIT == 1 && sizeof(TS) == 4) {
+        load_hist();
+        load_inputs();
+    } else {
+        load_inputs();
+        load_hist();
     }
-    // this warp's state rows, float32 as float4; bf16 rows stay packed (half the
+
+    // (3) this warp's state rows, float32 as float4; bf16 rows stay packed (half the
     // registers: 3 CTAs per SM)
     using Reg = typename std::conditional<sizeof(TS) == 4, float4, uint2>::type;
     Reg st[NG][4];
@@ -241,11 +279,7 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
             }
         }
     }
-    conv_window_load_hist<NTOK>(src_hist + (size_t)c_qk * (W - 1), W, wqk);
-    if (tid < ROWS)
-        conv_window_load_hist<NTOK>(src_hist + (size_t)c_v * (W - 1), W, wv);
-
-    // (3) conv + SiLU; every read of the shared Q/K history is now complete: the
+    // (4) conv + SiLU; every read of the shared Q/K history is now complete: the
     // arrive below issues after the arithmetic that consumed those loads (a
     // warp issues in order), so it needs no release fence, which would also
     // wait for this warp's state loads still in flight
@@ -286,8 +320,8 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
                                            : nullptr,
                                   sk, sq, sv, ROWS, sdecay, sbeta, sy, warp * RPW, a.scale,
                                   state + head_off + warp_off);
-    // this CTA's state stores are issued: the next step in the stream may start its
-    // prologue (it waits for this whole grid before it reads what this one writes)
+    // this CTA's state stores are issued: a dependent launch that follows may make its
+    // CTAs resident (it waits for this whole grid before it reads anything)
     allow_next_grid();
     __syncthreads();
 

@@ -155,23 +155,7 @@ __device__ __forceinline__ void conv_window_load(const float *hist_c, const TIn 
         cw.w[tau] = tau < W ? __ldg(w_c + tau) : 0.0f;
 }
 
-// conv_window_load in two halves: the new rows and the taps (inputs of this call), then
-// the history (which the previous call may have written)
-template <typename TIn, int NTOK>
-__device__ __forceinline__ void conv_window_load_x(const TIn *x_c, int64_t x_stride, const float *w_c,
-                                                   int W, ConvWindow<NTOK> &cw)
-{
-#pragma unroll
-    for (int e = 0; e < kMaxW - 1 + NTOK; ++e) {
-        if (e >= W - 1 && e < W - 1 + NTOK)
-            cw.win[e] = load_act<TIn>(x_c + (int64_t)(e - (W - 1)) * x_stride);
-        else if (e >= W - 1 + NTOK)
-            cw.win[e] = 0.0f;
-    }
-#pragma unroll
-    for (int tau = 0; tau < kMaxW; ++tau)
-        cw.w[tau] = tau < W ? __ldg(w_c + tau) : 0.0f;
-}
+// The history part of conv_window_load (the previous call may have written it)
 template <int NTOK>
 __device__ __forceinline__ void conv_window_load_hist(const float *hist_c, int W, ConvWindow<NTOK> &cw)
 {

@@ -24,11 +24,13 @@
 //
 // Pass 2 (prefill_chain_kernel) walks the chunks of one (sequence, V head)
 // with the fp32 state master in tensor memory. Its warps are specialised:
-//   * 8 conv warps: conv + SiLU + L2 of chunk c+1's Q, K, V rows (from the
-//     staged rows) and the gates, while chunk c's products run;
 //   * 8 epilogue warps (two per TMEM lane quarter, value row j = lane):
-//     X, U, the state re-split, the state write-back, and the gated RMSNorm;
-//     lane 0 of warp 0 also issues every bulk / tensor copy and every product.
+//     X, U, the state re-split, the state write-back and the readout rows;
+//   * 1 issuer warp: one lane issues every bulk / tensor copy and every product
+//     and waits on their completions, so no copy or product waits for an
+//     epilogue to reach it;
+//   * 8 conv warps: conv + SiLU of chunk c+1's V rows (from the staged rows)
+//     while chunk c's products run, and the gated RMSNorm of chunk c's outputs.
 // The products (transposed orientation, M = 128 value rows j, A operands in
 // tensor memory, B operands in shared memory):
 //   D1 = S_0^T [Q; K]^T        ((Q S_0)^T | (K S_0)^T)
@@ -714,9 +716,9 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
 
 // ================================================================== pass 2
 namespace p2 {
-// warps 0-7: epilogue (two per TMEM lane quarter); warp 8: the issuer; warps 9-12: the
-// V conv and the gated norm (16 tokens each). At most four warps share a scheduler, so
-// every thread keeps 128 registers.
+// warps 0-7: epilogue (two per TMEM lane quarter); warp 8: the issuer; warps 9-16: the
+// V conv and the gated norm (8 tokens each). 17 warps of 96 registers fit the SM's
+// 65536 registers with one CTA per SM.
 constexpr int kIssuerWarp = 8, kConvWarp0 = 9, kConvWarps = 8;
 constexpr int kConvThreads = 32 * kConvWarps, kConvTok = kC / kConvWarps;
 constexpr int kThreads = 32 * (kConvWarp0 + kConvWarps);

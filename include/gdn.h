@@ -8,8 +8,17 @@
  *               never allocates, frees, or keeps a pointer past the call.
  *   Streams     Work is enqueued on `stream` (NULL = the legacy default
  *               stream). No entry point synchronises; results are ready when
- *               the stream reaches them. Calls may be captured into CUDA
- *               graphs.
+ *               the stream reaches them. Calls other than
+ *               gdn_prefill_chunked_noalloc may be captured into CUDA
+ *               graphs. gdn_decode_step, gdn_decode_step_bf16_state,
+ *               gdn_decode_step_select and gdn_verify_k2 launch as
+ *               programmatic dependents of the previous kernel in the
+ *               stream: their blocks may become resident while that kernel
+ *               finishes. Before it has completed they read only the layer
+ *               parameters (gdn_params: conv weights, dt, A_log, norm
+ *               weight), which that kernel must therefore not write; every
+ *               other argument (activations, state, conv history, snapshots,
+ *               accepted counts) is read after it, in stream order.
  *   Errors      Host-side validation runs before anything is launched. A
  *               call that returns anything but GDN_OK has enqueued nothing,
  *               except GDN_ERR_CUDA, where the launch itself failed;

@@ -410,3 +410,44 @@ def test_repeat_runs_are_deterministic():
         torch.cuda.synchronize()
         res.append((out, st, hi))
     assert all(torch.equal(a, b) for a, b in zip(res[0], res[1]))
+
+
+def test_step_reads_inputs_the_previous_step_just_wrote():
+    """The decode launch is a programmatic dependent of the kernel before it in the
+    stream, and the decode kernel lets its dependents start before its outputs are
+    written. A step whose x and z rows ARE the output of the step just before it must
+    still read them only once that step is done: the same bits as with a device
+    synchronisation between the two calls. The first step's output buffer starts as
+    NaN, so a read that came too early would show."""
+    big = synth.Shape(B=64, T=1, Hq=4, Hv=8, act_dtype="f32", warm=True)
+    inp1 = synth.make_inputs(big, seed=140)
+    dev1 = device_inputs(big, inp1)
+    # the second step: 16 sequences whose fp32 x rows (x then z in one row) are
+    # carved out of the first step's [64][8][128] output
+    small = synth.Shape(B=16, T=1, Hq=4, Hv=8, act_dtype="f32", warm=True)
+    row = 2 * small.conv_dim
+    assert small.B * row <= big.B * big.Hv * big.d
+    inp2 = synth.make_inputs(small, seed=141)
+    dev2 = device_inputs(small, inp2)
+    dims2 = gdn.Dims(n_seq=small.B, n_qk_heads=small.Hq, n_v_heads=small.Hv, head_dim=small.d,
+                     d_conv=small.W, x_stride=row, z_stride=row, gate_stride=small.Hv)
+    results = []
+    for sync in (False, True):
+        st1, hi1 = dev1["state"].clone(), dev1["hist"].clone()
+        st2, hi2 = dev2["state"].clone(), dev2["hist"].clone()
+        out1 = torch.full((big.B, big.Hv, big.d), float("nan"), device="cuda")
+        out2 = torch.empty(small.B, small.Hv, small.d, device="cuda")
+        rows = out1.view(-1)[:small.B * row].view(small.B, row)
+        torch.cuda.synchronize()
+        gdn.decode_step(st1, hi1, dev1["x"][:, 0], dev1["z"][:, 0], dev1["alpha"][:, 0],
+                        dev1["beta_logit"][:, 0], params_of(dev1), out1, dims_of(big))
+        if sync:
+            torch.cuda.synchronize()
+        gdn.decode_step(st2, hi2, rows, rows[:, small.conv_dim:], dev2["alpha"][:, 0],
+                        dev2["beta_logit"][:, 0], params_of(dev2), out2, dims2)
+        torch.cuda.synchronize()
+        results.append((out2, st2, hi2))
+    assert gdn.check_device() == 0
+    assert torch.isfinite(results[1][0]).all()
+    for a, b in zip(results[0], results[1]):
+        assert torch.equal(a, b)
