@@ -165,9 +165,13 @@ __device__ __forceinline__ int next_rho(const Gates *G, int rho)
     return (int)fminf(fmaxf(floorf(-lmax), 0.0f), 60.0f);
 }
 
-// Gates of tokens c0 .. c0+n-1 of sequence b, V head h; executed by one warp.
+// Gates of tokens c0 .. c0+n-1 of sequence b, V head h; executed by one warp. With cf
+// set, also the decays from each 16-token block start back to the earlier tokens:
+// cf[64 (I - 1) + s] = exp(Gam_{16 I} - Gam_s) for I = 1, 2, 3 and s < 16 I (at most 1:
+// Gam does not increase).
 template <typename TIn>
-__device__ __forceinline__ void chunk_gates(const PrefillArgs &a, int b, int h, int c0, int n, Gates *G)
+__device__ __forceinline__ void chunk_gates(const PrefillArgs &a, int b, int h, int c0, int n, Gates *G,
+                                            float *cf = nullptr)
 {
     const int lane = threadIdx.x & 31;
     const float dtv = __ldg(a.dt + h), alog = __ldg(a.A_log + h);
@@ -229,6 +233,17 @@ __device__ __forceinline__ void chunk_gates(const PrefillArgs &a, int b, int h, 
         G->ec = exp_diff(gch, gcl, 0.0f, 0.0f);
         G->lc = __fmul_rn(__fadd_rn(gch, gcl), l2e);
         G->lu = lu;
+    }
+    if (cf != nullptr) {
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int sidx = lane + 32 * u;
+#pragma unroll
+            for (int I = 1; I < 4; ++I)
+                if (sidx < 16 * I)
+                    cf[64 * (I - 1) + sidx] = exp_diff_fast(G->gh[16 * I], G->gl[16 * I], G->gh[sidx], G->gl[sidx]);
+        }
     }
 }
 
@@ -421,7 +436,8 @@ constexpr uint32_t QK_LO = QK + 32768;
 constexpr uint32_t AM = QK;                        // after G: A of two heads, fp32 [64][64]
 constexpr uint32_t TB = QK + 32768;                // after G: T of two heads, fp32 [64][64]
 constexpr uint32_t GATES = QK + 65536;             // two Gates
-constexpr uint32_t MBAR = GATES + 2 * sizeof(Gates);
+constexpr uint32_t CF = GATES + 2 * sizeof(Gates);   // two block-reference decay tables, [3][64]
+constexpr uint32_t MBAR = CF + 2 * 3 * 64 * 4;
 constexpr uint32_t SLOT = MBAR + 16;
 constexpr uint32_t BYTES = SLOT + 16 + 1024;      // + alignment slack
 static_assert(QK % 1024 == 0, "swizzled tiles on 1 KB boundaries");
@@ -466,6 +482,7 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
     const uint32_t sbase = tc::smem_addr(smem);
     const uint32_t mb_raw = sbase + p1::MBAR, mb_mma = sbase + p1::MBAR + 8;
     Gates *gates = reinterpret_cast<Gates *>(smem + p1::GATES);
+    float *cft = reinterpret_cast<float *>(smem + p1::CF);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + p1::SLOT + 4);
     const uint64_t lim = a.wait_ns;
 
@@ -491,7 +508,7 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
 
     // the first head pair's gates, while the rows are in flight (they read nothing staged)
     if (warp < 2 && warp < r)
-        chunk_gates<TIn>(a, b, hk * r + warp, c0, n, gates + warp);
+        chunk_gates<TIn>(a, b, hk * r + warp, c0, n, gates + warp, cft + warp * 192);
 
     // Q and K rows: conv + SiLU + L2 (warp = 8-token block, lane = 4 channels) -> [Q; K] tile
     bool ok = tc::mbar_wait_ns(mb_raw, 0, lim, abort);
@@ -559,7 +576,7 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
 #pragma unroll 1
     for (int hp = 0; ok && hp < r; hp += 2) {
         if (hp > 0 && warp < 2 && hp + warp < r)
-            chunk_gates<TIn>(a, b, hk * r + hp + warp, c0, n, gates + warp);
+            chunk_gates<TIn>(a, b, hk * r + hp + warp, c0, n, gates + warp, cft + warp * 192);
         tc::fence_smem_to_async();
         __syncthreads();
         if (tid == 0) {      // the gates travel with the chunk's image
@@ -581,17 +598,36 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
             uint8_t *pimg = chunk_image(a, b, hk * r + hh, c) + kImgP;
             float *A = Am + hsel * kC * kC;
             const int tmax = 32 * (q4 & 1) + 31;              // largest row of this warp
+            // Below the 16-token diagonal blocks the decay factors split at the start of the
+            // row's block, exp(Gam_t - Gam_s) = exp(Gam_t - Gam_16I) exp(Gam_16I - Gam_s),
+            // both factors at most 1; inside them each factor is formed on its own.
+            const int I = t >> 4, Iw = (32 * (q4 & 1)) >> 4;  // the row's block, the warp's first
+            const float rf = exp_diff_fast(gt, gtl, G->gh[16 * I], G->gl[16 * I]);
+            const float *cfI = cft + hsel * 192 + 64 * (I > 0 ? I - 1 : 0);
 #pragma unroll 1
             for (int s0 = 0; s0 < kC; s0 += 16) {
+                const int J = s0 >> 4;
                 float gv[16];
                 if (s0 <= tmax)                               // warp-uniform
                     tc::tmem_ld16(tmem + lane_q + s0, gv);
                 float o[16];
+                if (J > Iw + 1) {                             // above every row of the warp
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int s = s0 + e;
-                    const bool keep = t < n && (is_a ? s < t : s <= t);
-                    o[e] = keep ? __fmul_rn(__fmul_rn(rowf, exp_diff_fast(gt, gtl, G->gh[s], G->gl[s])), gv[e]) : 0.0f;
+                    for (int e = 0; e < 16; ++e)
+                        o[e] = 0.0f;
+                } else if (J < Iw) {                          // below every row's diagonal block
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        o[e] = t < n ? __fmul_rn(__fmul_rn(rowf, __fmul_rn(rf, cfI[s0 + e])), gv[e]) : 0.0f;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int s = s0 + e;
+                        const bool keep = t < n && (is_a ? s < t : s <= t);
+                        const float f = J < I ? __fmul_rn(rf, cfI[s])
+                                              : exp_diff_fast(gt, gtl, G->gh[s], G->gl[s]);
+                        o[e] = keep ? __fmul_rn(__fmul_rn(rowf, f), gv[e]) : 0.0f;
+                    }
                 }
                 if (is_a) {
 #pragma unroll
@@ -716,10 +752,10 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
 
 // ================================================================== pass 2
 namespace p2 {
-// warps 0-7: epilogue (two per TMEM lane quarter); warp 8: the issuer; warps 9-16: the
-// V conv and the gated norm (8 tokens each). 17 warps of 96 registers fit the SM's
-// 65536 registers with one CTA per SM.
-constexpr int kIssuerWarp = 8, kConvWarp0 = 9, kConvWarps = 8;
+// warps 0-7: epilogue (two per TMEM lane quarter); warp 8: the products; warp 9: the
+// workspace copies; warps 10-17: the V conv and the gated norm (8 tokens each). 18 warps
+// of at most 112 registers fit the SM's 65536 registers with one CTA per SM.
+constexpr int kIssuerWarp = 8, kCopyWarp = 9, kConvWarp0 = 10, kConvWarps = 8;
 constexpr int kConvThreads = 32 * kConvWarps, kConvTok = kC / kConvWarps;
 constexpr int kThreads = 32 * (kConvWarp0 + kConvWarps);
 constexpr uint32_t QB = 0;                        // Q rows of the chunk: two parts, [64 t][128 i] sw128
@@ -737,9 +773,9 @@ constexpr uint32_t BYTES = CONVW + kD * 16 + 1024;
 static_assert(BYTES <= 232448, "shared memory budget");
 static_assert(RAW % 1024 == 0 && KB % 1024 == 0, "tiles on 1 KB boundaries");
 // barriers: copies (expected bytes), products (commits), and role hand-offs
-enum { B_Q, B_K0, B_K1, B_T, B_G, B_P, B_RAW, B_M1, B_M1Q, B_M2, B_M3, B_PU,
+enum { B_Q, B_K0, B_K1, B_T, B_G, B_P, B_RAW, B_M1, B_M1QA, B_M1Q, B_M2, B_M3, B_PU,
        B_RAWFREE, B_V, B_OSFREE,       // the conv threads arrive
-       B_ST, B_X, B_U, B_OR, B_OS,     // 256 epilogue threads arrive
+       B_ST, B_X, B_U, B_UP, B_OR, B_OS,   // 256 epilogue threads arrive
        B_N };
 static_assert(B_N <= 24, "barrier slots");
 // TMEM columns: TS the fp32 state master (S^T), D1 = [(Q S_0)^T | (K S_0)^T], R1 the
@@ -1001,16 +1037,13 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
         // drain: the staged-row copy in flight lands before the CTA ends
         if (raw_issuer && raw_last >= 0 && !tc::mbar_wait_ns(bar(B_RAW), raw_last & 1, lim))
             atomicOr(&g_device_error, (int)kErrDrain);
-    } else if (warp == kIssuerWarp) {
-        // ============================================ issuer: every workspace copy and product
-        // Lane 0 walks the chunks, issuing each copy and product as soon as its inputs are
-        // ready and its destination is free. The products the next chunk waits for (K S_0,
-        // U = T X, the state update) go out apart from those only the readout needs
-        // ((Q S_0)^T, (P U)^T), which run on the tensor core while the epilogue works.
+    } else if (warp == kCopyWarp) {
+        // ============================================ copies: the workspace images and gates
+        // Lane 0 refills each shared-memory buffer from the workspace as soon as the products
+        // or epilogues that read its previous contents are done, so that the issuing lane of
+        // the products never waits behind a copy.
         if (lane == 0) {
             int q_last = -1, k_last0 = -1, k_last1 = -1, t_last = -1, g_last = -1, p_last = -1;
-            int last_commit = -1;
-            uint32_t last_phase = 0;
             auto issue_q = [&](int cc) {     // Q rows of chunk cc
                 tc::mbar_expect_tx(bar(B_Q), kQKRows);
                 tc::bulk_copy_g2s(sbase + QB, qk_image(a, b, hk, cc), kQKRows, bar(B_Q));
@@ -1039,6 +1072,68 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 tc::bulk_copy_g2s(sbase + PP, chunk_image(a, b, h, cc) + kImgP, 16384u, bar(B_P));
                 p_last = cc;
             };
+            issue_k(0);
+            if (nch > 1)
+                issue_k(1);
+            issue_q(0);
+            issue_g(0);
+            issue_t(0);
+            issue_p(0);
+            bool ok = true;
+#pragma unroll 1
+            // Each barrier waited on here cannot complete its next phase before this lane has
+            // waited for the current one: that phase needs a copy this lane issues after the
+            // wait (chunk c+1's gates, Q rows, T and P).
+            for (int c = 0; ok && c + 1 < nch; ++c) {
+                // chunk c+1's gates once every value row has read chunk c-1's (the buffer
+                // of c+1's parity): the epilogue has finished chunk c-1 when it publishes X^T
+                if (!(ok = waitb(B_X, c & 1, lim)))
+                    break;
+                issue_g(c + 1);
+                // the Q rows once (Q S_0)^T has read chunk c's
+                if (!(ok = waitb(B_M1Q, c & 1, lim)))
+                    break;
+                issue_q(c + 1);
+                // T (read by D2's product) and chunk c's K buffer (read by K S_0 and the state
+                // update) once the state update is done: a commit covers every earlier product
+                if (!(ok = waitb(B_M3, c & 1, lim)))
+                    break;
+                issue_t(c + 1);
+                if (c + 2 < nch)
+                    issue_k(c + 2);
+                // P once (P U)^T has read chunk c's
+                if (!(ok = waitb(B_PU, c & 1, lim)))
+                    break;
+                issue_p(c + 1);
+            }
+            // drain: copies in flight land before the CTA releases its shared memory
+            bool drained = true;
+            if (q_last >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_Q), q_last & 1, lim);
+            if (k_last0 >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_K0), (k_last0 >> 1) & 1, lim);
+            if (k_last1 >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_K1), (k_last1 >> 1) & 1, lim);
+            if (t_last >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_T), t_last & 1, lim);
+            if (g_last >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_G), g_last & 1, lim);
+            if (p_last >= 0)
+                drained &= tc::mbar_wait_ns(bar(B_P), p_last & 1, lim);
+            if (!drained)
+                atomicOr(&g_device_error, (int)kErrDrain);
+        }
+        __syncwarp();
+    } else if (warp == kIssuerWarp) {
+        // ============================================ issuer: every product
+        // Lane 0 walks the chunks, issuing each product as soon as its operands are ready and
+        // its accumulator is free. Per chunk the tensor pipe, which runs products in issue
+        // order, gets K S_0, part A of (Q S_0)^T, U = T X, part B of (Q S_0)^T, the state
+        // update and (P U)^T: the three the next chunk waits for, with the readout's in the
+        // gaps while the epilogue works.
+        if (lane == 0) {
+            int last_commit = -1;
+            uint32_t last_phase = 0;
             auto commit = [&](int i, int c) {   // a commit tracks every product issued before it
                 tc::mma_commit(bar(i));
                 last_commit = i;
@@ -1050,8 +1145,9 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             auto issue_m1k = [&](int c) -> bool {
                 const int kb = c & 1;
                 // the first wait of the kernel takes its limit from first_wait_ns (a test hook)
-                if (!waitb(B_K0 + kb, (c >> 1) & 1, c == 0 ? a.first_wait_ns : lim) ||
-                    !waitb(B_ST, c & 1, lim))
+                if (!waitb(B_K0 + kb, (c >> 1) & 1, c == 0 ? a.first_wait_ns : lim))
+                    return false;
+                if (!waitb(B_ST, c & 1, lim))
                     return false;
                 tc::fence_after_sync();
                 const uint32_t kt = sbase + KB + kb * kQKRows;
@@ -1067,39 +1163,44 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 commit(B_M1, c);
                 return true;
             };
-            // D1[:, 0..63] = S_0^T Q^T, once the Q rows are in and the previous chunk's readout
-            // has read these columns
-            auto issue_m1q = [&](int c) -> bool {
+            // D1[:, 0..63] = S_0^T Q^T in two parts, so that the tensor pipe (which runs
+            // products in issue order) holds no more of it before D2's product than fits
+            // while the epilogue forms X. Part A, the terms of the low part of S_0^T (which
+            // U'^T overwrites once D2 is done), once the Q rows are in and the previous
+            // chunk's readout has read these columns:
+            auto issue_m1q_lo = [&](int c) -> bool {
                 if ((c > 0 && !waitb(B_OR, (c - 1) & 1, lim)) || !waitb(B_Q, c & 1, lim))
                     return false;
                 tc::fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t ko = (kk >> 2) * 8192 + (kk & 3) * 32;
-                    const uint32_t shi = tmem + R1 + 8 * kk, slo = tmem + R1 + 64 + 8 * kk;
-                    const uint64_t q1 = tc::sdesc_sw128(sbase + QB + ko);
-                    const uint64_t q2 = tc::sdesc_sw128(sbase + QB + kQKPart + ko);
-                    tc::mma_f16_ta(tmem + D1, shi, q1, id64, kk > 0);
-                    tc::mma_f16_ta(tmem + D1, shi, q2, id64, 1);
-                    tc::mma_f16_ta(tmem + D1, slo, q1, id64, 1);
+                    const uint32_t slo = tmem + R1 + 64 + 8 * kk;
+                    tc::mma_f16_ta(tmem + D1, slo, tc::sdesc_sw128(sbase + QB + ko), id64, kk > 0);
                 }
-                commit(B_M1Q, c);
+                commit(B_M1QA, c);
                 return true;
             };
-            // D2 = X^T T^T, once every value row's X^T is in TMEM and T has arrived; the next
-            // chunk's gates (every value row has read chunk c-1's) and its Q rows once this
-            // chunk's (Q S_0)^T has read them (that product also has to finish before U'^T
-            // overwrites the low part of S_0^T)
+            // part B, the terms of the high part (rewritten only after the state update),
+            // issued right after D2's product
+            auto issue_m1q_hi = [&](int c) {
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t ko = (kk >> 2) * 8192 + (kk & 3) * 32;
+                    const uint32_t shi = tmem + R1 + 8 * kk;
+                    tc::mma_f16_ta(tmem + D1, shi, tc::sdesc_sw128(sbase + QB + ko), id64, 1);
+                    tc::mma_f16_ta(tmem + D1, shi, tc::sdesc_sw128(sbase + QB + kQKPart + ko), id64, 1);
+                }
+                commit(B_M1Q, c);
+            };
+            // D2 = X^T T^T, once every value row's X^T is in TMEM and T has arrived, then part
+            // B of (Q S_0)^T. A commit tracks every product issued before it, so B_M2 also
+            // covers part A: the epilogue that overwrites the low part of S_0^T with U'^T
+            // waits for B_M2 only.
             auto issue_m2 = [&](int c) -> bool {
-                if (!waitb(B_X, c & 1, lim))
-                    return false;
-                if (c + 1 < nch)
-                    issue_g(c + 1);
-                if (!waitb(B_T, c & 1, lim) || !waitb(B_M1Q, c & 1, lim))
+                if (!waitb(B_X, c & 1, lim) || !waitb(B_T, c & 1, lim))
                     return false;
                 tc::fence_after_sync();
-                if (c + 1 < nch)
-                    issue_q(c + 1);
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk) {
                     const uint64_t b1 = tc::sdesc(sbase + TT + kk * 256, 128, 1024);
@@ -1110,16 +1211,14 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                     tc::mma_f16_ta(tmem + D2, xlo, b1, id64, 1);
                 }
                 commit(B_M2, c);
+                issue_m1q_hi(c);
                 return true;
             };
-            // the next chunk's T once D2's product has read this chunk's; then S^T += U'^T K (K
-            // rows read MN-major) and (P U)^T = U^T P^T into D2 (U^T has been read from it)
+            // S^T += U'^T K (K rows read MN-major) once U'^T is written; then, once the U^T
+            // operand is written and D2's columns have been read (B_UP) and P has arrived,
+            // (P U)^T = U^T P^T into D2
             auto issue_m3 = [&](int c) -> bool {
-                if (!waitb(B_M2, c & 1, lim))
-                    return false;
-                if (c + 1 < nch)
-                    issue_t(c + 1);
-                if (!waitb(B_U, c & 1, lim) || !waitb(B_P, c & 1, lim))
+                if (!waitb(B_U, c & 1, lim))
                     return false;
                 tc::fence_after_sync();
                 const uint32_t kt = sbase + KB + (c & 1) * kQKRows;
@@ -1134,6 +1233,9 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                     tc::mma_f16_ta(tmem + TS, uplo, k1, id128 | tc::kIdescTransB, 1);
                 }
                 commit(B_M3, c);
+                if (!waitb(B_UP, c & 1, lim) || !waitb(B_P, c & 1, lim))
+                    return false;
+                tc::fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk) {
                     const uint64_t p1d = tc::sdesc(sbase + PP + kk * 256, 128, 1024);
@@ -1146,48 +1248,12 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 commit(B_PU, c);
                 return true;
             };
-            issue_k(0);
-            if (nch > 1)
-                issue_k(1);
-            issue_q(0);
-            issue_g(0);
-            issue_t(0);
-            issue_p(0);
-            bool ok = issue_m1k(0) && issue_m1q(0);
+            bool ok = true;
 #pragma unroll 1
-            for (int c = 0; ok && c < nch; ++c) {
-                if (!(ok = issue_m2(c) && issue_m3(c)) || c + 1 >= nch)
-                    break;
-                // this chunk's K rows have been read by both of its products
-                if (!(ok = waitb(B_M3, c & 1, lim)))
-                    break;
-                if (c + 2 < nch)
-                    issue_k(c + 2);
-                if (!(ok = issue_m1k(c + 1)))
-                    break;
-                // this chunk's P has been read by its product
-                if (!(ok = waitb(B_PU, c & 1, lim)))
-                    break;
-                issue_p(c + 1);
-                ok = issue_m1q(c + 1);
-            }
-            // drain: copies and products in flight finish before the CTA releases TMEM
-            bool drained = true;
-            if (last_commit >= 0)
-                drained &= tc::mbar_wait_ns(bar(last_commit), last_phase, lim);
-            if (q_last >= 0)
-                drained &= tc::mbar_wait_ns(bar(B_Q), q_last & 1, lim);
-            if (k_last0 >= 0)
-                drained &= tc::mbar_wait_ns(bar(B_K0), (k_last0 >> 1) & 1, lim);
-            if (k_last1 >= 0)
-                drained &= tc::mbar_wait_ns(bar(B_K1), (k_last1 >> 1) & 1, lim);
-            if (t_last >= 0)
-                drained &= tc::mbar_wait_ns(bar(B_T), t_last & 1, lim);
-            if (g_last >= 0)
-                drained &= tc::mbar_wait_ns(bar(B_G), g_last & 1, lim);
-            if (p_last >= 0)
-                drained &= tc::mbar_wait_ns(bar(B_P), p_last & 1, lim);
-            if (!drained)
+            for (int c = 0; ok && c < nch; ++c)
+                ok = issue_m1k(c) && issue_m1q_lo(c) && issue_m2(c) && issue_m3(c);
+            // drain: products in flight finish before the CTA releases TMEM
+            if (last_commit >= 0 && !tc::mbar_wait_ns(bar(last_commit), last_phase, lim))
                 atomicOr(&g_device_error, (int)kErrDrain);
         }
         __syncwarp();
@@ -1258,6 +1324,11 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 tmem_st8u(tl + XU + tb0 / 2, hi);
                 tmem_st8u(tl + XU + 32 + tb0 / 2, lo);
             }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            tc::mbar_arrive(bar(B_X));
+            // the state master scaled by e^{Gam_C} while D2's product runs: only the state
+            // update reads it, and that is issued after B_U (whose fence covers these stores)
             {
                 const float ec = __fmul_rn(G->ec, exp2i(rho_next - rho));
 #pragma unroll
@@ -1270,14 +1341,33 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                     tc::tmem_st16(tl + TS + 64 * hf + 16 * k, sv);
                 }
             }
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            tc::mbar_arrive(bar(B_X));
-            // ---- U = T X (from D2): U^T for the output product, U'^T = U^T diag(e^{Gam_C - Gam})
-            //      for the state update
+            // ---- U = T X (from D2): first U'^T = U^T diag(e^{Gam_C - Gam}) for the state
+            //      update (B_U), then U^T for the output product (B_UP), which also reads D2's
+            //      columns again before that product overwrites them
             if (!(ok = waitb(B_M2, par, lim)))
                 break;
             tc::fence_after_sync();
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const int tb0 = 32 * hf + 16 * p;
+                float u[16];
+                tc::tmem_ld16(tl + D2 + tb0, u);
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const float4 g4 = ld4(G->egc + tb0 + 4 * qq);
+                    u[4 * qq + 0] = __fmul_rn(u[4 * qq + 0], __fmul_rn(g4.x, s_out));
+                    u[4 * qq + 1] = __fmul_rn(u[4 * qq + 1], __fmul_rn(g4.y, s_out));
+                    u[4 * qq + 2] = __fmul_rn(u[4 * qq + 2], __fmul_rn(g4.z, s_out));
+                    u[4 * qq + 3] = __fmul_rn(u[4 * qq + 3], __fmul_rn(g4.w, s_out));
+                }
+                uint32_t hi[8], lo[8];
+                pack_split16(u, hi, lo);
+                tmem_st8u(tl + R1 + 64 + tb0 / 2, hi);
+                tmem_st8u(tl + R1 + 96 + tb0 / 2, lo);
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            tc::mbar_arrive(bar(B_U));
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
                 const int tb0 = 32 * hf + 16 * p;
@@ -1287,21 +1377,10 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 pack_split16(u, hi, lo);
                 tmem_st8u(tl + XU + tb0 / 2, hi);
                 tmem_st8u(tl + XU + 32 + tb0 / 2, lo);
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const float4 g4 = ld4(G->egc + tb0 + 4 * qq);
-                    u[4 * qq + 0] = __fmul_rn(u[4 * qq + 0], __fmul_rn(g4.x, s_out));
-                    u[4 * qq + 1] = __fmul_rn(u[4 * qq + 1], __fmul_rn(g4.y, s_out));
-                    u[4 * qq + 2] = __fmul_rn(u[4 * qq + 2], __fmul_rn(g4.z, s_out));
-                    u[4 * qq + 3] = __fmul_rn(u[4 * qq + 3], __fmul_rn(g4.w, s_out));
-                }
-                pack_split16(u, hi, lo);
-                tmem_st8u(tl + R1 + 64 + tb0 / 2, hi);
-                tmem_st8u(tl + R1 + 96 + tb0 / 2, lo);
             }
             tc::tmem_wait_st();
             tc::fence_before_sync();
-            tc::mbar_arrive(bar(B_U));
+            tc::mbar_arrive(bar(B_UP));
             // ---- the updated state: the next chunk's S_0^T operand (its first product follows)
             if (!(ok = waitb(B_M3, par, lim)))
                 break;
