@@ -446,6 +446,56 @@ static_assert(QK % 1024 == 0, "swizzled tiles on 1 KB boundaries");
 // A[t][s] and T[i][j] (fp32, 64 floats per row), float4 chunks XOR-swizzled by the row
 __device__ __forceinline__ int a_idx(int t, int s) { return t * kC + ((((s >> 2) ^ (t & 15))) << 2) + (s & 3); }
 
+// Warp-level 16 x 16 block products for the chunk's (I + A)^-1 (blocks too small for the
+// CTA-wide tcgen05 products): D += A B with A 16 x 16 and B 16 x 8, fp16 operands, fp32
+// accumulation; g = lane / 4 and q = lane % 4 index the PTX fragment layouts.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// The 16 x 16 block at (r0, c0) of an a_idx-laid fp32 matrix as the A operand (two fp16 parts)
+__device__ __forceinline__ void blk_a(const float *M, int r0, int c0, int lane, uint32_t (&hi)[4], uint32_t (&lo)[4])
+{
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int row = r0 + g + 8 * (i & 1), col = c0 + 2 * q + 8 * (i >> 1);
+        const float2 v = *reinterpret_cast<const float2 *>(M + a_idx(row, col));
+        split_pair(v.x, v.y, hi[i], lo[i]);
+    }
+}
+// The 16 x 8 block at (r0, c0) as the B operand (B[k][n] = M[r0 + k][c0 + n]), two fp16 parts
+__device__ __forceinline__ void blk_b(const float *M, int r0, int c0, int lane, uint32_t (&hi)[2], uint32_t (&lo)[2])
+{
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int row = r0 + 2 * q + 8 * i;
+        split_pair(M[a_idx(row, c0 + g)], M[a_idx(row + 1, c0 + g)], hi[i], lo[i]);
+    }
+}
+// D += A B with both operands in two fp16 parts (the product of the low parts is dropped)
+__device__ __forceinline__ void mma_16816_x3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                             const uint32_t (&bh)[2], const uint32_t (&bl)[2])
+{
+    mma_16816(d, ah, bh[0], bh[1]);
+    mma_16816(d, ah, bl[0], bl[1]);
+    mma_16816(d, al, bh[0], bh[1]);
+}
+// A 16 x 16 accumulator (two 16 x 8 halves), times s, into the block at (r0, c0)
+__device__ __forceinline__ void blk_store(float *M, int r0, int c0, int lane, const float (&d)[2][4], float s)
+{
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            *reinterpret_cast<float2 *>(M + a_idx(r0 + g + 8 * i, c0 + 8 * h + 2 * q)) =
+                make_float2(__fmul_rn(d[h][2 * i], s), __fmul_rn(d[h][2 * i + 1], s));
+}
+
 // One chunk's image in the workspace: T = (I + A)^-1 then P, each as two fp16
 // parts of a [64][64] K-major core-matrix tile (8 KB per part), then the gates.
 constexpr uint32_t kImgP = 16384, kImgGates = 32768;
@@ -650,62 +700,67 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
             }
         }
         __syncthreads();
-        // ---- T = (I + A)^-1, two threads per column j (the row blocks of the sum split by
-        //      parity), blocks of 8 rows: T[i][j] = [i == j] - sum_{s < i} A[i][s] T[s][j]
-        {
-            const int hs = tid >> 7, j = (tid >> 1) & 63, half = tid & 1;
-            if (hp + hs < r) {
-                const float *A = Am + hs * kC * kC;
-                float *Tc = Tb + hs * kC * kC;
-                const int S0 = 2 * (warp & 3);                 // T[s][j] = 0 for s < j: skip those blocks
+        // ---- T = (I + A)^-1 in 16-token blocks. Warp I of a head inverts the diagonal block
+        //      T_II = (I + A_II)^-1 by forward substitution (lane j: column j) and clears the
+        //      blocks right of it; then warp J walks block column J on its own:
+        //      T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ for I = J+1 .. 3.
+        const int hs = tid >> 7, wb = (tid >> 5) & 3;
+        float *Tc = Tb + hs * kC * kC;
+        const float *Ah = Am + hs * kC * kC;
+        if (hp + hs < r) {
+            const int r0 = 16 * wb;
+            if (lane < 16) {
+                float x[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    x[q] = q == lane ? 1.0f : 0.0f;
+#pragma unroll
+                for (int e = 0; e < 15; ++e)
+#pragma unroll
+                    for (int q = e + 1; q < 16; ++q)
+                        x[q] = __fmaf_rn(-Ah[a_idx(r0 + q, r0 + e)], x[e], x[q]);
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    Tc[a_idx(r0 + q, r0 + lane)] = x[q];
+            } else {
+                const int w4 = 4 * (3 - wb);                    // float4 slots per row right of it
+                for (int i = lane - 16; i < 16 * w4; i += 16)
+                    *reinterpret_cast<float4 *>(Tc + a_idx(r0 + i / w4, 16 * (wb + 1) + 4 * (i % w4))) =
+                        make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+        }
+        __syncthreads();
+        if (hp + hs < r) {
+            const int J = wb;
 #pragma unroll 1
-                for (int I = 0; I < 8; ++I) {
-                    float acc[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        acc[q] = 0.0f;
+            for (int I = J + 1; I < 4; ++I) {
+                float d[2][4] = {};
 #pragma unroll 1
-                    for (int S = S0 + half; S < I; S += 2) {
-                        float ts[8];
+                for (int K = J; K < I; ++K) {
+                    uint32_t ah[4], al[4];
+                    blk_a(Ah, 16 * I, 16 * K, lane, ah, al);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            ts[e] = Tc[a_idx(8 * S + e, j)];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int i = 8 * I + q;
-                            const float4 a0 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * S));
-                            const float4 a1 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * S + 4));
-                            acc[q] = __fmaf_rn(a0.x, ts[0], acc[q]);
-                            acc[q] = __fmaf_rn(a0.y, ts[1], acc[q]);
-                            acc[q] = __fmaf_rn(a0.z, ts[2], acc[q]);
-                            acc[q] = __fmaf_rn(a0.w, ts[3], acc[q]);
-                            acc[q] = __fmaf_rn(a1.x, ts[4], acc[q]);
-                            acc[q] = __fmaf_rn(a1.y, ts[5], acc[q]);
-                            acc[q] = __fmaf_rn(a1.z, ts[6], acc[q]);
-                            acc[q] = __fmaf_rn(a1.w, ts[7], acc[q]);
-                        }
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t bh[2], bl[2];
+                        blk_b(Tc, 16 * K, 16 * J + 8 * h, lane, bh, bl);
+                        mma_16816_x3(d[h], ah, al, bh, bl);
                     }
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        acc[q] = __fadd_rn(acc[q], __shfl_xor_sync(0xffffffffu, acc[q], 1));
-                    float x[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int i = 8 * I + q;
-                        const float4 a0 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * I));
-                        const float4 a1 = *reinterpret_cast<const float4 *>(A + a_idx(i, 8 * I + 4));
-                        const float ad[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                        float sum = acc[q];
-#pragma unroll
-                        for (int e = 0; e < q; ++e)
-                            sum = __fmaf_rn(ad[e], x[e], sum);
-                        x[q] = __fsub_rn(i == j ? 1.0f : 0.0f, sum);
-                    }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        Tc[a_idx(8 * I + 4 * half + q, j)] = x[4 * half + q];
-                    __syncwarp();
                 }
+                // the sum goes through T_IJ's place to become the B operand of T_II (.)
+                blk_store(Tc, 16 * I, 16 * J, lane, d, 1.0f);
+                __syncwarp();
+                uint32_t ah[4], al[4];
+                blk_a(Tc, 16 * I, 16 * I, lane, ah, al);
+                float e[2][4] = {};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t bh[2], bl[2];
+                    blk_b(Tc, 16 * I, 16 * J + 8 * h, lane, bh, bl);
+                    mma_16816_x3(e[h], ah, al, bh, bl);
+                }
+                __syncwarp();
+                blk_store(Tc, 16 * I, 16 * J, lane, e, -1.0f);
+                __syncwarp();
             }
         }
         __syncthreads();
