@@ -516,7 +516,7 @@ __device__ __forceinline__ uint8_t *qk_image(const PrefillArgs &a, int b, int hk
 }
 
 template <typename TIn, int WC>
-__global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_constant__ CUtensorMap xmap,
+__global__ void __launch_bounds__(p1::kThreads, 2) prefill_ut_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                 PrefillArgs a, int staged)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -714,11 +714,22 @@ __global__ void __launch_bounds__(p1::kThreads) prefill_ut_kernel(const __grid_c
 #pragma unroll
                 for (int q = 0; q < 16; ++q)
                     x[q] = q == lane ? 1.0f : 0.0f;
+                // four columns of the block at a time: rows q > e4 of A_II[:, e4 .. e4+3] as
+                // float4 loads issued together, then four substitution steps from registers
 #pragma unroll
-                for (int e = 0; e < 15; ++e)
+                for (int e4 = 0; e4 < 16; e4 += 4) {
+                    float4 ac[16];
 #pragma unroll
-                    for (int q = e + 1; q < 16; ++q)
-                        x[q] = __fmaf_rn(-Ah[a_idx(r0 + q, r0 + e)], x[e], x[q]);
+                    for (int q = e4 + 1; q < 16; ++q)
+                        ac[q] = *reinterpret_cast<const float4 *>(Ah + a_idx(r0 + q, r0 + e4));
+#pragma unroll
+                    for (int e = e4; e < e4 + 4 && e < 15; ++e)
+#pragma unroll
+                        for (int q = e + 1; q < 16; ++q) {
+                            const float av = e == e4 ? ac[q].x : e == e4 + 1 ? ac[q].y : e == e4 + 2 ? ac[q].z : ac[q].w;
+                            x[q] = __fmaf_rn(-av, x[e], x[q]);
+                        }
+                }
 #pragma unroll
                 for (int q = 0; q < 16; ++q)
                     Tc[a_idx(r0 + q, r0 + lane)] = x[q];
