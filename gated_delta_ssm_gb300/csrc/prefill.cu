@@ -647,38 +647,14 @@ __global__ void __launch_bounds__(p1::kThreads, 2) prefill_ut_kernel(const __gri
             const float rowf = is_a ? __fmul_rn(G->beta[t], kInvQK2) : kInvQK2;
             uint8_t *pimg = chunk_image(a, b, hk * r + hh, c) + kImgP;
             float *A = Am + hsel * kC * kC;
-            const int tmax = 32 * (q4 & 1) + 31;              // largest row of this warp
             // Below the 16-token diagonal blocks the decay factors split at the start of the
             // row's block, exp(Gam_t - Gam_s) = exp(Gam_t - Gam_16I) exp(Gam_16I - Gam_s),
             // both factors at most 1; inside them each factor is formed on its own.
             const int I = t >> 4, Iw = (32 * (q4 & 1)) >> 4;  // the row's block, the warp's first
             const float rf = exp_diff_fast(gt, gtl, G->gh[16 * I], G->gl[16 * I]);
             const float *cfI = cft + hsel * 192 + 64 * (I > 0 ? I - 1 : 0);
-#pragma unroll 1
-            for (int s0 = 0; s0 < kC; s0 += 16) {
-                const int J = s0 >> 4;
-                float gv[16];
-                if (s0 <= tmax)                               // warp-uniform
-                    tc::tmem_ld16(tmem + lane_q + s0, gv);
-                float o[16];
-                if (J > Iw + 1) {                             // above every row of the warp
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        o[e] = 0.0f;
-                } else if (J < Iw) {                          // below every row's diagonal block
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        o[e] = t < n ? __fmul_rn(__fmul_rn(rowf, __fmul_rn(rf, cfI[s0 + e])), gv[e]) : 0.0f;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int s = s0 + e;
-                        const bool keep = t < n && (is_a ? s < t : s <= t);
-                        const float f = J < I ? __fmul_rn(rf, cfI[s])
-                                              : exp_diff_fast(gt, gtl, G->gh[s], G->gl[s]);
-                        o[e] = keep ? __fmul_rn(__fmul_rn(rowf, f), gv[e]) : 0.0f;
-                    }
-                }
+            // one 16-column block of the row: A to shared memory, P as its two-part image
+            auto store_blk = [&](int s0, const float (&o)[16]) {
                 if (is_a) {
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq)
@@ -697,6 +673,48 @@ __global__ void __launch_bounds__(p1::kThreads, 2) prefill_ut_kernel(const __gri
                         *reinterpret_cast<uint4 *>(pimg + 8192 + off) = lo;
                     }
                 }
+            };
+            // column blocks wholly below the warp's rows' diagonal blocks, or wholly above
+#pragma unroll 1
+            for (int J = 0; J < 4; ++J) {
+                if (J == Iw || J == Iw + 1)                   // warp-uniform
+                    continue;
+                float o[16];
+                if (J > Iw + 1) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        o[e] = 0.0f;
+                } else {
+                    float gv[16];
+                    tc::tmem_ld16(tmem + lane_q + 16 * J, gv);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        o[e] = t < n ? __fmul_rn(__fmul_rn(rowf, __fmul_rn(rf, cfI[16 * J + e])), gv[e]) : 0.0f;
+                }
+                store_blk(16 * J, o);
+            }
+            // the warp's own two row blocks: each lane forms the decay factors of its own
+            // diagonal block only; of the other block, lanes of the second row block need
+            // the part below their diagonal, lanes of the first the zero part above it
+            {
+                float ga[16], gb[16];
+                tc::tmem_ld16(tmem + lane_q + 16 * Iw, ga);
+                tc::tmem_ld16(tmem + lane_q + 16 * (Iw + 1), gb);
+                const bool first = I == Iw;
+                float od[16], oo[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int s = 16 * I + e;
+                    const bool keep = t < n && (is_a ? s < t : s <= t);
+                    od[e] = keep ? __fmul_rn(__fmul_rn(rowf, exp_diff_fast(gt, gtl, G->gh[s], G->gl[s])),
+                                             first ? ga[e] : gb[e])
+                                 : 0.0f;
+                    oo[e] = !first && t < n
+                                ? __fmul_rn(__fmul_rn(rowf, __fmul_rn(rf, cfI[16 * Iw + e])), ga[e])
+                                : 0.0f;
+                }
+                store_blk(16 * I, od);
+                store_blk(16 * (first ? Iw + 1 : Iw), oo);
             }
         }
         __syncthreads();
