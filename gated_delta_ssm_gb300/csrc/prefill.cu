@@ -283,7 +283,7 @@ __device__ __forceinline__ void lds_row4(uint32_t saddr, float (&v)[4])
     v[2] = __uint_as_float(y << 16); v[3] = __uint_as_float(y & 0xFFFF0000u);
 }
 
-template <typename TIn, int WC, int NCH>
+template <typename TIn, int WC, int NCH, bool kSilu = true>
 __device__ __forceinline__ void conv_block(const PrefillArgs &a, int b, int c0, int n, int ch0,
                                            int t0, bool staged, uint32_t raw_s, float (&out)[8][NCH],
                                            const float4 *wsm = nullptr, int wstride = 0)
@@ -363,7 +363,7 @@ __device__ __forceinline__ void conv_block(const PrefillArgs &a, int b, int c0, 
         const bool live = t0 + t < n;
 #pragma unroll
         for (int e = 0; e < NCH; ++e)
-            out[t][e] = live ? silu_f(out[t][e]) : 0.0f;
+            out[t][e] = live ? (kSilu ? silu_f(out[t][e]) : out[t][e]) : 0.0f;
     }
 }
 
@@ -844,7 +844,7 @@ constexpr int kConvThreads = 32 * kConvWarps, kConvTok = kC / kConvWarps;
 constexpr int kThreads = 32 * (kConvWarp0 + kConvWarps);
 constexpr uint32_t QB = 0;                        // Q rows of the chunk: two parts, [64 t][128 i] sw128
 constexpr uint32_t KB = 32768;                    // K rows, two buffers (even and odd chunks)
-constexpr uint32_t VF = 98304;                    // V^T fp32 footprint [128 j][64 t]
+constexpr uint32_t VF = 98304;                    // V^T fp32 footprint [128 j][64 t], before SiLU
 constexpr uint32_t TT = 131072;                   // T image of the current chunk (16 KB)
 constexpr uint32_t PP = 147456;                   // P image of the current chunk (16 KB)
 constexpr uint32_t OS = 163840;                   // O staging, fp32 [64 t][128 j]
@@ -1070,13 +1070,14 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 z_prefetch(c - 1);
             if (staged && !(ok = waitb(B_RAW, c & 1, lim)))
                 break;
-            // V^T of chunk c, 8 tokens at a time, written once chunk c-1's X has read the
-            // footprint
+            // V^T of chunk c before its SiLU (the epilogue applies it as it reads V for X,
+            // which moves that work off these warps), 8 tokens at a time, written once
+            // chunk c-1's X has read the footprint
             bool x_seen = c == 0;
 #pragma unroll
             for (int k = 0; k < kConvTok / 8; ++k) {
                 float v[8][4];
-                conv_block<TIn, WC, 4>(a, b, c0, n, v_ch, kConvTok * cw + 8 * k, staged != 0, sbase + RAW,
+                conv_block<TIn, WC, 4, false>(a, b, c0, n, v_ch, kConvTok * cw + 8 * k, staged != 0, sbase + RAW,
                                        v, v_w, 32);
                 if (!x_seen && !(ok = x_seen = waitb(B_X, (c - 1) & 1, lim)))
                     break;
@@ -1396,7 +1397,8 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 float x[16];
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
-                    const float4 f = *reinterpret_cast<const float4 *>(smem + foot_off(j, tb0 / 4 + qq));
+                    float4 f = *reinterpret_cast<const float4 *>(smem + foot_off(j, tb0 / 4 + qq));
+                    f.x = silu_f(f.x); f.y = silu_f(f.y); f.z = silu_f(f.z); f.w = silu_f(f.w);
                     const float4 bt = ld4(G->beta + tb0 + 4 * qq), bg = ld4(G->bg + tb0 + 4 * qq);
                     x[4 * qq + 0] = __fsub_rn(__fmul_rn(bt.x, f.x), __fmul_rn(__fmul_rn(bg.x, s_in), ks[4 * qq + 0]));
                     x[4 * qq + 1] = __fsub_rn(__fmul_rn(bt.y, f.y), __fmul_rn(__fmul_rn(bg.y, s_in), ks[4 * qq + 1]));
