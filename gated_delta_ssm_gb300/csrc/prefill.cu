@@ -1179,13 +1179,15 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 if (!(ok = waitb(B_M1Q, c & 1, lim)))
                     break;
                 issue_q(c + 1);
-                // T (read by D2's product) and chunk c's K buffer (read by K S_0 and the state
-                // update) once the state update is done: a commit covers every earlier product
+                // chunk c's K buffer (read by K S_0 and the state update) and T (read by D2's
+                // product) once the state update is done: a commit covers every earlier
+                // product. K first: chunk c+2's first product waits for it, while T is needed
+                // only after chunk c+1's X.
                 if (!(ok = waitb(B_M3, c & 1, lim)))
                     break;
-                issue_t(c + 1);
                 if (c + 2 < nch)
                     issue_k(c + 2);
+                issue_t(c + 1);
                 // P once (P U)^T has read chunk c's
                 if (!(ok = waitb(B_PU, c & 1, lim)))
                     break;
