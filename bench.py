@@ -429,15 +429,36 @@ class Gpu:
             j = i % nbuf
             gdn.verify_commit(d["states"][j], d["hists"][j], snaps[j], hsnaps[j], d["accept"], dims)
 
+        # the token after the verify: with the rollback folded in (each sequence reads the
+        # snapshot its accepted count selects), or the plain step that follows a commit;
+        # one token row of the two-token buffers is the step's input
+        zs = shape.xs if shape.z_in_x else shape.Hv * shape.d
+        step_dims = gdn.Dims(shape.B, shape.Hq, shape.Hv, shape.d, shape.W, 2 * shape.xs, 2 * zs, 2 * shape.Hv)
+        sout = torch.empty(shape.B, shape.Hv, shape.d, device=self.dev)
+        tok = {k: d[k][:, 0] for k in ("x", "z", "alpha", "beta_logit")}
+
+        def sstep(i):
+            j = i % nbuf
+            gdn.decode_step_select(d["states"][j], d["hists"][j], snaps[j], hsnaps[j], 1, d["accept"], 2,
+                                   tok["x"], tok["z"], tok["alpha"], tok["beta_logit"], prm, sout, step_dims)
+
+        def pstep(i):
+            j = i % nbuf
+            gdn.decode_step(d["states"][j], d["hists"][j], tok["x"], tok["z"], tok["alpha"],
+                            tok["beta_logit"], prm, sout, step_dims)
+
         tv = self.time_steps(vstep, steps, warmup)
         tc = self.time_steps(cstep, steps, warmup)
-        self.launches += 2 * steps
+        ts = self.time_steps(sstep, steps, warmup)
+        tp = self.time_steps(pstep, steps, warmup)
+        self.launches += 4 * steps
         sb = shape.B * shape.Hv * shape.d * shape.d * 4
         n_rb = int((inp["accept"] == 1).sum())
-        mv, mc = statistics.mean(tv), statistics.mean(tc)
+        mv, mc, ms, mp = (statistics.mean(t) for t in (tv, tc, ts, tp))
         return {"verify_us": mv * 1e6, "verify_state_GBps": 3 * sb / mv / 1e9,
                 "commit_us": mc * 1e6, "commit_GBps": 2 * n_rb * (sb // shape.B) / mc / 1e9,
-                "rollbacks": n_rb}
+                "rollbacks": n_rb, "select_step_us": ms * 1e6, "step_us": mp * 1e6,
+                "verify_commit_step_us": (mv + mc + mp) * 1e6, "verify_select_step_us": (mv + ms) * 1e6}
 
     # -- generic-K draft verification (K = 4) + commit, K=2 verify's batch
     def verify_kn(self, steps, warmup, K=4):
