@@ -113,7 +113,8 @@ __global__ void __launch_bounds__(256) gated_norm_kernel(const float *y, const f
 }
 
 // ------------------------------------------------------------------ fused step
-// NTOK = 1: one decode step. NTOK = 2: K=2 verify, snapshot after token 0.
+// NTOK = 1: one decode step. NTOK = 2: K=2 verify, snapshot after token 0, or
+// (with the per-token snapshot layout) the generic K-token verify for K = 2..4.
 //
 // Order of a CTA's work, chosen so that no fence ever waits on the state
 // loads or stores: (0) wait for the previous kernel in the stream (the launch
@@ -139,7 +140,12 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
     constexpr int RPW = ROWS / 8;       // rows per warp
     constexpr int NG = RPW / 4;         // 4-row groups per warp
     constexpr int NBLK = ROWS / 32;     // 32-row norm blocks in this CTA
-    constexpr bool SNAP = NTOK == 2;
+    constexpr bool SNAP = NTOK >= 2;
+    // snapshot layouts: the two-token verify keeps the state and conv window after token
+    // 0 (one entry); the generic form (conv_snap_entries == NTOK) keeps the state after
+    // each of the first NTOK - 1 tokens ([B][NTOK-1][Hv][d][d]) and the conv window after
+    // every token ([B][NTOK][conv_dim][W-1], the last one the committed window)
+    const bool per_token = SNAP && a.conv_snap_entries == NTOK;
     __shared__ __align__(16) float sq[NTOK * kD];
     __shared__ __align__(16) float sk[NTOK * kD];
     __shared__ float sv[NTOK * ROWS], sy[NTOK * ROWS];
@@ -297,8 +303,13 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
             sv[p * ROWS + tid] = silu_f(conv_window_pre<NTOK>(wv, W, p));
         float nh[kMaxW - 1];
         if (SNAP) {
-            conv_window_history<NTOK>(wv, W, 1, nh);
-            store_history(a.conv_snap + ((size_t)b * cd + c_v) * (W - 1), W, nh);
+#pragma unroll
+            for (int p = 0; p < NTOK; ++p)
+                if (per_token || p == 0) {
+                    conv_window_history<NTOK>(wv, W, p + 1, nh);
+                    store_history(a.conv_snap + ((size_t)(b * (per_token ? NTOK : 1) + p) * cd + c_v) * (W - 1),
+                                  W, nh);
+                }
         }
         conv_window_history<NTOK>(wv, W, NTOK, nh);
         store_history(histb + (size_t)c_v * (W - 1), W, nh);
@@ -316,18 +327,22 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
 
     // (5) recurrence over this CTA's rows, in registers; the rows go back to HBM group
     // by group as they are finished
-    step_rows<NG, NTOK, SNAP, TS, Reg>(st, SNAP ? static_cast<float *>(a.state_snap) + head_off + warp_off
-                                           : nullptr,
-                                  sk, sq, sv, ROWS, sdecay, sbeta, sy, warp * RPW, a.scale,
-                                  state + head_off + warp_off);
+    float *snap_rows = nullptr;
+    if (SNAP)
+        snap_rows = static_cast<float *>(a.state_snap) + warp_off +
+                    (per_token ? ((size_t)b * (NTOK - 1) * a.Hv + h) * kD * kD : head_off);
+    step_rows<NG, NTOK, SNAP, TS, Reg>(st, snap_rows, sk, sq, sv, ROWS, sdecay, sbeta, sy, warp * RPW,
+                                       a.scale, state + head_off + warp_off, per_token ? NTOK - 1 : 1,
+                                       (size_t)a.Hv * kD * kD);
     // this CTA's state stores are issued: a dependent launch that follows may make its
     // CTAs resident (it waits for this whole grid before it reads anything)
     allow_next_grid();
     __syncthreads();
 
     // (6) gated RMSNorm: 32-row block partials, combined in block order
-    if (warp < NTOK * NBLK) {
-        const int p = warp / NBLK, bl = warp % NBLK;
+#pragma unroll
+    for (int i = warp; i < NTOK * NBLK; i += 8) {
+        const int p = i / NBLK, bl = i % NBLK;
         const float s = norm_block_partial(sy[p * ROWS + bl * 32 + lane]);
         if (lane == 0)
             spart[p * NBLK + bl] = s;
@@ -374,8 +389,13 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
         float *hist_c = histb + (size_t)c_qk * (W - 1);
         float nh[kMaxW - 1];
         if (SNAP) {
-            conv_window_history<NTOK>(wqk, W, 1, nh);
-            store_history(a.conv_snap + ((size_t)b * cd + c_qk) * (W - 1), W, nh);
+#pragma unroll
+            for (int p = 0; p < NTOK; ++p)
+                if (per_token || p == 0) {
+                    conv_window_history<NTOK>(wqk, W, p + 1, nh);
+                    store_history(a.conv_snap + ((size_t)(b * (per_token ? NTOK : 1) + p) * cd + c_qk) * (W - 1),
+                                  W, nh);
+                }
         }
         conv_window_history<NTOK>(wqk, W, NTOK, nh);
         store_history(hist_c, W, nh);
@@ -431,11 +451,21 @@ cudaError_t launch_decode_fused_bf16_state(const FusedArgs &a, bool bf16, cudaSt
                 : fused_dispatch<float, 1, __nv_bfloat16>(a, s);
 }
 
+template <typename TIn>
+static cudaError_t fused_dispatch_ntok(const FusedArgs &a, int ntok, cudaStream_t s)
+{
+    switch (ntok) {
+    case 1: return fused_dispatch<TIn, 1>(a, s);
+    case 2: return fused_dispatch<TIn, 2>(a, s);
+    case 3: return fused_dispatch<TIn, 3>(a, s);
+    case 4: return fused_dispatch<TIn, 4>(a, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t launch_decode_fused(const FusedArgs &a, bool bf16, int ntok, cudaStream_t s)
 {
-    if (bf16)
-        return ntok == 1 ? fused_dispatch<__nv_bfloat16, 1>(a, s) : fused_dispatch<__nv_bfloat16, 2>(a, s);
-    return ntok == 1 ? fused_dispatch<float, 1>(a, s) : fused_dispatch<float, 2>(a, s);
+    return bf16 ? fused_dispatch_ntok<__nv_bfloat16>(a, ntok, s) : fused_dispatch_ntok<float>(a, ntok, s);
 }
 
 cudaError_t launch_decay_gate(const void *alpha, bool bf16, int64_t alpha_stride, const float *dt,

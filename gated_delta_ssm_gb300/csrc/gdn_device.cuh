@@ -268,7 +268,8 @@ __device__ __forceinline__ float gated_out(float y, float inv, float w, float z)
 // prologue so the HBM latency overlaps it); step_rows advances them in
 // registers; store_rows writes them back:
 //   rows       first row of this warp's block in global memory (row stride kD)
-//   snap_rows  same rows in the snapshot buffer (used when SNAP)
+//   snap_rows  same rows in the snapshot buffer (used when SNAP): the rows after
+//              token p go to snap_rows + p * snap_stride for p < n_snap
 //   sk, sq     shared [NTOK][kD] normalised k, q
 //   sv         shared [NTOK][v_stride] v, indexed by the row's local index
 //   sdecay, sbeta shared [NTOK]
@@ -325,7 +326,8 @@ __device__ __forceinline__ void step_rows(Reg (&r)[NG][4], float *snap_rows,
                                           const float *sk, const float *sq, const float *sv,
                                           int v_stride, const float *sdecay, const float *sbeta,
                                           float *sy, int local_row0, float scale,
-                                          TSt *final_rows = nullptr)
+                                          TSt *final_rows = nullptr, int n_snap = 1,
+                                          size_t snap_stride = 0)
 {
     const int lane = threadIdx.x & 31;
     const int rg = lane >> 3;
@@ -394,12 +396,12 @@ __device__ __forceinline__ void step_rows(Reg (&r)[NG][4], float *snap_rows,
             }
         }
         if constexpr (SNAP) {
-            if (p == 0) {
+            if (p < n_snap) {
 #pragma unroll
                 for (int gi = 0; gi < NG; ++gi)
 #pragma unroll
                     for (int m = 0; m < 4; ++m)
-                        st_stream(snap_rows + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4,
+                        st_stream(snap_rows + p * snap_stride + (size_t)(gi * 4 + rg) * kD + (m * 8 + sub) * 4,
                                   to_f4(r[gi][m]));
             }
         }
