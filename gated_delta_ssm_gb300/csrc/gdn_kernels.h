@@ -100,12 +100,15 @@ inline size_t prefill_workspace_bytes(int B, int Hq, int Hv, int n_chunks)
 int sm_count();
 
 // Row slices per head of the single-token decode: enough CTAs (about four per
-// SM) to keep every SM streaming state, within an 8-CTA cluster (r CTAs share a
-// QK head, ns slices per head).
+// SM) to keep every SM streaming state, without growing a cluster (r CTAs share
+// a QK head, ns slices per head) past 4 CTAs by slicing. Past that the cluster's
+// barriers and shared-memory exchanges cost more than the extra CTAs give
+// (measured: one sequence of 32 V heads in 16 QK pairs, 3.92 us per step with
+// 8-CTA clusters of 4 slices, 3.72 us with 4-CTA clusters of 2).
 inline int pick_nsplit(int B, int Hv, int r, int sms)
 {
     int ns = 1;
-    while (ns < 4 && (int64_t)B * Hv * ns < 4 * (int64_t)sms && r * ns * 2 <= 8)
+    while (ns < 4 && (int64_t)B * Hv * ns < 4 * (int64_t)sms && r * ns * 2 <= 4)
         ns *= 2;
     return ns;
 }

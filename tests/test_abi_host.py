@@ -146,11 +146,13 @@ def test_row_splits_follow_the_sm_count(lib):
                     # and split as far as that allows
                     if scan < 4 and r * scan * 2 <= 8:
                         assert B * Hv * scan * 2 > 2 * sms
-                    # the decode splits until about four CTAs per SM (or the cluster limit)
-                    if dec < 4 and r * dec * 2 <= 8:
+                    # the decode splits until about four CTAs per SM, or until a further
+                    # split would grow a cluster past 4 CTAs
+                    assert dec == 1 or r * dec <= 4
+                    if dec < 4 and r * dec * 2 <= 4:
                         assert B * Hv * dec >= 4 * sms
     # the GB300's 152 SMs: the benchmarked shapes keep their splits
-    assert gdn.testing_row_splits(1, 32, 2, 152) == (4, 4)     # one sequence, 16 / 32 heads
+    assert gdn.testing_row_splits(1, 32, 2, 152) == (2, 4)     # one sequence, 16 / 32 heads
     assert gdn.testing_row_splits(64, 48, 3, 152) == (1, 1)    # 64 sequences, 16 / 48 heads
     assert gdn.testing_row_splits(32, 32, 2, 152) == (1, 1)    # 32 sequences, 16 / 32 heads
 
