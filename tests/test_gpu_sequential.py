@@ -141,6 +141,29 @@ def test_verify_kn_equals_decode_steps_and_oracle(K, B, Hq, Hv, act):
         assert np.array_equal(csnap[:, mid].cpu().numpy(), part["hist"].astype(np.float32))
 
 
+@pytest.mark.parametrize("K,B,Hq,Hv,W,act", [(4, 1, 1, 8, 8, "f32"), (3, 2, 2, 2, 2, "bf16"),
+                                             (2, 5, 1, 4, 5, "bf16"), (4, 3, 2, 4, 3, "f32")])
+def test_verify_kn_fused_edge_shapes_equal_decode_steps(K, B, Hq, Hv, W, act):
+    # drafts of up to four positions run in the fused step kernel: conv windows of 2..8
+    # taps, eight V heads per QK head, one sequence (row slices and clusters)
+    shape = synth.Shape(B=B, T=K, Hq=Hq, Hv=Hv, W=W, act_dtype=act, warm=True)
+    inp = synth.make_inputs(shape, seed=70 + 10 * K + W)
+    dev = device_inputs(shape, inp)
+    st, hi = dev["state"].clone(), dev["hist"].clone()
+    out, ssnap, csnap = _verify(shape, dev, K)
+    ref_out, after = _steps(shape, dev, st, hi, K, snaps=True)
+    assert gdn.check_device() == 0
+    assert torch.equal(out, ref_out)
+    assert torch.equal(dev["state"], st) and torch.equal(dev["hist"], hi)
+    for p in range(K):
+        assert torch.equal(csnap[:, p], after[p][1])
+        if p < K - 1:
+            assert torch.equal(ssnap[:, p], after[p][0])
+    ref = run_oracle(shape, inp)
+    check_out(out.cpu().numpy(), ref["out"])
+    assert max_rel(dev["state"].cpu().numpy(), ref["state"], 2) <= STATE_TOL
+
+
 def test_verify_kn_at_k2_equals_verify_k2_bitwise():
     shape = synth.WORKLOADS["verify_k2"]
     inp = synth.make_inputs(shape, seed=60)
