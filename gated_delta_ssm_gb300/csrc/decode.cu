@@ -195,6 +195,18 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
         g_dt = __ldg(a.dt + h);
         g_alog = __ldg(a.A_log + h);
     }
+    // a grid of at most one wave starts while the previous kernel finishes: its CTAs
+    // bring their state rows into L2 ahead of the wait. Nothing is read into registers
+    // before the wait, and L2 is where every SM's stores land, so rows that kernel is
+    // still writing are current there when the loads below read them.
+    if (NTOK == 1 && a.n_accept == nullptr && tid < 4 &&
+        (long long)gridDim.x * gridDim.y <= 2LL * a.sm_count) {
+        const uint32_t quarter = ROWS * kD * sizeof(TS) / 4;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                     :: "l"(reinterpret_cast<const char *>(state + head_off + (size_t)row0 * kD) + tid * quarter),
+                        "r"(quarter)
+                     : "memory");
+    }
     wait_previous_grid();
 
     // (1) the conv windows' new rows, z and the gate inputs

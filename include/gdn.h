@@ -19,7 +19,9 @@
  *               parameters (gdn_params: conv weights, dt, A_log, norm
  *               weight), which that kernel must therefore not write; every
  *               other argument (activations, state, conv history, snapshots,
- *               accepted counts) is read after it, in stream order.
+ *               accepted counts) is read after it, in stream order. (A
+ *               launch of at most one wave also asks for its state rows to
+ *               be brought into L2 before then, which reads nothing.)
  *   Errors      Host-side validation runs before anything is launched. A
  *               call that returns anything but GDN_OK has enqueued nothing,
  *               except GDN_ERR_CUDA, where the launch itself failed;
