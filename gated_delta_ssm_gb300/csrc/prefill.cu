@@ -18,19 +18,22 @@
 // chunk): it stages the chunk's raw Q and K rows in shared memory by tensor
 // copy, runs the conv + SiLU + L2 on them, forms G = [Q; K] K^T on the tensor
 // core, and for each V head of the group builds P (from Q K^T) and A (from
-// K K^T) in parallel and solves T = (I + A)^-1 by blocked forward
-// substitution, writing T and P as 16 KB two-part fp16 operand images to the
+// K K^T) in parallel and solves T = (I + A)^-1 in 16-token blocks (diagonal
+// blocks by forward substitution, the blocks below them by warp-level tensor
+// core products), writing T and P as 16 KB two-part fp16 operand images to the
 // caller's workspace. Nothing in it depends on the state.
 //
 // Pass 2 (prefill_chain_kernel) walks the chunks of one (sequence, V head)
 // with the fp32 state master in tensor memory. Its warps are specialised:
 //   * 8 epilogue warps (two per TMEM lane quarter, value row j = lane):
-//     X, U, the state re-split, the state write-back and the readout rows;
-//   * 1 issuer warp: one lane issues every bulk / tensor copy and every product
-//     and waits on their completions, so no copy or product waits for an
-//     epilogue to reach it;
-//   * 8 conv warps: conv + SiLU of chunk c+1's V rows (from the staged rows)
-//     while chunk c's products run, and the gated RMSNorm of chunk c's outputs.
+//     X (with the V rows' SiLU), U' and U, the state re-split, the state
+//     write-back and the readout rows;
+//   * 1 product warp: one lane issues every product as soon as its operands are
+//     ready and its accumulator is free;
+//   * 1 copy warp: one lane refills every workspace buffer as soon as the
+//     products that read it are done;
+//   * 8 conv warps: the conv of chunk c+1's V rows (from the staged rows) while
+//     chunk c's products run, and the gated RMSNorm of chunk c's outputs.
 // The products (transposed orientation, M = 128 value rows j, A operands in
 // tensor memory, B operands in shared memory):
 //   D1 = S_0^T [Q; K]^T        ((Q S_0)^T | (K S_0)^T)
