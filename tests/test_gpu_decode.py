@@ -412,19 +412,22 @@ def test_repeat_runs_are_deterministic():
     assert all(torch.equal(a, b) for a, b in zip(res[0], res[1]))
 
 
-def test_step_reads_inputs_the_previous_step_just_wrote():
+@pytest.mark.parametrize("n_first", [64, 8])
+def test_step_reads_inputs_the_previous_step_just_wrote(n_first):
     """The decode launch is a programmatic dependent of the kernel before it in the
     stream, and the decode kernel lets its dependents start before its outputs are
-    written. A step whose x and z rows ARE the output of the step just before it must
-    still read them only once that step is done: the same bits as with a device
+    written (a launch of one wave or less as soon as its own grid wait returns, a
+    larger one once its state stores are issued: 64 sequences here give 1024 CTAs,
+    8 give 128). A step whose x and z rows ARE the output of the step just before it
+    must still read them only once that step is done: the same bits as with a device
     synchronisation between the two calls. The first step's output buffer starts as
     NaN, so a read that came too early would show."""
-    big = synth.Shape(B=64, T=1, Hq=4, Hv=8, act_dtype="f32", warm=True)
+    big = synth.Shape(B=n_first, T=1, Hq=4, Hv=8, act_dtype="f32", warm=True)
     inp1 = synth.make_inputs(big, seed=140)
     dev1 = device_inputs(big, inp1)
-    # the second step: 16 sequences whose fp32 x rows (x then z in one row) are
-    # carved out of the first step's [64][8][128] output
-    small = synth.Shape(B=16, T=1, Hq=4, Hv=8, act_dtype="f32", warm=True)
+    # the second step: a quarter as many sequences, whose fp32 x rows (x then z in
+    # one row) are carved out of the first step's [B][8][128] output
+    small = synth.Shape(B=n_first // 4, T=1, Hq=4, Hv=8, act_dtype="f32", warm=True)
     row = 2 * small.conv_dim
     assert small.B * row <= big.B * big.Hv * big.d
     inp2 = synth.make_inputs(small, seed=141)
@@ -450,4 +453,30 @@ def test_step_reads_inputs_the_previous_step_just_wrote():
     assert gdn.check_device() == 0
     assert torch.isfinite(results[1][0]).all()
     for a, b in zip(results[0], results[1]):
+        assert torch.equal(a, b)
+
+
+def test_back_to_back_steps_on_one_state_equal_synchronised_steps():
+    """Single-sequence steps (one wave: each launch prefetches its state rows into L2
+    and makes the next launch resident before its own work) stepping the SAME state
+    and conv history 24 times in a row give the bits of the same steps with a device
+    synchronisation after each."""
+    shape = synth.WORKLOADS["decode_b1"]
+    inp = synth.make_inputs(shape, seed=142)
+    dev = device_inputs(shape, inp)
+    res = []
+    for sync in (False, True):
+        st, hi = dev["state"].clone(), dev["hist"].clone()
+        outs = torch.full((24, shape.B, shape.Hv, shape.d), float("nan"), device="cuda")
+        torch.cuda.synchronize()
+        for i in range(24):
+            gdn.decode_step(st, hi, dev["x"][:, 0], dev["z"][:, 0], dev["alpha"][:, 0],
+                            dev["beta_logit"][:, 0], params_of(dev), outs[i], dims_of(shape))
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        res.append((outs, st, hi))
+    assert gdn.check_device() == 0
+    assert torch.isfinite(res[1][0]).all()
+    for a, b in zip(res[0], res[1]):
         assert torch.equal(a, b)
