@@ -670,7 +670,7 @@ def main(argv=None):
         extra["verify_k2"] = gpu.verify_k2(max(5, args.steps // 2), args.warmup)
         extra["verify_kn"] = gpu.verify_kn(max(5, args.steps // 2), args.warmup)
         extra["conv_tokens"] = gpu.conv_tokens(max(5, args.steps // 2), args.warmup)
-        extra["prefill"] = gpu.prefill(max(3, args.steps // 5), 3)
+        extra["prefill"] = gpu.prefill(max(10, args.steps // 2), 3)
     if rank != 0:
         if dist is not None:
             dist.barrier()
