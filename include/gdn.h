@@ -422,8 +422,9 @@ gdn_status gdn_prefill_chunked_noalloc(float *state, float *conv_state, const vo
                                        gdn_stream_t stream);
 
 /*
- * Every wait inside a kernel on a bulk copy, a tensor-core operation or
- * another warp group of the same CTA is bounded by the GPU's global timer
+ * Every wait inside a kernel on a bulk copy, a tensor-core operation,
+ * another warp group of the same CTA or data pushed by another CTA of the
+ * same cluster is bounded by the GPU's global timer
  * (2 s); a kernel whose wait gives up sets a bit in a device-side error word,
  * stops its remaining work, waits (bounded again) for the copies and products
  * it already issued, frees its tensor memory and returns instead of hanging:
@@ -435,6 +436,9 @@ gdn_status gdn_prefill_chunked_noalloc(float *state, float *conv_state, const vo
  *   bit 32  (checked build only, libgdn_checked.so) a kernel's index
  *           arithmetic left the range its arguments allow
  *   bit 64  the multi-token conv gave up its tile-copy wait
+ *   bit 128 a row slice of a fused decode / verify step gave up waiting for
+ *           the gated-norm partial sums of the head's other row slices (that
+ *           head's outputs are not valid)
  * The one wait not bounded by the library is the hardware's tensor-memory
  * allocation at the start of the prefill kernels, which lasts until CTAs of
  * other launches on the same SM release their columns. This call waits for
