@@ -235,8 +235,27 @@ class Gpu:
         return self.gdn.Params(d["conv_w"], d["dt"], d["A_log"], d["norm_w"], 1e-6, 1e-6)
 
     def time_steps(self, fn, steps, warmup):
-        """Per-step device time (s) with CUDA events on the launching stream; the
-        callable receives the step index (used to rotate buffers)."""
+        """Device time (s) of `steps` calls issued back to back after `warmup` untimed
+        ones: one pair of CUDA events on the launching stream around all of them, so
+        consecutive launches overlap as they do in a serving loop (each decode launch is a
+        programmatic dependent of the one before it). Returns the mean per call, once per
+        call. The callable receives the step index (used to rotate buffers)."""
+        torch = self.torch
+        for i in range(warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(self.stream)
+        for i in range(steps):
+            fn(warmup + i)
+        b.record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) * 1e-3 / steps] * steps
+
+    def time_each(self, fn, steps, warmup):
+        """Per-call device times (s), an event pair around each call. The event recorded
+        between two launches keeps the second from starting before the first ends, so
+        this is the serialised time of one launch."""
         torch = self.torch
         for i in range(warmup):
             fn(i)
@@ -271,6 +290,8 @@ class Gpu:
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
+        self.launches += steps
+        self.per_launch_s = statistics.mean(self.time_each(step, steps, warmup))
         self.launches += steps
         # end to end through the C ABI: inputs from pinned host memory each step, output back
         hx = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -690,7 +711,11 @@ def main(argv=None):
                                "state, conv_dim 10240, d_conv 4, bf16 activations, qkvz row stride "
                                "20480, one fused launch per step",
                    "global_batch": 64 * world, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2: 3 rotating state sets of 192 MiB"},
+                   "l2": "inputs larger than L2: 3 rotating state sets of 192 MiB",
+                   "timing": "one pair of CUDA events on the launching stream around the K "
+                             "back-to-back steps (each launch a programmatic dependent of the one "
+                             "before, as in a serving loop)"},
+        "ms_per_launch_serialized": gpu.per_launch_s * 1e3,
         "pct_of_peak": 100.0 * value / world / hbm_peak,
         "pct_of_nominal": 100.0 * value / world / NOMINAL_HBM_GBS,
         "seqs_per_s": shape.B * world / mean,
