@@ -313,48 +313,73 @@ class Gpu:
 
         # The serving loop: every step's inputs still come from pinned host memory and
         # its output still goes back to pinned host memory, but the copies run on a
-        # second stream, double-buffered, so step i+1's inputs arrive while step i runs.
-        # A step's three inputs travel as one copy: x rows, then the alpha rows, then the
-        # beta-logit rows, back to back in one pinned host buffer and one device buffer per
-        # slot; the step reads views of it.
+        # second stream while the kernels run. Steps go in groups (of G, except one step
+        # in the first and the last): the inputs of group g+1 (its steps' inputs, back
+        # to back in pinned host memory) travel in one copy while group g runs, and the
+        # outputs of a group come back in one copy.
+        # The kernels of a group follow one another with nothing between them in the
+        # stream, so each is a programmatic dependent of the one before, as in the
+        # kernel-only loop, and the host issues one call per step. A step's three
+        # inputs are its x rows, then its alpha rows, then its beta-logit rows; the step
+        # reads views of its slot. Two sets of slots alternate.
+        G = 4
         cd = shape.conv_dim
         copy = torch.cuda.Stream(device=self.dev)
         comp = self.stream
         nx, na = hx.numel(), ha.numel()
-        hpk = torch.cat([hx.reshape(-1), ha.reshape(-1), hb.reshape(-1)]).pin_memory()
+        one = torch.cat([hx.reshape(-1), ha.reshape(-1), hb.reshape(-1)])
+        per = one.numel()
+        hpk = one.repeat(G).pin_memory()                         # G steps' inputs
         dpk = [torch.empty_like(hpk, device=self.dev) for _ in range(2)]
-        dx = [t[:nx].view(d["x"].shape) for t in dpk]
-        da = [t[nx:nx + na].view(d["alpha"].shape) for t in dpk]
-        db = [t[nx + na:].view(d["beta_logit"].shape) for t in dpk]
-        dz = [t[..., cd:cd + shape.Hv * shape.d] for t in dx]
-        outs = [out, torch.empty_like(out)]
-        houts = [hout, torch.empty(out.shape, dtype=out.dtype).pin_memory()]
-        ev_in = [torch.cuda.Event(), torch.cuda.Event()]
-        ev_k = [torch.cuda.Event(), torch.cuda.Event()]
-        assert hpk.numel() * hpk.element_size() == h2d
-
-        def h2d_into(j):
-            dpk[j].copy_(hpk, non_blocking=True)
+        slot = [[dpk[sset][u * per:(u + 1) * per] for u in range(G)] for sset in range(2)]
+        dx = [[t[:nx].view(d["x"].shape) for t in slot[sset]] for sset in range(2)]
+        da = [[t[nx:nx + na].view(d["alpha"].shape) for t in slot[sset]] for sset in range(2)]
+        db = [[t[nx + na:].view(d["beta_logit"].shape) for t in slot[sset]] for sset in range(2)]
+        dz = [[t[..., cd:cd + shape.Hv * shape.d] for t in dx[sset]] for sset in range(2)]
+        outs = [torch.empty((G,) + tuple(out.shape), dtype=out.dtype, device=self.dev) for _ in range(2)]
+        houts = [torch.empty((G,) + tuple(out.shape), dtype=out.dtype).pin_memory() for _ in range(2)]
+        ev_in = [torch.cuda.Event(), torch.cuda.Event()]     # a slot set's inputs are in
+        ev_k = [torch.cuda.Event(), torch.cuda.Event()]      # its kernels are done
+        ev_out = [torch.cuda.Event(), torch.cuda.Event()]    # its outputs are back on the host
+        assert per * one.element_size() == h2d
 
         def pipelined(n_steps, first):
-            with torch.cuda.stream(copy):
-                h2d_into(0)
-                ev_in[0].record(copy)
-            for i in range(n_steps):
-                j = i % 2
-                if i + 1 < n_steps:
-                    with torch.cuda.stream(copy):
-                        if i >= 1:
-                            copy.wait_event(ev_k[1 - j])   # step i-1 has read that buffer
-                        h2d_into(1 - j)
-                        ev_in[1 - j].record(copy)
-                comp.wait_event(ev_in[j])
-                gdn.decode_step(d["states"][(first + i) % nbuf], d["hists"][(first + i) % nbuf],
-                                dx[j], dz[j], da[j], db[j], prm, outs[j], dims, stream=comp)
-                ev_k[j].record(comp)
+            # one step in the first and in the last group: the first group's input copy
+            # and the last group's output copy are the ones nothing overlaps
+            if n_steps <= 2:
+                size = [1] * n_steps
+            else:
+                mid = n_steps - 2
+                size = [1] + [G] * (mid // G) + ([mid % G] if mid % G else []) + [1]
+            n_groups = len(size)
+            start = [sum(size[:g]) for g in range(n_groups)]
+
+            def h2d_group(g):
+                sset = g % 2
                 with torch.cuda.stream(copy):
-                    copy.wait_event(ev_k[j])
-                    houts[j].copy_(outs[j], non_blocking=True)
+                    if g >= 2:
+                        copy.wait_event(ev_k[sset])          # group g-2 has read these slots
+                    dpk[sset][:size[g] * per].copy_(hpk[:size[g] * per], non_blocking=True)
+                    ev_in[sset].record(copy)
+
+            h2d_group(0)
+            for g in range(n_groups):
+                sset = g % 2
+                if g + 1 < n_groups:
+                    h2d_group(g + 1)
+                comp.wait_event(ev_in[sset])
+                if g >= 2:
+                    comp.wait_event(ev_out[sset])            # group g-2's outputs have left
+                xs, zs, als, bls, os_ = dx[sset], dz[sset], da[sset], db[sset], outs[sset]
+                for u in range(size[g]):
+                    i = start[g] + u
+                    gdn.decode_step(d["states"][(first + i) % nbuf], d["hists"][(first + i) % nbuf],
+                                    xs[u], zs[u], als[u], bls[u], prm, os_[u], dims, stream=comp)
+                ev_k[sset].record(comp)
+                with torch.cuda.stream(copy):
+                    copy.wait_event(ev_k[sset])
+                    houts[sset][:size[g]].copy_(outs[sset][:size[g]], non_blocking=True)
+                    ev_out[sset].record(copy)
 
         pipelined(max(3, warmup), 0)
         torch.cuda.synchronize()
