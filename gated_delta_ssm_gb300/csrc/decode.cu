@@ -1,7 +1,8 @@
 // decode.cu -- decode-side kernels of libgdn: the fused one-launch layer step
-// (single token, and the K=2 verify form with its rollback snapshot), the
-// standalone gate / conv / recurrence / gated-norm kernels it is equal to bit
-// for bit, and the verify commit.
+// (single token; the K=2 verify form with its rollback snapshot; the K = 2..4
+// verify with a snapshot per position; the step that reads the snapshot an
+// accepted count selects), the standalone gate / conv / recurrence / gated-norm
+// kernels it is equal to bit for bit, and the verify commit.
 //
 // Decode is bound by HBM bandwidth on the recurrent state (128x128 fp32 per
 // V head, read once and written once per step); everything else is small.
