@@ -243,10 +243,6 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
         g_dt = __ldg(a.dt + h);
         g_alog = __ldg(a.A_log + h);
     }
-    // a grid of at most one wave starts while the previous kernel finishes: its CTAs
-    // bring their state rows into L2 ahead of the wait. Nothing is read into registers
-    // before the wait, and L2 is where every SM's stores land, so rows that kernel is
-    // still writing are current there when the loads below read them.
     // the slices of a head push their norm partials to one another: each CTA's barrier
     // completes when the other slices' bytes have landed (initialised before the cluster
     // barrier that every CTA passes before it sends)
@@ -257,6 +253,10 @@ __global__ void __launch_bounds__(256, sizeof(TS) == 4 ? 2 : 3) decode_fused_ker
                      :: "r"(bar), "r"((uint32_t)((NSPLIT - 1) * NTOK * NBLK * 4)) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    // a grid of at most one wave starts while the previous kernel finishes: its CTAs
+    // bring their state rows into L2 ahead of the wait. Nothing is read into registers
+    // before the wait, and L2 is where every SM's stores land, so rows that kernel is
+    // still writing are current there when the loads below read them.
     const bool one_wave = (long long)gridDim.x * gridDim.y <= 2LL * a.sm_count;
     if (NTOK == 1 && a.n_accept == nullptr && tid < 4 && one_wave) {
         const uint32_t quarter = ROWS * kD * sizeof(TS) / 4;
