@@ -167,6 +167,16 @@ def recorded_traffic(kernel: str):
     return d.get("bytes_per_launch")
 
 
+def e2e_group_sizes(n_steps: int, group: int) -> list:
+    """Steps per group of the end-to-end loop: groups of `group` steps, except one step
+    in the first and in the last group (the first group's input copy and the last
+    group's output copy are the ones that nothing overlaps)."""
+    if n_steps <= 2:
+        return [1] * n_steps
+    mid = n_steps - 2
+    return [1] + [group] * (mid // group) + ([mid % group] if mid % group else []) + [1]
+
+
 def decode_bytes(shape: synth.Shape) -> dict:
     """Algorithmic HBM bytes of one fused decode step (each compulsory byte counted once)."""
     B, Hv, Hq, d, W, cd = shape.B, shape.Hv, shape.Hq, shape.d, shape.W, shape.conv_dim
@@ -344,13 +354,7 @@ class Gpu:
         assert per * one.element_size() == h2d
 
         def pipelined(n_steps, first):
-            # one step in the first and in the last group: the first group's input copy
-            # and the last group's output copy are the ones nothing overlaps
-            if n_steps <= 2:
-                size = [1] * n_steps
-            else:
-                mid = n_steps - 2
-                size = [1] + [G] * (mid // G) + ([mid % G] if mid % G else []) + [1]
+            size = e2e_group_sizes(n_steps, G)
             n_groups = len(size)
             start = [sum(size[:g]) for g in range(n_groups)]
 
