@@ -25,7 +25,7 @@
 //
 // Pass 2 (prefill_chain_kernel) walks the chunks of one (sequence, V head)
 // with the fp32 state master in tensor memory. Its warps are specialised:
-//   * 8 epilogue warps (two per TMEM lane quarter, value row j = lane):
+//   * 16 epilogue warps (four per TMEM lane quarter, value row j = lane, 16 tokens each):
 //     X (with the V rows' SiLU), U' and U, the state re-split, the state
 //     write-back and the readout rows;
 //   * 1 product warp: one lane issues every product as soon as its operands are
@@ -839,10 +839,18 @@ __global__ void __launch_bounds__(p1::kThreads, 2) prefill_ut_kernel(const __gri
 
 // ================================================================== pass 2
 namespace p2 {
-// warps 0-7: epilogue (two per TMEM lane quarter); warp 8: the products; warp 9: the
-// workspace copies; warps 10-17: the V conv and the gated norm (8 tokens each). 18 warps
-// of at most 112 registers fit the SM's 65536 registers with one CTA per SM.
-constexpr int kIssuerWarp = 8, kCopyWarp = 9, kConvWarp0 = 10, kConvWarps = 8;
+// warps 0-15: epilogue (four per TMEM lane quarter); warp 16: the products; warp 17: the
+// workspace copies; warps 18-25: the V conv and the gated norm (8 tokens each). 26 warps
+// of at most 72 registers fit the SM's 65536 registers with one CTA per SM. Each epilogue
+// warp handles kEpiTok tokens of the chunk and kEpiCols columns of the state master for its
+// 32 value rows. (Two epilogue warps per quarter, 32 tokens and 64 columns each, measured
+// 1.280 against 1.257-1.275 ms for the 4 x 8192 prefill on one box, 1.358 against
+// 1.281-1.290 ms on another; four conv warps with the sixteen took 2.31 ms.)
+constexpr int kEpiWarps = 16, kEpiQ = kEpiWarps / 4;
+constexpr int kEpiTok = kC / kEpiQ, kEpiCols = kD / kEpiQ;
+static_assert(kEpiWarps == 8 || kEpiWarps == 16, "two or four epilogue warps per lane quarter");
+constexpr int kIssuerWarp = kEpiWarps, kCopyWarp = kEpiWarps + 1, kConvWarp0 = kEpiWarps + 2;
+constexpr int kConvWarps = 8;
 constexpr int kConvThreads = 32 * kConvWarps, kConvTok = kC / kConvWarps;
 constexpr int kThreads = 32 * (kConvWarp0 + kConvWarps);
 constexpr uint32_t QB = 0;                        // Q rows of the chunk: two parts, [64 t][128 i] sw128
@@ -939,7 +947,7 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
 
     if (tid == 0) {
         for (int i = 0; i < B_N; ++i)
-            tc::mbar_init(bar(i), i < B_RAWFREE ? 1 : i < B_ST ? kConvThreads : 256);
+            tc::mbar_init(bar(i), i < B_RAWFREE ? 1 : i < B_ST ? kConvThreads : 32 * kEpiWarps);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1352,17 +1360,17 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
         const int q4 = warp & 3, hf = warp >> 2;
         const int j = 32 * q4 + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-        float *state_row = a.state + (((size_t)b * a.Hv + h) * kD + j) * kD + 64 * hf;
+        float *state_row = a.state + (((size_t)b * a.Hv + h) * kD + j) * kD + kEpiCols * hf;
         // the S_0^T operand (R1, two parts) from the fp32 master (TS)
         auto state_operand = [&]() {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < kEpiCols / 16; ++k) {
                 float sv[16];
-                tc::tmem_ld16(tl + TS + 64 * hf + 16 * k, sv);
+                tc::tmem_ld16(tl + TS + kEpiCols * hf + 16 * k, sv);
                 uint32_t hi[8], lo[8];
                 pack_split16(sv, hi, lo);
-                tmem_st8u(tl + R1 + 32 * hf + 8 * k, hi);
-                tmem_st8u(tl + R1 + 64 + 32 * hf + 8 * k, lo);
+                tmem_st8u(tl + R1 + kEpiCols / 2 * hf + 8 * k, hi);
+                tmem_st8u(tl + R1 + 64 + kEpiCols / 2 * hf + 8 * k, lo);
             }
             tc::tmem_wait_st();
             tc::fence_before_sync();
@@ -1370,14 +1378,14 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
         };
         // prologue: entering state -> fp32 master (TS) and the S_0^T operand (R1)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kEpiCols / 16; ++k) {
             float v16[16];
 #pragma unroll
             for (int e = 0; e < 16; e += 4) {
                 const float4 f = __ldg(reinterpret_cast<const float4 *>(state_row + 16 * k + e));
                 v16[e] = f.x; v16[e + 1] = f.y; v16[e + 2] = f.z; v16[e + 3] = f.w;
             }
-            tc::tmem_st16(tl + TS + 64 * hf + 16 * k, v16);
+            tc::tmem_st16(tl + TS + kEpiCols * hf + 16 * k, v16);
         }
         state_operand();
         bool ok = true;
@@ -1395,8 +1403,8 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             // ---- X^T[j][t] = beta_t V[t][j] - beta_t e^{Gam_t} (K S_0)[t][j]; the state master
             //      scaled by e^{Gam_C} ahead of this chunk's update
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int tb0 = 32 * hf + 16 * p;
+            for (int p = 0; p < kEpiTok / 16; ++p) {
+                const int tb0 = kEpiTok * hf + 16 * p;
                 float ks[16];
                 tc::tmem_ld16(tl + D1 + kC + tb0, ks);
                 float x[16];
@@ -1423,13 +1431,13 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             {
                 const float ec = __fmul_rn(G->ec, exp2i(rho_next - rho));
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < kEpiCols / 16; ++k) {
                     float sv[16];
-                    tc::tmem_ld16(tl + TS + 64 * hf + 16 * k, sv);
+                    tc::tmem_ld16(tl + TS + kEpiCols * hf + 16 * k, sv);
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         sv[e] = __fmul_rn(sv[e], ec);
-                    tc::tmem_st16(tl + TS + 64 * hf + 16 * k, sv);
+                    tc::tmem_st16(tl + TS + kEpiCols * hf + 16 * k, sv);
                 }
             }
             // ---- U = T X (from D2): first U'^T = U^T diag(e^{Gam_C - Gam}) for the state
@@ -1439,8 +1447,8 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 break;
             tc::fence_after_sync();
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int tb0 = 32 * hf + 16 * p;
+            for (int p = 0; p < kEpiTok / 16; ++p) {
+                const int tb0 = kEpiTok * hf + 16 * p;
                 float u[16];
                 tc::tmem_ld16(tl + D2 + tb0, u);
 #pragma unroll
@@ -1460,8 +1468,8 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             tc::fence_before_sync();
             tc::mbar_arrive(bar(B_U));
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int tb0 = 32 * hf + 16 * p;
+            for (int p = 0; p < kEpiTok / 16; ++p) {
+                const int tb0 = kEpiTok * hf + 16 * p;
                 float u[16];
                 tc::tmem_ld16(tl + D2 + tb0, u);
                 uint32_t hi[8], lo[8];
@@ -1482,9 +1490,9 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
                 // ---- final state back to HBM (S^T rows = the library layout), unscaled
                 const float us = exp2i(-rho_next);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < kEpiCols / 16; ++k) {
                     float sv[16];
-                    tc::tmem_ld16(tl + TS + 64 * hf + 16 * k, sv);
+                    tc::tmem_ld16(tl + TS + kEpiCols * hf + 16 * k, sv);
 #pragma unroll
                     for (int e = 0; e < 16; e += 4)
                         *reinterpret_cast<float4 *>(state_row + 16 * k + e) =
@@ -1499,10 +1507,10 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             if (!(ok = waitb(B_PU, par, lim)))
                 break;
             tc::fence_after_sync();
-            float o[32];
+            float o[kEpiTok];
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int tb0 = 32 * hf + 16 * p;
+            for (int p = 0; p < kEpiTok / 16; ++p) {
+                const int tb0 = kEpiTok * hf + 16 * p;
                 float qs[16], pu[16];
                 tc::tmem_ld16(tl + D1 + tb0, qs);
                 tc::tmem_ld16(tl + D2 + tb0, pu);
@@ -1523,10 +1531,10 @@ __global__ void __launch_bounds__(p2::kThreads, 1) prefill_chain_kernel(const __
             if (c > 0 && !(ok = waitb(B_OSFREE, (c - 1) & 1, lim)))
                 break;
 #pragma unroll
-            for (int p = 0; p < 2; ++p)
+            for (int p = 0; p < kEpiTok / 16; ++p)
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
-                    Os[(32 * hf + 16 * p + k) * kD + j] = o[16 * p + k];
+                    Os[(kEpiTok * hf + 16 * p + k) * kD + j] = o[16 * p + k];
             tc::mbar_arrive(bar(B_OS));
             rho = rho_next;
         }
