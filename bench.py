@@ -678,7 +678,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-extra", action="store_true", help="headline workload only")
     ap.add_argument("--only", choices=["decode_b1", "decode_b64_bf16_state", "verify_k2",
-                                       "verify_kn", "conv_tokens", "prefill"],
+                                       "verify_kn", "verify_kn8", "conv_tokens", "prefill"],
                     help="run one secondary workload alone and print its figures (for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-tokens", type=int, default=None,
@@ -694,6 +694,7 @@ def main(argv=None):
         gpu = Gpu(local)
         fn = {"decode_b1": lambda: gpu.decode_b1(), "verify_k2": lambda: gpu.verify_k2(args.steps, args.warmup),
               "verify_kn": lambda: gpu.verify_kn(args.steps, args.warmup),
+              "verify_kn8": lambda: gpu.verify_kn(args.steps, args.warmup, K=8),
               "decode_b64_bf16_state": lambda: gpu.decode_b64_bf16_state(args.steps, args.warmup),
               "conv_tokens": lambda: gpu.conv_tokens(args.steps, args.warmup),
               "prefill": lambda: gpu.prefill(args.steps, args.warmup, args.prefill_tokens)}[args.only]
@@ -719,6 +720,8 @@ def main(argv=None):
         extra["decode_b64_bf16_state"] = gpu.decode_b64_bf16_state(args.steps, args.warmup)
         extra["verify_k2"] = gpu.verify_k2(max(5, args.steps // 2), args.warmup)
         extra["verify_kn"] = gpu.verify_kn(max(5, args.steps // 2), args.warmup)
+        # K = 8: past the fused forms, the token-serial scan with snapshots
+        extra["verify_kn8"] = gpu.verify_kn(max(5, args.steps // 4), args.warmup, K=8)
         extra["conv_tokens"] = gpu.conv_tokens(max(5, args.steps // 2), args.warmup)
         extra["prefill"] = gpu.prefill(max(10, args.steps // 2), 3)
     if rank != 0:

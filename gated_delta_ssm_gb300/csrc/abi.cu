@@ -420,10 +420,10 @@ gdn_status gdn_verify_kn(float *state, float *conv_state, float *state_snap, flo
     if (!conv_snap || (n_draft > 1 && !state_snap) || state_snap == state ||
         conv_snap == conv_state)
         return GDN_ERR_INVALID_ARG;
-    // up to four positions: the fused step kernel over all positions at once (state rows
+    // up to eight positions: the fused step kernel over all positions at once (state rows
     // held in registers, one snapshot entry per position); longer drafts: the layer scan.
     // Both give the bits of n_draft single steps.
-    if (n_draft >= 2 && n_draft <= 4)
+    if (n_draft >= 2 && n_draft <= 8)
         return fused_common(state, conv_state, state_snap, conv_snap, x, z, alpha, beta_logit,
                             act_dtype, params, out, dims, n_draft, false, stream, nullptr, 0, n_draft);
     return layer_scan_common(state, conv_state, state_snap, conv_snap, x, z, alpha, beta_logit,

@@ -1,5 +1,5 @@
 // decode.cu -- decode-side kernels of libgdn: the fused one-launch layer step
-// (single token; the K=2 verify form with its rollback snapshot; the K = 2..4
+// (single token; the K=2 verify form with its rollback snapshot; the K = 2..8
 // verify with a snapshot per position; the step that reads the snapshot an
 // accepted count selects), the standalone gate / conv / recurrence / gated-norm
 // kernels it is equal to bit for bit, and the verify commit.
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(256) gated_norm_kernel(const float *y, const f
 
 // ------------------------------------------------------------------ fused step
 // NTOK = 1: one decode step. NTOK = 2: K=2 verify, snapshot after token 0, or
-// (with the per-token snapshot layout) the generic K-token verify for K = 2..4.
+// (with the per-token snapshot layout) the generic K-token verify for K = 2..8.
 //
 // Order of a CTA's work, chosen so that no fence ever waits on the state
 // loads or stores: (0) wait for the previous kernel in the stream (the launch
@@ -559,6 +559,10 @@ static cudaError_t fused_dispatch_ntok(const FusedArgs &a, int ntok, cudaStream_
     case 2: return fused_dispatch<TIn, 2>(a, s);
     case 3: return fused_dispatch<TIn, 3>(a, s);
     case 4: return fused_dispatch<TIn, 4>(a, s);
+    case 5: return fused_dispatch<TIn, 5>(a, s);
+    case 6: return fused_dispatch<TIn, 6>(a, s);
+    case 7: return fused_dispatch<TIn, 7>(a, s);
+    case 8: return fused_dispatch<TIn, 8>(a, s);
     default: return cudaErrorInvalidValue;
     }
 }

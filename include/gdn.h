@@ -12,7 +12,7 @@
  *               gdn_prefill_chunked_noalloc may be captured into CUDA
  *               graphs. gdn_decode_step, gdn_decode_step_bf16_state,
  *               gdn_decode_step_select, gdn_verify_k2 and gdn_verify_kn
- *               with n_draft 2..4 launch as
+ *               with n_draft 2..8 launch as
  *               programmatic dependents of the previous kernel in the
  *               stream: their blocks may become resident while that kernel
  *               finishes. Before it has completed they read only the layer
@@ -324,7 +324,7 @@ gdn_status gdn_layer_scan(float *state, float *conv_state, const void *x, const 
  *              position p; entry K-1 duplicates the committed conv_state
  *   out float [B][K][Hv][d]; inputs are [B][K] token rows (row b*K + p).
  * The snapshot arrays may not overlap state, conv_state or each other.
- * For K = 2..4 the positions run in the fused step kernel (each state row
+ * For K = 2..8 the positions run in the fused step kernel (each state row
  * read once and held in registers across the positions); longer drafts run
  * in the layer scan of gdn_layer_scan. Both give the same bits.
  * Errors: INVALID_ARG (null, n_draft < 1, bad dims), UNSUPPORTED (d, W, r).

@@ -142,10 +142,13 @@ def test_verify_kn_equals_decode_steps_and_oracle(K, B, Hq, Hv, act):
 
 
 @pytest.mark.parametrize("K,B,Hq,Hv,W,act", [(4, 1, 1, 8, 8, "f32"), (3, 2, 2, 2, 2, "bf16"),
-                                             (2, 5, 1, 4, 5, "bf16"), (4, 3, 2, 4, 3, "f32")])
+                                             (2, 5, 1, 4, 5, "bf16"), (4, 3, 2, 4, 3, "f32"),
+                                             (8, 1, 1, 8, 8, "f32"), (6, 2, 2, 2, 2, "bf16"),
+                                             (5, 3, 2, 4, 3, "f32"), (7, 40, 2, 8, 4, "bf16")])
 def test_verify_kn_fused_edge_shapes_equal_decode_steps(K, B, Hq, Hv, W, act):
-    # drafts of up to four positions run in the fused step kernel: conv windows of 2..8
-    # taps, eight V heads per QK head, one sequence (row slices and clusters)
+    # drafts of up to eight positions run in the fused step kernel: conv windows of 2..8
+    # taps, eight V heads per QK head, one sequence (row slices and clusters), and a
+    # batch of whole heads (K = 7, 40 sequences)
     shape = synth.Shape(B=B, T=K, Hq=Hq, Hv=Hv, W=W, act_dtype=act, warm=True)
     inp = synth.make_inputs(shape, seed=70 + 10 * K + W)
     dev = device_inputs(shape, inp)
